@@ -1,0 +1,116 @@
+"""Float64 CPU oracle for paged grouped-query decode attention.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product package imports this module;
+only the tests, the smoke check and the benchmark's CPU-baseline leg do.  It
+shares no code with the CUDA library.
+
+``decode_f64`` wraps the C oracle (oracle.c) through ctypes.  Inputs are numpy
+arrays in their stored type: float32, or bfloat16 held as uint16 bit patterns;
+the C code widens them exactly to double.  ``brute`` is an independent dense
+numpy formulation used only to pin the C oracle on tiny inputs.
+"""
+import ctypes
+
+import numpy as np
+
+from . import build as _build
+
+F32 = 0
+BF16 = 1
+STATUS = {0: "ok", 1: "bad arguments", 2: "block id out of range", 3: "sequence length out of range"}
+
+
+def _prep(q, k_pool, v_pool, block_table, seq_lens):
+    q = np.ascontiguousarray(q)
+    k_pool = np.ascontiguousarray(k_pool)
+    v_pool = np.ascontiguousarray(v_pool)
+    if q.dtype == np.float32:
+        dtype = F32
+    elif q.dtype == np.uint16:
+        dtype = BF16
+    else:
+        raise TypeError("q must be float32 or uint16 (bfloat16 bits), got %s" % q.dtype)
+    if k_pool.dtype != q.dtype or v_pool.dtype != q.dtype:
+        raise TypeError("q, k_pool and v_pool must share one dtype")
+    if q.ndim != 3 or k_pool.ndim != 4 or k_pool.shape != v_pool.shape:
+        raise ValueError("q must be [B,Hq,D]; pools [num_blocks,block_size,Hkv,D]")
+    block_table = np.ascontiguousarray(block_table, dtype=np.int32)
+    seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, Hq, D = q.shape
+    num_blocks, block_size, Hkv, D2 = k_pool.shape
+    if D2 != D:
+        raise ValueError("head_dim mismatch")
+    if block_table.ndim != 2 or block_table.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("block_table must be [B,max_blocks], seq_lens [B]")
+    dims = (B, Hq, Hkv, D, block_size, num_blocks, block_table.shape[1])
+    return q, k_pool, v_pool, block_table, seq_lens, dtype, dims
+
+
+class Oracle:
+    """ctypes view of one compiled oracle library."""
+
+    def __init__(self, path):
+        lib = ctypes.CDLL(path)
+        argt = ([ctypes.c_void_p] * 5 + [ctypes.c_int] * 6 + [ctypes.c_int64, ctypes.c_int,
+                                                              ctypes.c_double])
+        lib.oracle_decode_f64.argtypes = argt + [ctypes.c_void_p]
+        lib.oracle_decode_f64.restype = ctypes.c_int
+        lib.oracle_decode_rows_f64.argtypes = argt + [ctypes.c_void_p, ctypes.c_int64,
+                                                      ctypes.c_void_p]
+        lib.oracle_decode_rows_f64.restype = ctypes.c_int
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = ctypes.c_int
+        self.lib = lib
+        self.path = path
+
+    def num_threads(self):
+        return int(self.lib.oracle_num_threads())
+
+    def decode_f64(self, q, k_pool, v_pool, block_table, seq_lens, scale):
+        """All rows.  Returns (out[B,Hq,D] float64, status)."""
+        q, k_pool, v_pool, bt, sl, dtype, dims = _prep(q, k_pool, v_pool, block_table, seq_lens)
+        B, Hq, Hkv, D, bs, nb, mb = dims
+        out = np.empty((B, Hq, D), dtype=np.float64)
+        rc = self.lib.oracle_decode_f64(q.ctypes.data, k_pool.ctypes.data, v_pool.ctypes.data,
+                                        bt.ctypes.data, sl.ctypes.data, dtype, B, Hq, Hkv, D,
+                                        bs, nb, mb, float(scale), out.ctypes.data)
+        if rc == 1:
+            raise ValueError("oracle rejected the arguments")
+        return out, int(rc)
+
+    def decode_rows_f64(self, q, k_pool, v_pool, block_table, seq_lens, scale, rows):
+        """Selected (b, h) rows; rows is [n, 2].  Returns (out[n, D] float64, status)."""
+        q, k_pool, v_pool, bt, sl, dtype, dims = _prep(q, k_pool, v_pool, block_table, seq_lens)
+        B, Hq, Hkv, D, bs, nb, mb = dims
+        rows = np.ascontiguousarray(rows, dtype=np.int32).reshape(-1, 2)
+        out = np.empty((rows.shape[0], D), dtype=np.float64)
+        rc = self.lib.oracle_decode_rows_f64(q.ctypes.data, k_pool.ctypes.data,
+                                             v_pool.ctypes.data, bt.ctypes.data, sl.ctypes.data,
+                                             dtype, B, Hq, Hkv, D, bs, nb, mb, float(scale),
+                                             rows.ctypes.data, rows.shape[0], out.ctypes.data)
+        if rc == 1:
+            raise ValueError("oracle rejected the arguments")
+        return out, int(rc)
+
+
+_default = None
+
+
+def default():
+    """The oracle built from oracle.c beside this file (built on first use)."""
+    global _default
+    if _default is None:
+        _default = Oracle(_build.build())
+    return _default
+
+
+def num_threads():
+    return default().num_threads()
+
+
+def decode_f64(q, k_pool, v_pool, block_table, seq_lens, scale):
+    return default().decode_f64(q, k_pool, v_pool, block_table, seq_lens, scale)
+
+
+def decode_rows_f64(q, k_pool, v_pool, block_table, seq_lens, scale, rows):
+    return default().decode_rows_f64(q, k_pool, v_pool, block_table, seq_lens, scale, rows)

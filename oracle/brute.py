@@ -1,0 +1,50 @@
+"""Dense numpy brute force for tiny inputs; pins the C oracle.
+
+TEST INFRASTRUCTURE ONLY.  A second, independent formulation of the same
+textbook result: materialise every sequence's logical K and V with fancy
+indexing, repeat each KV head over its query-head group, and evaluate
+softmax(q K^T * scale) V as dense matrix products (Attention(Q,K,V) equation in
+"Modern LLM Inference - Workloads, Bottlenecks, and Optimization Techniques",
+section "Why Cross-Layer Attention Shares K/V but Not Q"; group sharing per its
+section 4.1).  Sizes are meant to be tiny (L <= a few hundred).
+"""
+import numpy as np
+
+
+def bf16_bits_to_f64(bits):
+    """uint16 bfloat16 bit patterns -> float64, exactly."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(
+        np.float64)
+
+
+def to_f64(a):
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return bf16_bits_to_f64(a)
+    return a.astype(np.float64)
+
+
+def brute_decode(q, k_pool, v_pool, block_table, seq_lens, scale):
+    q = to_f64(q)
+    k_pool = to_f64(k_pool)
+    v_pool = to_f64(v_pool)
+    B, Hq, D = q.shape
+    _, bs, Hkv, _ = k_pool.shape
+    G = Hq // Hkv
+    out = np.zeros((B, Hq, D))
+    for b in range(B):
+        L = int(seq_lens[b])
+        if L == 0:
+            continue
+        t = np.arange(L)
+        phys = np.asarray(block_table[b])[t // bs]
+        K = k_pool[phys, t % bs]            # [L, Hkv, D]
+        V = v_pool[phys, t % bs]
+        K = np.repeat(K, G, axis=1)         # [L, Hq, D]: query head h reads KV head h // G
+        V = np.repeat(V, G, axis=1)
+        S = np.einsum("hd,lhd->hl", q[b], K) * scale   # [Hq, L]
+        S = S - S.max(axis=1, keepdims=True)
+        P = np.exp(S)
+        P = P / P.sum(axis=1, keepdims=True)
+        out[b] = np.einsum("hl,lhd->hd", P, V)
+    return out

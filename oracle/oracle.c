@@ -1,0 +1,218 @@
+/*
+ * Float64 CPU oracle for paged grouped-query decode attention.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the checker, not the product: only the
+ * test suite, the smoke check and the benchmark's CPU-baseline leg load it.  It
+ * shares no code, header, table or helper with the CUDA library.
+ *
+ * What it computes (textbook definition, no blocking, no fusion, no reordering):
+ *
+ *   For every sequence b and query head h:
+ *     kv      = h / G,  G = Hq / Hkv            (contiguous head groups)
+ *     k_t,v_t = the t-th logical token of sequence b, for t in [0, L_b),
+ *               found in physical block block_table[b][t / bs] at slot t % bs
+ *     s_t     = scale * sum_d q[b,h,d] * k_t[d]
+ *     out     = sum_t exp(s_t - max s) v_t / sum_t exp(s_t - max s)
+ *
+ * Passages followed:
+ *   - "Modern LLM Inference - Workloads, Bottlenecks, and Optimization
+ *     Techniques" (Stanford LLM lecture 11 notes), section "Why Cross-Layer
+ *     Attention Shares K/V but Not Q", equation Attention(Q,K,V) =
+ *     softmax(Q K^T / sqrt(d)) V.  The 1/sqrt(d) factor is the `scale` argument.
+ *   - same notes, section 4.1 "Grouped-Query Attention": N query heads share K
+ *     key/value heads, each KV head serving one group of query heads.
+ *   - "The Ultimate Guide to LLM Inference Optimization - Part 2", section
+ *     "Grouped Query Attention" (num heads divisible by num kv groups) and
+ *     section "Paged Attention" (fixed-size blocks, e.g. 16 tokens, and a block
+ *     table mapping a request's logical sequence to physical blocks).
+ *   - itinai.com page on packed variable-length batches and GQA: the 5-D query
+ *     layout [batch, seq, groups, per-group heads, dim] with a singleton KV head
+ *     axis, which fixes the contiguous grouping kv = h / G.
+ *   - "Advanced Optimizations: MQA, GQA, and PagedAttention", section
+ *     "PagedAttention: The OS Analogy": the model sees a continuous logical
+ *     sequence while the data is scattered over physical blocks.
+ *
+ * Readings where the pages are silent:
+ *   - seq_lens[b] counts the cached tokens; the single decode query attends to
+ *     all of them (no causal mask for one query token).
+ *   - L_b == 0 gives an all-zero output row.
+ *   - A block id outside [0, num_blocks) or L_b outside [0, max_blocks*bs]
+ *     gives NaN for the affected rows and a non-zero return code.
+ *   - Inputs are read in their stored type and widened exactly to double
+ *     (bf16 -> float is exact by appending 16 zero bits; float -> double is
+ *     exact).  All arithmetic is double with libm exp().
+ *
+ * Parallelised over (b, h) rows with OpenMP when compiled with -fopenmp; each
+ * row is computed by one thread in the order written above.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_OK = 0, ORACLE_ERR_ARG = 1, ORACLE_ERR_BLOCK_ID = 2, ORACLE_ERR_SEQ_LEN = 3 };
+
+/* Exact widening of element `idx` of a float32 or bfloat16 array. */
+static double load_elem(const void *base, int64_t idx, int dtype)
+{
+    if (dtype == ORACLE_F32) {
+        return (double)((const float *)base)[idx];
+    }
+    uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* One output row out[0..D) for sequence b, query head h.  Returns a status. */
+static int decode_row(const void *q, const void *k_pool, const void *v_pool,
+                      const int32_t *block_table, const int32_t *seq_lens, int dtype,
+                      int Hq, int Hkv, int D, int block_size, int64_t num_blocks,
+                      int max_blocks, double scale, int b, int h, double *out)
+{
+    const int G = Hq / Hkv;
+    const int kv = h / G;
+    const int64_t L = seq_lens[b];
+    int d;
+
+    if (L < 0 || L > (int64_t)max_blocks * block_size) {
+        for (d = 0; d < D; ++d) out[d] = NAN;
+        return ORACLE_ERR_SEQ_LEN;
+    }
+    for (d = 0; d < D; ++d) out[d] = 0.0;
+    if (L == 0) return ORACLE_OK;
+
+    /* Gather: physical (block, slot) of every logical token, checked first. */
+    int64_t *row_base = (int64_t *)malloc((size_t)L * sizeof(int64_t));
+    double *s = (double *)malloc((size_t)L * sizeof(double));
+    if (!row_base || !s) {
+        free(row_base);
+        free(s);
+        for (d = 0; d < D; ++d) out[d] = NAN;
+        return ORACLE_ERR_ARG;
+    }
+    for (int64_t t = 0; t < L; ++t) {
+        int64_t phys = block_table[(int64_t)b * max_blocks + t / block_size];
+        int64_t slot = t % block_size;
+        if (phys < 0 || phys >= num_blocks) {
+            free(row_base);
+            free(s);
+            for (d = 0; d < D; ++d) out[d] = NAN;
+            return ORACLE_ERR_BLOCK_ID;
+        }
+        /* pool layout [num_blocks, block_size, Hkv, D] */
+        row_base[t] = ((phys * block_size + slot) * Hkv + kv) * (int64_t)D;
+    }
+
+    /* Scores s_t = scale * <q, k_t>. */
+    const int64_t q_base = ((int64_t)b * Hq + h) * (int64_t)D;
+    for (int64_t t = 0; t < L; ++t) {
+        double dot = 0.0;
+        for (d = 0; d < D; ++d) {
+            dot += load_elem(q, q_base + d, dtype) * load_elem(k_pool, row_base[t] + d, dtype);
+        }
+        s[t] = scale * dot;
+    }
+
+    /* Softmax weights, max-subtracted for range, then the weighted mean of V. */
+    double m = s[0];
+    for (int64_t t = 1; t < L; ++t) {
+        if (s[t] > m) m = s[t];
+    }
+    double z = 0.0;
+    for (int64_t t = 0; t < L; ++t) {
+        s[t] = exp(s[t] - m);
+        z += s[t];
+    }
+    for (int64_t t = 0; t < L; ++t) {
+        for (d = 0; d < D; ++d) {
+            out[d] += s[t] * load_elem(v_pool, row_base[t] + d, dtype);
+        }
+    }
+    for (d = 0; d < D; ++d) out[d] /= z;
+
+    free(row_base);
+    free(s);
+    return ORACLE_OK;
+}
+
+static int check_args(int dtype, int B, int Hq, int Hkv, int D, int block_size,
+                      int64_t num_blocks, int max_blocks)
+{
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return ORACLE_ERR_ARG;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || block_size <= 0) return ORACLE_ERR_ARG;
+    if (num_blocks < 0 || max_blocks < 0) return ORACLE_ERR_ARG;
+    if (Hq % Hkv != 0) return ORACLE_ERR_ARG;
+    return ORACLE_OK;
+}
+
+/*
+ * Selected rows.  rows[2*i], rows[2*i+1] = (b, h) of output row i; out is
+ * [n_rows, D] doubles.  Returns the first non-zero row status, else 0.
+ */
+int oracle_decode_rows_f64(const void *q, const void *k_pool, const void *v_pool,
+                           const int32_t *block_table, const int32_t *seq_lens, int dtype,
+                           int B, int Hq, int Hkv, int D, int block_size, int64_t num_blocks,
+                           int max_blocks, double scale, const int32_t *rows, int64_t n_rows,
+                           double *out)
+{
+    int rc = check_args(dtype, B, Hq, Hkv, D, block_size, num_blocks, max_blocks);
+    if (rc) return rc;
+    for (int64_t i = 0; i < n_rows; ++i) {
+        if (rows[2 * i] < 0 || rows[2 * i] >= B || rows[2 * i + 1] < 0 || rows[2 * i + 1] >= Hq)
+            return ORACLE_ERR_ARG;
+    }
+    int status = ORACLE_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n_rows; ++i) {
+        int r = decode_row(q, k_pool, v_pool, block_table, seq_lens, dtype, Hq, Hkv, D,
+                           block_size, num_blocks, max_blocks, scale, rows[2 * i],
+                           rows[2 * i + 1], out + i * (int64_t)D);
+        if (r) {
+#pragma omp critical
+            {
+                if (!status) status = r;
+            }
+        }
+    }
+    return status;
+}
+
+/* Every row: out is [B, Hq, D] doubles. */
+int oracle_decode_f64(const void *q, const void *k_pool, const void *v_pool,
+                      const int32_t *block_table, const int32_t *seq_lens, int dtype, int B,
+                      int Hq, int Hkv, int D, int block_size, int64_t num_blocks, int max_blocks,
+                      double scale, double *out)
+{
+    int rc = check_args(dtype, B, Hq, Hkv, D, block_size, num_blocks, max_blocks);
+    if (rc) return rc;
+    int status = ORACLE_OK;
+    const int64_t n_rows = (int64_t)B * Hq;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n_rows; ++i) {
+        int r = decode_row(q, k_pool, v_pool, block_table, seq_lens, dtype, Hq, Hkv, D,
+                           block_size, num_blocks, max_blocks, scale, (int)(i / Hq),
+                           (int)(i % Hq), out + i * (int64_t)D);
+        if (r) {
+#pragma omp critical
+            {
+                if (!status) status = r;
+            }
+        }
+    }
+    return status;
+}
+
+/* Threads OpenMP will use (1 without OpenMP). */
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,331 @@
+"""Pins for the float64 oracle: facts fixed by the pages and by the mathematics.
+
+Each ``pin_*`` takes an oracle object (with ``decode_f64``) and raises
+AssertionError when the oracle disagrees with something that does not depend
+on the oracle itself: a second dense formulation (brute force on tiny inputs),
+closed forms, exact special cases, and invariances the pages state.  The same
+pins are run against deliberately broken copies of the oracle in
+``test_oracle_mutants.py`` to show each plausible mistake is caught.
+
+Sources:
+  * Attention(Q,K,V) = softmax(Q K^T / sqrt(d)) V -- "Modern LLM Inference -
+    Workloads, Bottlenecks, and Optimization Techniques", section "Why
+    Cross-Layer Attention Shares K/V but Not Q".
+  * N query heads share K KV heads, one group per KV head, and the cache shrinks
+    by N/K -- same notes, section 4.1 "Grouped-Query Attention".
+  * Contiguous grouping: query layout [batch, seq, groups, per-group heads, dim]
+    with a singleton KV-head axis -- itinai.com page on variable-length batches
+    and GQA.
+  * A continuous logical sequence over scattered physical blocks -- "Advanced
+    Optimizations: MQA, GQA, and PagedAttention", section "PagedAttention: The
+    OS Analogy"; blocks of e.g. 16 tokens and a block table -- "The Ultimate
+    Guide to LLM Inference Optimization - Part 2", section "Paged Attention".
+  * Several sequences pointing at the same blocks (prefix sharing) -- "Modern
+    LLM Inference ...", section 8.2 "Prefix Sharing (Copy-on-Write)".
+  * FlashAttention computes the exact softmax -- same notes, "Linear Attention
+    vs. FlashAttention (Online Softmax)".
+"""
+import math
+
+import numpy as np
+import torch
+
+from oracle.brute import bf16_bits_to_f64, brute_decode
+
+
+# ----------------------------------------------------------------------------- inputs
+def bf16_bits(a):
+    """float array -> uint16 bfloat16 bits (round to nearest even, via torch)."""
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def paged_case(rng, B, Hq, Hkv, D, bs, lens, dtype="f32", spare=3, max_blocks=None):
+    """Random q / pools with a random physical block permutation."""
+    lens = np.asarray(lens, dtype=np.int32)
+    nb = [-(-int(L) // bs) for L in lens]
+    used = sum(nb)
+    num_blocks = used + spare
+    max_blocks = max_blocks if max_blocks is not None else max(1, max(nb) if nb else 1)
+    perm = rng.permutation(num_blocks)
+    table = np.full((B, max_blocks), -1, dtype=np.int32)
+    p = 0
+    for b in range(B):
+        table[b, :nb[b]] = perm[p:p + nb[b]]
+        p += nb[b]
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    k = rng.standard_normal((num_blocks, bs, Hkv, D)).astype(np.float32)
+    v = rng.standard_normal((num_blocks, bs, Hkv, D)).astype(np.float32)
+    if dtype == "bf16":
+        q, k, v = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+    return q, k, v, table, lens
+
+
+def as_f64(a):
+    return bf16_bits_to_f64(a) if a.dtype == np.uint16 else a.astype(np.float64)
+
+
+def contiguous_layout(q, k, v, table, lens, bs_new=None):
+    """The same logical caches laid out in order: sequence b's tokens in
+    consecutive physical blocks, starting at block 0, optionally re-blocked."""
+    B = q.shape[0]
+    _, bs, Hkv, D = k.shape
+    bs_new = bs_new or bs
+    nb_new = [-(-int(L) // bs_new) for L in lens]
+    total = max(1, sum(nb_new))
+    kk = np.zeros((total, bs_new, Hkv, D), dtype=k.dtype)
+    vv = np.zeros((total, bs_new, Hkv, D), dtype=v.dtype)
+    tt = np.full((B, max(1, max(nb_new) if nb_new else 1)), -1, dtype=np.int32)
+    p = 0
+    for b in range(B):
+        for t in range(int(lens[b])):
+            src_blk, src_slot = table[b, t // bs], t % bs
+            dst_blk, dst_slot = p + t // bs_new, t % bs_new
+            kk[dst_blk, dst_slot] = k[src_blk, src_slot]
+            vv[dst_blk, dst_slot] = v[src_blk, src_slot]
+        tt[b, :nb_new[b]] = np.arange(p, p + nb_new[b])
+        p += nb_new[b]
+    return q, kk, vv, tt, lens
+
+
+# ----------------------------------------------------------------------------- pins
+def pin_brute_force(orc):
+    """Dense numpy formulation agrees to 1e-12 on tiny random inputs."""
+    rng = np.random.default_rng(7)
+    cases = [
+        (3, 4, 2, 8, 4, [5, 1, 9], "f32"),
+        (2, 4, 4, 16, 2, [3, 8], "f32"),          # MHA
+        (2, 6, 1, 8, 3, [7, 4], "bf16"),          # MQA, odd block size
+        (4, 8, 2, 16, 16, [1, 7, 16, 33], "bf16"),
+        (1, 2, 1, 4, 5, [40], "f32"),
+    ]
+    for B, Hq, Hkv, D, bs, lens, dt in cases:
+        q, k, v, t, L = paged_case(rng, B, Hq, Hkv, D, bs, lens, dt)
+        scale = 1.0 / math.sqrt(D)
+        out, rc = orc.decode_f64(q, k, v, t, L, scale)
+        ref = brute_decode(q, k, v, t, L, scale)
+        assert rc == 0
+        assert np.abs(out - ref).max() <= 1e-12, (B, Hq, Hkv, D, bs, lens, dt)
+
+
+def pin_paged_equals_contiguous(orc):
+    """Scattered blocks give exactly the result of the same tokens laid out in
+    order, and of the same tokens re-blocked with another block size."""
+    rng = np.random.default_rng(11)
+    q, k, v, t, L = paged_case(rng, 5, 8, 2, 16, 4, [13, 1, 4, 22, 9], "bf16")
+    out, _ = orc.decode_f64(q, k, v, t, L, 0.25)
+    for bs_new in (4, 1, 7, 32):
+        out2, _ = orc.decode_f64(*contiguous_layout(q, k, v, t, L, bs_new), 0.25)
+        assert np.array_equal(out, out2), bs_new
+
+
+def pin_gqa_equals_repeated_mha(orc):
+    """GQA equals MHA whose KV head h holds the GQA KV head h // G."""
+    rng = np.random.default_rng(13)
+    for Hq, Hkv in ((8, 2), (6, 3), (5, 1)):
+        G = Hq // Hkv
+        q, k, v, t, L = paged_case(rng, 3, Hq, Hkv, 8, 4, [6, 11, 3], "f32")
+        out, _ = orc.decode_f64(q, k, v, t, L, 0.4)
+        k_mha = np.repeat(k, G, axis=2)
+        v_mha = np.repeat(v, G, axis=2)
+        out_mha, _ = orc.decode_f64(q, k_mha, v_mha, t, L, 0.4)
+        assert np.array_equal(out, out_mha), (Hq, Hkv)
+
+
+def pin_length_one_returns_v_row(orc):
+    """With one cached token the softmax weight is 1: out[b,h] is exactly the V
+    row of KV head h // G (this fixes the head grouping on its own)."""
+    rng = np.random.default_rng(17)
+    B, Hq, Hkv, D, bs = 3, 12, 3, 8, 4
+    q, k, v, t, L = paged_case(rng, B, Hq, Hkv, D, bs, [1, 1, 1], "bf16")
+    out, rc = orc.decode_f64(q, k, v, t, L, 0.3)
+    assert rc == 0
+    vf = as_f64(v)
+    G = Hq // Hkv
+    for b in range(B):
+        for h in range(Hq):
+            assert np.array_equal(out[b, h], vf[t[b, 0], 0, h // G]), (b, h)
+
+
+def pin_identical_keys_mean_of_v(orc):
+    """Equal logits give uniform weights: identical keys, or scale 0, return the
+    plain mean of the V rows."""
+    rng = np.random.default_rng(19)
+    B, Hq, Hkv, D, bs = 2, 4, 2, 8, 4
+    q, k, v, t, L = paged_case(rng, B, Hq, Hkv, D, bs, [10, 5], "f32")
+    k[:] = k[0, 0, 0]
+    vf = as_f64(v)
+    out, _ = orc.decode_f64(q, k, v, t, L, 0.5)
+    q2, k2, v2, t2, L2 = paged_case(rng, B, Hq, Hkv, D, bs, [10, 5], "f32")
+    out0, _ = orc.decode_f64(q2, k2, v2, t2, L2, 0.0)
+    v2f = as_f64(v2)
+    G = Hq // Hkv
+    for b in range(B):
+        n = int(L[b])
+        for h in range(Hq):
+            rows = np.stack([vf[t[b, i // bs], i % bs, h // G] for i in range(n)])
+            assert np.abs(out[b, h] - rows.mean(axis=0)).max() <= 1e-12
+            rows2 = np.stack([v2f[t2[b, i // bs], i % bs, h // G] for i in range(n)])
+            assert np.abs(out0[b, h] - rows2.mean(axis=0)).max() <= 1e-12
+
+
+def pin_hard_one_hot_large_logits(orc):
+    """A key aligned with q and all others orthogonal to it: the output is that
+    key's V row within exp(-margin).  Logits near 900 overflow exp() unless the
+    maximum is subtracted first, so this also pins the range handling."""
+    rng = np.random.default_rng(23)
+    D, bs, L = 16, 4, 11
+    q = np.zeros((1, 1, D), dtype=np.float32)
+    q[0, 0, 0] = 3.0
+    k = rng.standard_normal((4, bs, 1, D)).astype(np.float32)
+    k[..., 0] = 0.0                      # every key orthogonal to q ...
+    j = 6
+    t = np.array([[2, 0, 3]], dtype=np.int32)
+    k[t[0, j // bs], j % bs, 0, :] = 0.0
+    k[t[0, j // bs], j % bs, 0, 0] = 600.0  # ... except key j: logit 0.5*3*600 = 900
+    v = rng.standard_normal((4, bs, 1, D)).astype(np.float32)
+    out, _ = orc.decode_f64(q, k, v, t, np.array([L], np.int32), 0.5)
+    assert np.all(np.isfinite(out))
+    want = v[t[0, j // bs], j % bs, 0].astype(np.float64)
+    assert np.abs(out[0, 0] - want).max() <= 1e-12
+
+
+def pin_closed_form_three_tokens(orc):
+    """Logits 0, 1, 2 (q = e0, keys 0, 1, 2 times e0, scale 1) give weights
+    1 : e : e^2, so out = (v0 + e v1 + e^2 v2) / (1 + e + e^2)."""
+    D, bs = 2, 2
+    q = np.array([[[1.0, 0.0]]], dtype=np.float32)
+    k = np.zeros((3, bs, 1, D), dtype=np.float32)
+    v = np.zeros((3, bs, 1, D), dtype=np.float32)
+    t = np.array([[2, 0]], dtype=np.int32)          # logical block 0 -> physical 2, 1 -> 0
+    vals = [(0.5, -1.0), (2.0, 0.25), (-3.0, 4.0)]
+    for i, a in enumerate([0.0, 1.0, 2.0]):
+        blk, slot = t[0, i // bs], i % bs
+        k[blk, slot, 0, 0] = a
+        v[blk, slot, 0] = vals[i]
+    out, _ = orc.decode_f64(q, k, v, t, np.array([3], np.int32), 1.0)
+    e = math.e
+    z = 1.0 + e + e * e
+    want = [(vals[0][d] + e * vals[1][d] + e * e * vals[2][d]) / z for d in range(D)]
+    assert np.abs(out[0, 0] - np.array(want)).max() <= 1e-15
+
+
+def pin_scale_two_tokens(orc):
+    """Two tokens with logit gap `scale * delta`: out = v0 + (v1 - v0) *
+    1 / (1 + exp(-scale * delta)).  A dropped, squared or inverted scale fails."""
+    D, bs = 3, 1
+    q = np.array([[[2.0, 1.0, -1.0]]], dtype=np.float32)
+    k = np.array([[[[0.5, 0.0, 1.0]]], [[[1.0, 2.0, 0.0]]]], dtype=np.float32)  # [2,1,1,3]
+    v = np.array([[[[1.0, -2.0, 0.5]]], [[[3.0, 1.0, -0.5]]]], dtype=np.float32)
+    t = np.array([[0, 1]], dtype=np.int32)
+    for scale in (0.37, 1.9, 0.0):
+        out, _ = orc.decode_f64(q, k, v, t, np.array([2], np.int32), scale)
+        s0 = 2 * 0.5 + 1 * 0.0 + (-1) * 1.0
+        s1 = 2 * 1.0 + 1 * 2.0 + (-1) * 0.0
+        w1 = 1.0 / (1.0 + math.exp(-scale * (s1 - s0)))
+        want = v[0, 0, 0].astype(np.float64) + (v[1, 0, 0] - v[0, 0, 0]).astype(np.float64) * w1
+        assert np.abs(out[0, 0] - want).max() <= 1e-15, scale
+
+
+def pin_prefix_sharing_aliases(orc):
+    """Two table rows that point at the same physical blocks, with the same q
+    and length, give bit-identical rows; a row sharing only a prefix differs."""
+    rng = np.random.default_rng(29)
+    q, k, v, t, L = paged_case(rng, 3, 4, 2, 8, 4, [14, 3, 9], "bf16", max_blocks=4)
+    t[1] = t[0]
+    L[1] = L[0]
+    q[1] = q[0]
+    t[2, :3] = t[0, :3]                  # shares three blocks, then stops at 9 tokens
+    q[2] = q[0]
+    out, _ = orc.decode_f64(q, k, v, t, L, 0.35)
+    assert np.array_equal(out[0], out[1])
+    assert not np.array_equal(out[0], out[2])
+
+
+def pin_shift_invariance(orc):
+    """Adding one vector u to every key of a KV head adds scale*<q,u> to all of a
+    query head's logits, which the softmax removes."""
+    rng = np.random.default_rng(31)
+    q, k, v, t, L = paged_case(rng, 2, 6, 2, 8, 4, [9, 17], "f32")
+    out, _ = orc.decode_f64(q, k, v, t, L, 0.3)
+    u = rng.standard_normal((1, 1, 2, 8)).astype(np.float32)
+    k2 = (k.astype(np.float64) + u).astype(np.float32)
+    # the float32 rounding of k + u perturbs logits by ~1e-7 relative; compare loosely
+    out2, _ = orc.decode_f64(q, k2, v, t, L, 0.3)
+    assert np.abs(out - out2).max() <= 1e-5
+
+
+def pin_edge_statuses(orc):
+    """L = 0 gives zeros; a bad block id or an over-long length gives NaN rows
+    and a non-zero status; unused blocks and tail slots are never read."""
+    rng = np.random.default_rng(37)
+    q, k, v, t, L = paged_case(rng, 3, 4, 2, 8, 4, [0, 6, 5], "f32", max_blocks=3)
+    out, rc = orc.decode_f64(q, k, v, t, L, 0.3)
+    assert rc == 0 and np.array_equal(out[0], np.zeros_like(out[0]))
+    # poison everything the definition does not touch
+    used = set(t[1, :2]) | set(t[2, :2])
+    kp, vp = k.copy(), v.copy()
+    for blk in range(k.shape[0]):
+        if blk not in used:
+            kp[blk] = np.nan
+            vp[blk] = np.nan
+    kp[t[1, 1], 2:] = np.nan
+    vp[t[1, 1], 2:] = np.nan
+    kp[t[2, 1], 1:] = np.nan
+    vp[t[2, 1], 1:] = np.nan
+    t2 = t.copy()
+    t2[1:, 2] = 12345                    # entries past the last block are ignored
+    out_p, rc = orc.decode_f64(q, kp, vp, t2, L, 0.3)
+    assert rc == 0 and np.array_equal(out, out_p)
+    t3 = t.copy()
+    t3[1, 1] = k.shape[0]                # out of range
+    out_b, rc = orc.decode_f64(q, k, v, t3, L, 0.3)
+    assert rc == 2 and np.all(np.isnan(out_b[1])) and np.array_equal(out_b[2], out[2])
+    L4 = L.copy()
+    L4[2] = 3 * 4 + 1                    # longer than max_blocks * block_size
+    out_l, rc = orc.decode_f64(q, k, v, t, L4, 0.3)
+    assert rc == 3 and np.all(np.isnan(out_l[2])) and np.array_equal(out_l[1], out[1])
+
+
+def pin_bf16_widening(orc):
+    """bfloat16 bit patterns decode exactly (value = the float32 whose top 16
+    bits they are): 1.0, -2.0, 1 + 2^-7, the largest finite, the smallest
+    subnormal, -0."""
+    pats = np.array([0x3F80, 0xC000, 0x3F81, 0x7F7F, 0x0001, 0x8000, 0x4049, 0xBE80],
+                    dtype=np.uint16)
+    want = np.array([1.0, -2.0, 1.0 + 2.0 ** -7, (2 - 2.0 ** -7) * 2.0 ** 127, 2.0 ** -133,
+                     -0.0, 3.140625, -0.25])
+    D = pats.size
+    q = np.zeros((1, 1, D), dtype=np.uint16)
+    k = np.zeros((1, 1, 1, D), dtype=np.uint16)
+    v = pats.reshape(1, 1, 1, D)
+    out, _ = orc.decode_f64(q, k, v, np.array([[0]], np.int32), np.array([1], np.int32), 1.0)
+    assert np.array_equal(out[0, 0], want)
+
+
+def pin_rows_match_full(orc):
+    """The selected-rows entry point returns the same rows as the full one."""
+    rng = np.random.default_rng(41)
+    q, k, v, t, L = paged_case(rng, 4, 8, 2, 16, 4, [3, 17, 1, 8], "bf16")
+    out, _ = orc.decode_f64(q, k, v, t, L, 0.25)
+    rows = np.array([[0, 0], [3, 7], [1, 5], [2, 2]])
+    sub, _ = orc.decode_rows_f64(q, k, v, t, L, 0.25, rows)
+    for i, (b, h) in enumerate(rows):
+        assert np.array_equal(sub[i], out[b, h])
+
+
+PINS = [
+    pin_brute_force,
+    pin_paged_equals_contiguous,
+    pin_gqa_equals_repeated_mha,
+    pin_length_one_returns_v_row,
+    pin_identical_keys_mean_of_v,
+    pin_hard_one_hot_large_logits,
+    pin_closed_form_three_tokens,
+    pin_scale_two_tokens,
+    pin_prefix_sharing_aliases,
+    pin_shift_invariance,
+    pin_edge_statuses,
+    pin_bf16_widening,
+    pin_rows_match_full,
+]
