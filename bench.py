@@ -1,0 +1,382 @@
+"""Benchmark: paged GQA decode KV GB/s, % of HBM peak and tokens/s per layer.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+A step is one decode call (block-table walk, TMA page staging, q K^T, online
+softmax, P V, split-KV merge) over one batch of the workload, with every input
+resident in HBM.  The default workload is the Llama-3-8B layer shape: B=64
+sequences, lengths uniform in [128, 4096], Hq=32, Hkv=8, D=128, 16-token
+blocks, bf16, a pool of ceil(1.1 * used) blocks with a seeded shuffled block
+table.  Its K/V (about 0.6 GB) is larger than L2, so no flush is needed between
+steps.  Rank 0 prints one JSON line.
+
+--impl reference times the float64 CPU oracle on the host cores instead (the
+comparison arm), over the same workload.
+Multi-GPU (torchrun): every rank runs its own replica of the workload (seed +
+rank), no data-path collective; value = all ranks' bytes / max time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import gen  # noqa: E402
+from paged_gqa_decode_04_gb300 import accounting  # noqa: E402
+
+METRIC = "paged GQA decode KV GB/s and % of GB300 HBM peak; tokens/s per layer"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SRC = os.path.join(ROOT, "paged_gqa_decode_04_gb300", "csrc", "decode_tma.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def describe(w):
+    spec = gen.CONFIGS[w.name]
+    return ("%s: B=%d, Hq=%d, Hkv=%d (G=%d), D=%d, block_size=%d, %s, lengths %s, "
+            "pool %d blocks, seed %d" % (w.name, w.B, w.Hq, w.Hkv, w.G, w.D, w.block_size,
+                                         w.dtype, spec["lens"] if not isinstance(spec["lens"], list)
+                                         else "fixed", w.num_blocks, w.seed))
+
+
+def peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash():
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(config):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source and this workload; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            doc = json.load(f)
+        ent = doc.get(config)
+        if ent and ent.get("kernel_sha") == kernel_hash():
+            return int(ent["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while it runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "bench_clocks_%d.csv" % os.getpid())
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index),
+                                          "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                                          "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+                except ValueError:
+                    continue
+        if not rows:
+            return None
+        busy = [r for r in rows if r[2] > 1.5 * min(x[2] for x in rows)] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in busy for i, v in enumerate(r[3][1:5])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in busy),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(busy)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def cpu_oracle_rate(w, budget_s, rows_cap=None):
+    """Run the oracle over the whole workload (or a row subset) until
+    `budget_s` has passed; returns (GB/s over algorithmic bytes, sample, cores)."""
+    import oracle
+
+    q, k, v = gen.to_numpy_bits(w.q), gen.to_numpy_bits(w.k_pool), gen.to_numpy_bits(w.v_pool)
+    elt = accounting.ELT[w.dtype]
+    nbytes = accounting.algorithmic_bytes(w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt)
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.decode_f64(q, k, v, w.table_np, w.lens_np, w.scale)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    sample = "%d full pass(es) of the workload (all %d x %d rows) in %.1f s" % (reps, w.B, w.Hq, dt)
+    return nbytes * reps / dt / 1e9, sample, oracle.num_threads(), w.B * reps / dt
+
+
+def run_reference(args, world, rank):
+    """The comparison arm: the float64 CPU oracle as it stands."""
+    if rank != 0:
+        return
+    w = gen.make(args.config, device="cpu")
+    elt = accounting.ELT[w.dtype]
+    nbytes = accounting.algorithmic_bytes(w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt)
+    import oracle
+
+    q, k, v = gen.to_numpy_bits(w.q), gen.to_numpy_bits(w.k_pool), gen.to_numpy_bits(w.v_pool)
+    # One step = the oracle over a bounded sample: every sequence, a subset of
+    # query heads (whole KV groups) so that K+W steps fit in a few minutes.
+    heads = max(w.G, min(w.Hq, (w.Hq // 8) // w.G * w.G or w.G))
+    rows = np.array([[b, h] for b in range(w.B) for h in range(heads)], dtype=np.int32)
+    frac = heads / w.Hq
+    for _ in range(args.warmup):
+        oracle.decode_rows_f64(q, k, v, w.table_np, w.lens_np, w.scale, rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode_rows_f64(q, k, v, w.table_np, w.lens_np, w.scale, rows)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = nbytes * frac / dt / 1e9
+    sample = ("each step: every sequence, query heads 0..%d of %d (%.1f%% of the rows), "
+              "float64, host cores" % (heads - 1, w.Hq, 100 * frac))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(w), "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import paged_gqa_decode_04_gb300 as pgd
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = gen.make(args.config, device=dev, seed=gen.CONFIGS[args.config]["seed"] + rank)
+    elt = accounting.ELT[w.dtype]
+    nbytes = accounting.algorithmic_bytes(w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt)
+    pool = pgd.PagedKVPool(w.k_pool, w.v_pool)
+    out = torch.empty_like(w.q)
+    ws = pgd.alloc_workspace(pool, w.B, w.Hq, 0)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pgd.paged_gqa_decode(pool, w.q, w.block_table, w.seq_lens, w.scale, out=out,
+                             workspace=ws, stream=stream)
+
+    step()
+    status = pgd.paged_gqa_get_error(pool, stream)
+    if status != 0:
+        raise RuntimeError("device error: %s" % pgd.strerror(status))
+
+    if args.profile:
+        # exactly W + K launches of the step and nothing else, for profilers
+        for _ in range(args.warmup + args.steps):
+            step()
+        torch.cuda.synchronize()
+        status = pgd.paged_gqa_get_error(pool, stream)
+        if rank == 0:
+            print(json.dumps({"profile_run": args.config, "launch_steps": args.warmup + args.steps,
+                              "status": pgd.strerror(status)}), flush=True)
+        if status != 0:
+            raise RuntimeError("device error: %s" % pgd.strerror(status))
+        return
+
+    # warm-up: at least W steps and at least 0.5 s, so the clock sampler sees load
+    with ClockSampler(local) as clk:
+        t_warm = time.perf_counter()
+        n = 0
+        while n < args.warmup or time.perf_counter() - t_warm < 0.5:
+            step()
+            n += 1
+            if n % 64 == 0:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+    t_ms = ev0.elapsed_time(ev1) / args.steps
+    t_ms = max_over_ranks(t_ms, world, dev)
+    status = pgd.paged_gqa_get_error(pool, stream)
+    if status != 0:
+        raise RuntimeError("device error: %s" % pgd.strerror(status))
+
+    # end to end through the public API: per step, copy the step inputs (q, block
+    # table, lengths) from pinned host memory, decode, read the output back.  The
+    # KV pool is the resident cache and stays in HBM.
+    h_q = w.q.cpu().pin_memory()
+    h_bt = w.block_table.cpu().pin_memory()
+    h_sl = w.seq_lens.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    d_q, d_bt, d_sl = torch.empty_like(w.q), torch.empty_like(w.block_table), torch.empty_like(
+        w.seq_lens)
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        d_sl.copy_(h_sl, non_blocking=True)
+        pgd.paged_gqa_decode(pool, d_q, d_bt, d_sl, w.scale, out=out, workspace=ws, stream=stream)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    h2d = (w.q.numel() * w.q.element_size() + w.block_table.numel() * 4 + w.seq_lens.numel() * 4)
+    d2h = out.numel() * out.element_size()
+
+    if rank != 0:
+        return
+    peak, peak_src = peak_hbm()
+    value = world * nbytes / (t_ms * 1e-3) / 1e9
+    per_gpu = nbytes / (t_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": describe(w), "parallelism": "replicas x%d" % world,
+                   "l2": "no flush: each step streams %.0f MB of K/V, above the 126 MB L2"
+                         % (nbytes / 1e6),
+                   "algorithmic_bytes_per_step": nbytes},
+        "pct_of_peak": round(100 * per_gpu / peak, 2),
+        "pct_of_nominal_8tbs": round(100 * per_gpu / NOMINAL_HBM_GBS, 2),
+        "peak_source": "%s (%.0f GB/s)" % (peak_src, peak),
+        "tokens_per_s_per_layer": round(world * w.B / (t_ms * 1e-3), 1),
+        "roofline": {"bound": "hbm", "achieved": round(per_gpu, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(per_gpu / peak, 4), "traffic": ncu_traffic(args.config),
+                     "note": "achieved = algorithmic bytes / event-timed step (decode + merge "
+                             "kernels), so it under-states the decode kernel alone"},
+        "e2e": {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (1 if w.dtype == "bf16" else 2),
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        rate, sample, cores, _ = cpu_oracle_rate(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(rate, 4), "unit": "GB/s", "cores": cores,
+                                "kind": "oracle", "sample": sample}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="llama3_8b", choices=sorted(gen.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="only W + K step launches (for ncu); prints no bench line")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,151 @@
+/*
+ * paged_gqa.h -- C ABI of the paged grouped-query decode attention library
+ * (libpaged_gqa.so), sm_103a (GB300).
+ *
+ * The operation.  One decode step of attention: every sequence b of a batch
+ * has one new query token with Hq heads, and Lb cached key/value tokens held
+ * in a paged KV cache.  For each sequence b and query head h
+ *
+ *     kv      = h / G,   G = Hq / Hkv          (contiguous query-head groups)
+ *     k_t,v_t = token t of sequence b, t in [0, Lb), stored in physical block
+ *               block_table[b][t / block_size] at slot t % block_size
+ *     out[b,h,:] = sum_t softmax_t(scale * <q[b,h,:], k_t>) v_t
+ *
+ * Sources: the attention equation Attention(Q,K,V) = softmax(Q K^T / sqrt(d)) V
+ * ("Modern LLM Inference - Workloads, Bottlenecks, and Optimization
+ * Techniques", section "Why Cross-Layer Attention Shares K/V but Not Q");
+ * grouped-query attention, N query heads sharing K key/value heads (same notes,
+ * section 4.1, and "The Ultimate Guide to LLM Inference Optimization - Part 2",
+ * section "Grouped Query Attention": heads divisible by KV groups); the paged
+ * cache, fixed-size blocks found through a block table ("Advanced
+ * Optimizations: MQA, GQA, and PagedAttention", section "PagedAttention: The OS
+ * Analogy"; "Modern LLM Inference ...", section 8.2 "Paged Attention";
+ * "The Ultimate Guide ... Part 2", section "Paged Attention").  Reading the
+ * block pages inside the attention kernel itself follows the "kernel fusion"
+ * remark of "Modern LLM Inference ...", section 8.3.
+ *
+ * Layouts (all row-major, contiguous, device memory, 16-byte aligned):
+ *     q            [B, Hq, D]                          dtype
+ *     k_pool       [num_blocks, block_size, Hkv, D]    dtype
+ *     v_pool       [num_blocks, block_size, Hkv, D]    dtype
+ *     block_table  [B, max_blocks]                     int32
+ *     seq_lens     [B]                                 int32
+ *     out          [B, Hq, D]                          dtype
+ * dtype is float32 or bfloat16 (PGD_F32 / PGD_BF16); accumulation is float32.
+ * D (head_dim) is 64 or 128; G = Hq / Hkv is 1..64; block_size is 1..256
+ * (bfloat16 pools need a power of two in 8..256).
+ *
+ * Ownership.  The caller owns every buffer: the pools, q, the tables, out and
+ * the workspace.  A pool handle is a non-owning, immutable description of the
+ * two pool allocations; the library allocates only one 4-byte device error
+ * word per handle (freed by paged_kv_pool_destroy).
+ *
+ * Errors.  Every call returns a pgd_status and never throws.  Argument errors
+ * are returned before anything is launched.  paged_gqa_decode is asynchronous
+ * on `stream`; faults the device finds (a block id outside [0, num_blocks), a
+ * length outside [0, max_blocks * block_size], a pipeline wait that gave up)
+ * are latched in the handle's error word and returned by paged_gqa_get_error.
+ * The rows of an affected sequence are written as NaN.  The kernels never trap.
+ *
+ * Threads and streams.  A handle may be used from several host threads and
+ * streams at once as long as concurrent decodes use distinct workspaces and
+ * outputs.
+ */
+#ifndef PAGED_GQA_H
+#define PAGED_GQA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct pgd_pool_s *pgd_pool_t;
+
+enum pgd_dtype { PGD_F32 = 0, PGD_BF16 = 1 };
+
+enum pgd_status {
+    PGD_OK = 0,
+    PGD_ERR_ARG = 1,         /* null pointer, negative or zero size, bad enum value */
+    PGD_ERR_SHAPE = 2,       /* Hq % Hkv != 0, unsupported head_dim / group / block size */
+    PGD_ERR_DTYPE = 3,       /* unknown dtype */
+    PGD_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned */
+    PGD_ERR_WORKSPACE = 5,   /* workspace missing, misaligned or smaller than required */
+    PGD_ERR_CUDA = 6,        /* a CUDA runtime or driver call failed */
+    PGD_ERR_BLOCK_ID = 7,    /* device: a block id outside [0, num_blocks) (latched) */
+    PGD_ERR_SEQ_LEN = 8,     /* device: a length outside [0, max_blocks*block_size] (latched) */
+    PGD_ERR_UNSUPPORTED = 9, /* valid request this build does not implement */
+    PGD_ERR_TIMEOUT = 10     /* device: a pipeline wait gave up (latched) */
+};
+
+/*
+ * Describe a K/V block pool pair resident on the current CUDA device.
+ *   out          receives the handle (set to NULL on error)
+ *   k_pool,
+ *   v_pool       device pointers, [num_blocks, block_size, num_kv_heads, head_dim]
+ *   num_blocks   physical blocks in each pool (>= 1)
+ *   block_size   tokens per block
+ *   num_kv_heads Hkv (>= 1)
+ *   head_dim     D, 64 or 128
+ *   dtype        PGD_F32 or PGD_BF16
+ * The pools are not copied; they must outlive the handle.  Builds the TMA
+ * descriptors the bfloat16 kernel walks the pool with.
+ */
+int paged_kv_pool_create(pgd_pool_t *out, const void *k_pool, const void *v_pool,
+                         int64_t num_blocks, int block_size, int num_kv_heads, int head_dim,
+                         int dtype);
+
+/* Release a handle (not the pools).  NULL is accepted. */
+int paged_kv_pool_destroy(pgd_pool_t pool);
+
+/*
+ * Workspace bytes paged_gqa_decode needs for B sequences, Hq query heads and
+ * `num_splits` (same meaning as in paged_gqa_decode; 0 = automatic).  Written
+ * to *bytes.  The workspace holds per-split partial results, the tile prefix
+ * table and one counter per split run.  It must be zero-filled before its
+ * first use; every call that completes leaves it zero-filled again, so a
+ * workspace can be reused call after call.  After a call that latched
+ * PGD_ERR_TIMEOUT, zero it again.
+ */
+int paged_gqa_workspace_size(pgd_pool_t pool, int B, int Hq, int num_splits, size_t *bytes);
+
+/*
+ * Enqueue one decode step on `stream` (a cudaStream_t; NULL = legacy default
+ * stream).
+ *   q, out       [B, Hq, D] in the pool's dtype; out may not alias q
+ *   block_table  [B, max_blocks] int32; entries past ceil(Lb / block_size) are
+ *                never read and may hold anything
+ *   seq_lens     [B] int32, cached tokens per sequence; Lb == 0 gives zeros
+ *   scale        logit scale, usually 1/sqrt(D)
+ *   workspace    device buffer of at least paged_gqa_workspace_size bytes,
+ *                256-byte aligned, zero-filled before first use (see above);
+ *                calls that may overlap on the GPU need distinct workspaces
+ *   num_splits   how many equal spans the total KV work (all sequences times
+ *                KV heads, in 64-token tiles) is cut into, one CTA each; a
+ *                sequence crossing a span boundary is finished by a
+ *                log-sum-exp merge.  0 = automatic (one span per SM).
+ * The result does not depend on num_splits beyond float32 rounding.
+ */
+int paged_gqa_decode(pgd_pool_t pool, const void *q, int B, int Hq, const int32_t *block_table,
+                     int max_blocks, const int32_t *seq_lens, float scale, void *out,
+                     void *workspace, size_t workspace_bytes, int num_splits, void *stream);
+
+/*
+ * Synchronise `stream`, then read and clear the handle's latched device error.
+ * Returns PGD_OK when no error was latched, the latched pgd_status otherwise,
+ * or PGD_ERR_CUDA when the synchronisation itself failed.
+ */
+int paged_gqa_get_error(pgd_pool_t pool, void *stream);
+
+/* Number of spans num_splits = 0 resolves to for this handle's device. */
+int paged_gqa_auto_splits(pgd_pool_t pool, int *num_splits);
+
+/* Static, human-readable name of a pgd_status. */
+const char *paged_gqa_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_GQA_H */

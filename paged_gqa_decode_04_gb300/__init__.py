@@ -1,0 +1,160 @@
+"""Paged grouped-query decode attention for GB300 (sm_103a).
+
+Python face of libpaged_gqa.so.  The functions keep the C ABI's names and take
+torch tensors for device memory; they only marshal pointers, sizes and the
+current CUDA stream.  The computation -- block-table walk, TMA page staging,
+q K^T, online softmax, P V and the split-KV log-sum-exp merge -- runs in the
+library's kernels.
+"""
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import PagedGQAError, STATUS_NAMES, strerror  # noqa: F401
+
+__all__ = [
+    "PagedKVPool", "PagedGQAError", "paged_kv_pool_create", "paged_kv_pool_destroy",
+    "paged_gqa_workspace_size", "paged_gqa_decode", "paged_gqa_get_error",
+    "paged_gqa_auto_splits", "strerror", "decode",
+]
+
+_DTYPES = {torch.float32: _lib.PGD_F32, torch.bfloat16: _lib.PGD_BF16}
+
+
+def _check(rc, what=""):
+    if rc != 0:
+        raise PagedGQAError(rc, what)
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+class PagedKVPool:
+    """Non-owning handle on a K/V block pool pair [num_blocks, block_size, Hkv, D].
+
+    Keeps references to the two tensors so they outlive the handle.
+    """
+
+    def __init__(self, k_pool, v_pool):
+        lib = _lib.load()
+        if not (isinstance(k_pool, torch.Tensor) and isinstance(v_pool, torch.Tensor)):
+            raise TypeError("k_pool and v_pool must be torch tensors")
+        if k_pool.shape != v_pool.shape or k_pool.dim() != 4:
+            raise ValueError("pools must both be [num_blocks, block_size, Hkv, D]")
+        if k_pool.dtype != v_pool.dtype or k_pool.dtype not in _DTYPES:
+            raise TypeError("pools must be float32 or bfloat16, the same for K and V")
+        if not (k_pool.is_cuda and v_pool.is_cuda):
+            raise ValueError("pools must be CUDA tensors")
+        if not (k_pool.is_contiguous() and v_pool.is_contiguous()):
+            raise ValueError("pools must be contiguous")
+        self.k_pool, self.v_pool = k_pool, v_pool
+        self.num_blocks, self.block_size, self.num_kv_heads, self.head_dim = k_pool.shape
+        self.dtype = k_pool.dtype
+        h = ctypes.c_void_p()
+        with torch.cuda.device(k_pool.device):
+            _check(lib.paged_kv_pool_create(ctypes.byref(h), k_pool.data_ptr(), v_pool.data_ptr(),
+                                            self.num_blocks, self.block_size, self.num_kv_heads,
+                                            self.head_dim, _DTYPES[self.dtype]),
+                   "paged_kv_pool_create")
+        self._h = h
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise ValueError("pool handle destroyed")
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and _lib._lib is not None:
+            rc = _lib._lib.paged_kv_pool_destroy(self._h)
+            self._h = None
+            _check(rc, "paged_kv_pool_destroy")
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def paged_kv_pool_create(k_pool, v_pool):
+    return PagedKVPool(k_pool, v_pool)
+
+
+def paged_kv_pool_destroy(pool):
+    pool.close()
+
+
+def paged_gqa_workspace_size(pool, B, Hq, num_splits=0):
+    n = ctypes.c_size_t()
+    _check(_lib.load().paged_gqa_workspace_size(pool.handle, int(B), int(Hq), int(num_splits),
+                                                ctypes.byref(n)), "paged_gqa_workspace_size")
+    return n.value
+
+
+def paged_gqa_auto_splits(pool):
+    n = ctypes.c_int()
+    _check(_lib.load().paged_gqa_auto_splits(pool.handle, ctypes.byref(n)))
+    return n.value
+
+
+def alloc_workspace(pool, B, Hq, num_splits=0):
+    """A zero-filled workspace tensor of the right size on the pool's device.
+
+    Reusable across calls: every completed call leaves it zero-filled."""
+    nbytes = paged_gqa_workspace_size(pool, B, Hq, num_splits)
+    return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=pool.k_pool.device)
+
+
+def paged_gqa_decode(pool, q, block_table, seq_lens, scale, out=None, workspace=None,
+                     num_splits=0, stream=None):
+    """Enqueue one decode step; returns `out` ([B, Hq, D], q's dtype).
+
+    q [B, Hq, D], block_table [B, max_blocks] int32 and seq_lens [B] int32 are
+    CUDA tensors on the pool's device.  Raises PagedGQAError on an argument
+    error; device-side errors are reported by paged_gqa_get_error.
+    """
+    lib = _lib.load()
+    if q.dim() != 3 or block_table.dim() != 2 or seq_lens.dim() != 1:
+        raise ValueError("q must be [B,Hq,D], block_table [B,max_blocks], seq_lens [B]")
+    if q.dtype != pool.dtype:
+        raise TypeError("q dtype must match the pool")
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    for t in (q, block_table, seq_lens):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    B, Hq, D = q.shape
+    if D != pool.head_dim or block_table.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("shape mismatch between q, tables and pool")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = alloc_workspace(pool, B, Hq, num_splits)
+    _check(lib.paged_gqa_decode(pool.handle, q.data_ptr(), B, Hq, block_table.data_ptr(),
+                                block_table.shape[1], seq_lens.data_ptr(), float(scale),
+                                out.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                int(num_splits), _stream_handle(stream)), "paged_gqa_decode")
+    return out
+
+
+def paged_gqa_get_error(pool, stream=None):
+    """Synchronise the stream and return (then clear) the latched device status."""
+    return int(_lib.load().paged_gqa_get_error(pool.handle, _stream_handle(stream)))
+
+
+def decode(q, k_pool, v_pool, block_table, seq_lens, scale, num_splits=0):
+    """One-shot convenience: build a pool handle, decode, check device errors."""
+    pool = PagedKVPool(k_pool, v_pool)
+    try:
+        out = paged_gqa_decode(pool, q, block_table, seq_lens, scale, num_splits=num_splits)
+        _check(paged_gqa_get_error(pool), "device")
+        return out
+    finally:
+        pool.close()

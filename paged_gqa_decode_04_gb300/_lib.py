@@ -1,0 +1,73 @@
+"""ctypes binding of libpaged_gqa.so (the C ABI declared in include/paged_gqa.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI.  There is no CPU fallback; if the library is missing
+the first call raises.
+"""
+import ctypes
+import os
+import re
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpaged_gqa.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "paged_gqa.h")
+
+PGD_F32 = 0
+PGD_BF16 = 1
+
+STATUS_NAMES = {
+    0: "PGD_OK", 1: "PGD_ERR_ARG", 2: "PGD_ERR_SHAPE", 3: "PGD_ERR_DTYPE", 4: "PGD_ERR_ALIGN",
+    5: "PGD_ERR_WORKSPACE", 6: "PGD_ERR_CUDA", 7: "PGD_ERR_BLOCK_ID", 8: "PGD_ERR_SEQ_LEN",
+    9: "PGD_ERR_UNSUPPORTED", 10: "PGD_ERR_TIMEOUT",
+}
+globals().update({v: k for k, v in STATUS_NAMES.items()})
+
+_lib = None
+
+
+class PagedGQAError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        name = STATUS_NAMES.get(status, str(status))
+        msg = "%s: %s" % (name, strerror(status) if _lib is not None else "")
+        super().__init__(("%s (%s)" % (msg, what)) if what else msg)
+
+
+def load(path=LIB_PATH):
+    """Load the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError("libpaged_gqa.so not built: run `python -c \"import __graft_entry__ as "
+                           "g; g.build()\"` or paged_gqa_decode_04_gb300/build.py")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    lib.paged_kv_pool_create.argtypes = [ctypes.POINTER(vp), vp, vp, i64, i32, i32, i32, i32]
+    lib.paged_kv_pool_create.restype = i32
+    lib.paged_kv_pool_destroy.argtypes = [vp]
+    lib.paged_kv_pool_destroy.restype = i32
+    lib.paged_gqa_workspace_size.argtypes = [vp, i32, i32, i32, ctypes.POINTER(sz)]
+    lib.paged_gqa_workspace_size.restype = i32
+    lib.paged_gqa_decode.argtypes = [vp, vp, i32, i32, vp, i32, vp, ctypes.c_float, vp, vp, sz,
+                                     i32, vp]
+    lib.paged_gqa_decode.restype = i32
+    lib.paged_gqa_get_error.argtypes = [vp, vp]
+    lib.paged_gqa_get_error.restype = i32
+    lib.paged_gqa_auto_splits.argtypes = [vp, ctypes.POINTER(i32)]
+    lib.paged_gqa_auto_splits.restype = i32
+    lib.paged_gqa_strerror.argtypes = [i32]
+    lib.paged_gqa_strerror.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def strerror(status):
+    return load().paged_gqa_strerror(int(status)).decode()
+
+
+def declared_functions(header=HEADER):
+    """Names of the functions include/paged_gqa.h declares."""
+    text = open(header).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(paged_\w+)\s*\(", text)))

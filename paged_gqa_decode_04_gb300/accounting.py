@@ -1,0 +1,56 @@
+"""Byte and token accounting for paged decode attention (host side).
+
+The roofline of decode attention is HBM bandwidth: every cached K/V byte of
+every sequence is read once per step ("Modern LLM Inference ...", section 3:
+decode attention has arithmetic intensity about 1 whatever the batch, and
+"Advanced Optimizations: MQA, GQA, and PagedAttention": moving KV tensors
+dominates).  Algorithmic bytes of one step:
+
+    sum_b L_b * Hkv * D * elt * 2        K and V of the valid tokens
+  + 2 * B * Hq * D * elt                 q in, out back
+  + 4 * (B + sum_b ceil(L_b / bs))       seq_lens and the table entries used
+
+Tail slots of the last block, unused table entries, the rest of the pool and
+the split-KV workspace are not counted.
+"""
+import numpy as np
+
+ELT = {"f32": 4, "bf16": 2}
+
+
+def kv_bytes_per_token(hkv, d, elt):
+    """K plus V bytes one cached token holds for one layer."""
+    return 2 * hkv * d * elt
+
+
+def gqa_reduction_factor(hq, hkv):
+    """Cache shrink of GQA against MHA with the same query heads: N / K."""
+    return kv_bytes_per_token(hq, 1, 1) / kv_bytes_per_token(hkv, 1, 1)
+
+
+def algorithmic_bytes(lens, hq, hkv, d, block_size, elt):
+    lens = np.asarray(lens, dtype=np.int64)
+    pages = int(np.sum((lens + block_size - 1) // block_size))
+    B = int(lens.size)
+    return (int(lens.sum()) * kv_bytes_per_token(hkv, d, elt) + 2 * B * hq * d * elt
+            + 4 * (B + pages))
+
+
+def flops(lens, hq, d):
+    """Multiply-adds of q.k and p.v, two flops each."""
+    return 4 * int(np.sum(lens)) * hq * d
+
+
+def contiguous_waste(reserved_tokens, generated_tokens):
+    """Slots left unused by a contiguous reservation of `reserved_tokens`."""
+    return max(0, reserved_tokens - generated_tokens)
+
+
+def paged_waste(length, block_size):
+    """Slots left unused in the last block of a paged sequence (< block_size)."""
+    return (-length) % block_size
+
+
+def flattened_tokens(lengths):
+    """Tokens of a batch packed with no padding."""
+    return int(np.sum(lengths))

@@ -1,0 +1,269 @@
+// C ABI of libpaged_gqa.so: argument checks, pool descriptors, workspace
+// carve-up and kernel dispatch.  See include/paged_gqa.h for the contract.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <new>
+
+#include "pgd_internal.h"
+
+struct pgd_pool_s {
+    pgd::Pool p;
+};
+
+namespace pgd {
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Make `dev` current for the scope of a call; restore the caller's device.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) {
+            ok = false;
+            return;
+        }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 4-D view of a bf16 pool [num_blocks, bs, Hkv, D] as
+// [d_lo = 64, head-half = Hkv*D/64, slot = bs, block = num_blocks]; one box is
+// one 128-byte half head row for min(bs, 64) consecutive slots of one block.
+bool encode_pool_map(CUtensorMap* map, const void* base, int64_t num_blocks, int bs, int hkv,
+                     int d) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t row_bytes = (cuuint64_t)hkv * d * 2;
+    cuuint64_t dims[4] = {64, (cuuint64_t)hkv * (d / 64), (cuuint64_t)bs, (cuuint64_t)num_blocks};
+    cuuint64_t strides[3] = {128, row_bytes, row_bytes * bs};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)(bs < kTileTokens ? bs : kTileTokens), 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int resolve_parts(const Pool& p, int num_splits) {
+    return num_splits > 0 ? num_splits : p.num_sms;
+}
+
+}  // namespace
+
+WorkspaceLayout workspace_layout(int B, int hkv, int group, int d, int parts) {
+    WorkspaceLayout w;
+    const int mtiles = (group + 15) / 16;
+    w.counters_off = 0;
+    w.tile_base_off = round_up((size_t)B * hkv * mtiles * sizeof(int), 256);
+    w.part_lse_off = w.tile_base_off + round_up((size_t)(B + 1) * sizeof(int64_t), 256);
+    w.part_o_off = w.part_lse_off + round_up((size_t)parts * 2 * group * sizeof(float), 256);
+    w.total = w.part_o_off + round_up((size_t)parts * 2 * group * d * sizeof(float), 256);
+    return w;
+}
+
+}  // namespace pgd
+
+using namespace pgd;
+
+extern "C" {
+
+int paged_kv_pool_create(pgd_pool_t* out, const void* k_pool, const void* v_pool,
+                         int64_t num_blocks, int block_size, int num_kv_heads, int head_dim,
+                         int dtype) {
+    if (!out) return PGD_ERR_ARG;
+    *out = nullptr;
+    if (!k_pool || !v_pool) return PGD_ERR_ARG;
+    if (num_blocks < 1 || num_blocks > INT32_MAX || block_size < 1 || num_kv_heads < 1)
+        return PGD_ERR_ARG;
+    if (dtype != PGD_F32 && dtype != PGD_BF16) return PGD_ERR_DTYPE;
+    if (head_dim != 64 && head_dim != 128) return PGD_ERR_SHAPE;
+    if (block_size > 1024) return PGD_ERR_SHAPE;
+    if (dtype == PGD_BF16 &&
+        (block_size < 8 || block_size > 256 || (block_size & (block_size - 1)) != 0))
+        return PGD_ERR_SHAPE;
+    if (!aligned(k_pool, 16) || !aligned(v_pool, 16)) return PGD_ERR_ALIGN;
+
+    pgd_pool_s* h = new (std::nothrow) pgd_pool_s;
+    if (!h) return PGD_ERR_ARG;
+    memset(h, 0, sizeof(*h));
+    Pool& p = h->p;
+    p.k = k_pool;
+    p.v = v_pool;
+    p.num_blocks = num_blocks;
+    p.block_size = block_size;
+    p.hkv = num_kv_heads;
+    p.d = head_dim;
+    p.dtype = dtype;
+    if (cudaGetDevice(&p.device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&p.num_sms, cudaDevAttrMultiProcessorCount, p.device) !=
+            cudaSuccess ||
+        cudaMalloc(reinterpret_cast<void**>(&p.err), sizeof(int)) != cudaSuccess) {
+        delete h;
+        return PGD_ERR_CUDA;
+    }
+    if (cudaMemset(p.err, 0, sizeof(int)) != cudaSuccess) {
+        cudaFree(p.err);
+        delete h;
+        return PGD_ERR_CUDA;
+    }
+    if (dtype == PGD_BF16) {
+        if (!encode_pool_map(&p.tmap_k, k_pool, num_blocks, block_size, num_kv_heads, head_dim) ||
+            !encode_pool_map(&p.tmap_v, v_pool, num_blocks, block_size, num_kv_heads, head_dim)) {
+            cudaFree(p.err);
+            delete h;
+            return PGD_ERR_CUDA;
+        }
+        p.has_tmap = true;
+    }
+    *out = h;
+    return PGD_OK;
+}
+
+int paged_kv_pool_destroy(pgd_pool_t pool) {
+    if (!pool) return PGD_OK;
+    int rc = PGD_OK;
+    {
+        DeviceGuard g(pool->p.device);
+        if (!g.ok || cudaFree(pool->p.err) != cudaSuccess) rc = PGD_ERR_CUDA;
+    }
+    delete pool;
+    return rc;
+}
+
+int paged_gqa_auto_splits(pgd_pool_t pool, int* num_splits) {
+    if (!pool || !num_splits) return PGD_ERR_ARG;
+    *num_splits = resolve_parts(pool->p, 0);
+    return PGD_OK;
+}
+
+int paged_gqa_workspace_size(pgd_pool_t pool, int B, int Hq, int num_splits, size_t* bytes) {
+    if (!pool || !bytes || B < 0 || Hq < 1 || num_splits < 0 || num_splits > (1 << 20))
+        return PGD_ERR_ARG;
+    const Pool& p = pool->p;
+    if (Hq % p.hkv != 0 || Hq / p.hkv > kMaxGroup) return PGD_ERR_SHAPE;
+    *bytes = workspace_layout(B, p.hkv, Hq / p.hkv, p.d, resolve_parts(p, num_splits)).total;
+    return PGD_OK;
+}
+
+int paged_gqa_decode(pgd_pool_t pool, const void* q, int B, int Hq, const int32_t* block_table,
+                     int max_blocks, const int32_t* seq_lens, float scale, void* out,
+                     void* workspace, size_t workspace_bytes, int num_splits, void* stream) {
+    if (!pool || B < 0 || Hq < 1 || max_blocks < 0 || num_splits < 0 || num_splits > (1 << 20))
+        return PGD_ERR_ARG;
+    if (!isfinite(scale)) return PGD_ERR_ARG;
+    const Pool& p = pool->p;
+    if (Hq % p.hkv != 0) return PGD_ERR_SHAPE;
+    const int G = Hq / p.hkv;
+    if (G > kMaxGroup) return PGD_ERR_SHAPE;
+    if ((int64_t)max_blocks * p.block_size > INT32_MAX) return PGD_ERR_SHAPE;
+    if (B == 0) return PGD_OK;
+    if (!q || !out || !block_table || !seq_lens || !workspace) return PGD_ERR_ARG;
+    if (max_blocks < 1) return PGD_ERR_SHAPE;
+    const size_t elt = p.dtype == PGD_BF16 ? 2 : 4;
+    const size_t qbytes = (size_t)B * Hq * p.d * elt;
+    {
+        const uintptr_t q0 = reinterpret_cast<uintptr_t>(q), o0 = reinterpret_cast<uintptr_t>(out);
+        if (q0 < o0 + qbytes && o0 < q0 + qbytes) return PGD_ERR_ARG;  // out aliases q
+    }
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_table, 4) ||
+        !aligned(seq_lens, 4))
+        return PGD_ERR_ALIGN;
+    const int parts = resolve_parts(p, num_splits);
+    const WorkspaceLayout wl = workspace_layout(B, p.hkv, G, p.d, parts);
+    if (!aligned(workspace, 256) || workspace_bytes < wl.total) return PGD_ERR_WORKSPACE;
+
+    DeviceGuard g(p.device);
+    if (!g.ok) return PGD_ERR_CUDA;
+
+    DecodeArgs a;
+    memset(&a, 0, sizeof(a));
+    a.q = q;
+    a.k_pool = p.k;
+    a.v_pool = p.v;
+    a.out = out;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.B = B;
+    a.hq = Hq;
+    a.hkv = p.hkv;
+    a.group = G;
+    a.d = p.d;
+    a.block_size = p.block_size;
+    a.max_blocks = max_blocks;
+    a.num_blocks = p.num_blocks;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.num_parts = parts;
+    a.err = p.err;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    a.counters = reinterpret_cast<int*>(ws + wl.counters_off);
+    a.tile_base = reinterpret_cast<int64_t*>(ws + wl.tile_base_off);
+    a.part_lse = reinterpret_cast<float*>(ws + wl.part_lse_off);
+    a.part_o = reinterpret_cast<float*>(ws + wl.part_o_off);
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p.dtype == PGD_BF16) {
+        // one launch: the TMA kernel merges split runs itself
+        if (launch_decode_tma(a, p, s) != cudaSuccess) return PGD_ERR_CUDA;
+    } else {
+        if (launch_decode_simple(a, p.dtype, s) != cudaSuccess) return PGD_ERR_CUDA;
+        if (launch_merge(a, p.dtype, s) != cudaSuccess) return PGD_ERR_CUDA;
+    }
+    return PGD_OK;
+}
+
+int paged_gqa_get_error(pgd_pool_t pool, void* stream) {
+    if (!pool) return PGD_ERR_ARG;
+    DeviceGuard g(pool->p.device);
+    if (!g.ok) return PGD_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int host = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PGD_ERR_CUDA;
+    if (cudaMemcpy(&host, pool->p.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PGD_ERR_CUDA;
+    if (host != 0 && cudaMemset(pool->p.err, 0, sizeof(int)) != cudaSuccess) return PGD_ERR_CUDA;
+    return host;
+}
+
+const char* paged_gqa_strerror(int status) {
+    switch (status) {
+        case PGD_OK: return "ok";
+        case PGD_ERR_ARG: return "invalid argument";
+        case PGD_ERR_SHAPE: return "unsupported or inconsistent shape";
+        case PGD_ERR_DTYPE: return "unsupported dtype";
+        case PGD_ERR_ALIGN: return "pointer not aligned";
+        case PGD_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case PGD_ERR_CUDA: return "CUDA call failed";
+        case PGD_ERR_BLOCK_ID: return "block id out of range";
+        case PGD_ERR_SEQ_LEN: return "sequence length out of range";
+        case PGD_ERR_UNSUPPORTED: return "unsupported request";
+        case PGD_ERR_TIMEOUT: return "device pipeline wait timed out";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

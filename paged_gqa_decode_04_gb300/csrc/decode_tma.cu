@@ -1,0 +1,711 @@
+// bfloat16 paged GQA decode: TMA page staging, mbarrier pipeline, tensor-core
+// tile products, online softmax.  sm_103a.
+//
+// Decode attention reads every cached K/V byte once and does G multiply-adds
+// per element, far below the tensor cores' ridge point, so the kernel is built
+// around keeping HBM busy (the pages: "Moving KV tensors from global memory to
+// the compute cores takes significantly longer than the actual matrix
+// multiplication", "Advanced Optimizations: MQA, GQA, and PagedAttention",
+// section "The Memory Bandwidth Bottleneck").
+//
+// Structure of a CTA (one per span of the 64-token tile sequence, see
+// partition.cuh; the grid is one CTA per SM):
+//   * warp NC (producer): walks the span's tiles, reads the tile's block ids
+//     from the block table, and for each 16..64-row page slice issues
+//     cp.async.bulk.tensor loads of K and V ([rows, 64] bf16 boxes, 128-byte
+//     swizzle) into a ring of pipeline stages, each guarded by a "full"
+//     mbarrier (transaction bytes) and an "empty" mbarrier (consumer release).
+//     Reading the pages inside the attention kernel is the block-read +
+//     attention fusion of "Modern LLM Inference ...", section 8.3.
+//   * warps 0..NC-1 (consumers): warp (mt, tg) owns query rows
+//     [16 mt, 16 mt + 16) of the KV head's group and tokens
+//     [tg TW, (tg+1) TW) of every tile.  S = q K^T and O += P V run on
+//     mma.sync m16n8k16 (bf16 in, fp32 accumulate) fed by ldmatrix from the
+//     swizzled stage; the running max / sum softmax runs on the fp32
+//     accumulators in base-2 units.  At the end of a piece the token groups
+//     are combined through shared memory and the tg == 0 warps write the
+//     output row (whole run) or a normalised partial + log-sum-exp (split run).
+//
+// Every wait is bounded (kWaitNs); a wait that gives up latches
+// PGD_ERR_TIMEOUT, marks the CTA aborted and lets every warp leave.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "partition.cuh"
+
+namespace pgd {
+namespace {
+
+constexpr int T = kTileTokens;          // tokens per tile / stage
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
+constexpr int kSmemBudget = 227 * 1024;
+
+// ----------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase of `bar` with the given parity; false after kWaitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > kWaitNs) return false;
+    }
+    return true;
+}
+
+// L2 policy for data read exactly once per call (the K/V pages).
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// D = A(16x16, row) * B(16x8, col) + D; bf16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ----------------------------------------------------------------- configuration
+template <int D_, int MT_, int TG_, bool ROWS16_>
+struct Cfg {
+    static constexpr int D = D_;
+    static constexpr int MT = MT_;            // m16 row tiles of the query group
+    static constexpr int TG = TG_;            // token groups per tile
+    static constexpr bool ROWS16 = ROWS16_;   // rows 8..15 of an m-tile in use
+    static constexpr int NC = MT * TG;        // consumer warps
+    static constexpr int THREADS = (NC + 1) * 32;
+    static constexpr int TW = T / TG;         // tokens per consumer warp per tile
+    static constexpr int HALVES = D / 64;     // 128-byte halves of a head row
+    static constexpr int HALF_BYTES = T * 128;
+    static constexpr int STAGE_BYTES = 2 * HALVES * HALF_BYTES;  // K then V
+    static constexpr int ROWS = ROWS16 ? 16 : 8;
+    static constexpr int COMB_FLOATS = (TG - 1) * MT * ROWS * (D + 2);
+    static constexpr int COMB_BYTES = COMB_FLOATS * 4;
+    static constexpr int STATIC_RESERVE = 4096;  // static smem + alignment slack
+    static constexpr int STAGES_FIT = (kSmemBudget - STATIC_RESERVE - COMB_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+    // dynamic smem: [1024 align slack][stages][comb]
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + COMB_BYTES;
+    static_assert(STAGES >= 2, "pipeline needs at least two stages");
+    static_assert(TW % 16 == 0, "a warp's token slice must be whole k16 steps");
+};
+
+// What the producer tells the consumers about the tile in a stage.
+struct StageDesc {
+    int64_t run_start;  // flat index of tile 0 of the (b, kvh) run
+    int b, kvh, n_valid, flags;
+    int n_b;            // tiles of the run
+    int pad;
+};
+
+// ----------------------------------------------------------------- the kernel
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+    decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v, DecodeArgs a) {
+    constexpr int S = C::STAGES;
+    constexpr int D = C::D;
+    extern __shared__ uint8_t dyn_smem[];
+    __shared__ int64_t scratch[C::THREADS];
+    __shared__ SpanStart ss;
+    __shared__ __align__(8) uint64_t full_bar[S];
+    __shared__ __align__(8) uint64_t empty_bar[S];
+    __shared__ __align__(8) uint64_t comb_bar;
+    __shared__ StageDesc desc[S];
+    __shared__ volatile int aborted;
+
+    uint8_t* stage_base = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+    float* comb = reinterpret_cast<float*>(stage_base + S * C::STAGE_BYTES);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), C::NC * 32);
+        }
+        mbar_init(smem_u32(&comb_bar), C::NC * 32);
+        aborted = 0;
+        fence_barrier_init();
+    }
+    find_span_start(a.seq_lens, a.B, a.hkv, a.max_blocks, a.block_size, a.num_parts, scratch,
+                    &ss, a.tile_base);  // ends with __syncthreads
+
+    // Sequences that own no tiles: length 0 gives zeros, an out-of-range length
+    // gives NaN and latches PGD_ERR_SEQ_LEN.  CTA b % P writes sequence b.
+    for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
+        const int L = a.seq_lens[b];
+        if (L != 0 && seq_len_ok(L, a.max_blocks, a.block_size)) continue;
+        if (L != 0 && threadIdx.x == 0) latch_error(a.err, PGD_ERR_SEQ_LEN);
+        const __nv_bfloat16 fill = __float2bfloat16_rn(L == 0 ? 0.f : NAN);
+        __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) + (int64_t)b * a.hq * D;
+        for (int i = threadIdx.x; i < a.hq * D; i += blockDim.x) ob[i] = fill;
+    }
+    if (ss.r0 >= ss.r1) return;
+    const int64_t r0 = ss.r0, r1 = ss.r1;
+    const int n_tiles = (int)(r1 - r0);
+    const int bs = a.block_size;
+
+    if (warp == C::NC) {
+        // ============================================================ producer
+        const int box_rows = bs < T ? bs : T;
+        const uint32_t box_bytes = (uint32_t)box_rows * 128u;
+        TileCursor cur = cursor_at(ss, a.seq_lens, a.hkv, a.max_blocks, bs);
+        const uint64_t policy = policy_evict_first();
+        // Block-id window: lane l holds block_table[win_b][win_lb + l]; the next
+        // 32 entries are loaded ahead into nxt_id so that walking a run meets
+        // the table's latency once per window, not once per tile.
+        int win_b = -1, win_lb = 0, win_id = -1, nxt_id = -1;
+        auto table_row = [&](int b, int lb) -> int {
+            const int idx = lb + lane;
+            return idx < a.max_blocks ? a.block_table[(int64_t)b * a.max_blocks + idx] : -1;
+        };
+        int issued = 0;  // stages armed with expect_tx
+        int L = a.seq_lens[cur.b];
+        int L_b = cur.b;
+        for (int it = 0; it < n_tiles; ++it) {
+            const int s = it % S;
+            const uint32_t ph = (uint32_t)(it / S) & 1u;
+            const int64_t x = r0 + it;
+            if (cur.b != L_b) {
+                L = a.seq_lens[cur.b];
+                L_b = cur.b;
+            }
+            const int tok0 = cur.i * T;
+            const int n_valid = min(T, L - tok0);
+            const int npg = bs < T ? (n_valid + bs - 1) / bs : 1;
+            const int lb0 = tok0 / bs;
+            const int slot0 = bs < T ? 0 : tok0 % bs;
+            if (cur.b != win_b || lb0 < win_lb || lb0 + npg > win_lb + 32) {
+                if (cur.b == win_b && lb0 == win_lb + 32) {
+                    win_id = nxt_id;
+                    win_lb += 32;
+                } else {
+                    win_b = cur.b;
+                    win_lb = lb0;
+                    win_id = table_row(win_b, win_lb);
+                }
+                nxt_id = table_row(win_b, win_lb + 32);
+            }
+            const int64_t phys = __shfl_sync(0xffffffffu, win_id, (lb0 - win_lb + lane) & 31);
+            const bool want = lane < npg;
+            const bool ok = want && phys >= 0 && phys < a.num_blocks;
+            const bool bad = __any_sync(0xffffffffu, want && !ok);
+            const int nok = __popc(__ballot_sync(0xffffffffu, ok));
+            const int flags =
+                segment_flags(x, cur.run_start, cur.n_b, r0, r1) | (bad ? kTileBad : 0);
+
+            if (!mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1u)) {
+                if (lane == 0) {
+                    latch_error(a.err, PGD_ERR_TIMEOUT);
+                    aborted = 1;
+                }
+                break;
+            }
+            if (aborted) break;
+            const uint32_t fb = smem_u32(&full_bar[s]);
+            if (lane == 0) {
+                desc[s] = StageDesc{cur.run_start, cur.b, cur.kvh, n_valid, flags, cur.n_b, 0};
+                mbar_arrive_expect_tx(fb, (uint32_t)nok * box_bytes * 2u * C::HALVES);
+                if (bad) latch_error(a.err, PGD_ERR_BLOCK_ID);
+            }
+            ++issued;
+            __syncwarp();
+            if (ok) {
+                const uint32_t st = smem_u32(stage_base + s * C::STAGE_BYTES);
+                const uint32_t row_off = (uint32_t)(lane * box_rows) * 128u;
+#pragma unroll
+                for (int h = 0; h < C::HALVES; ++h) {
+                    const int c1 = cur.kvh * C::HALVES + h;
+                    tma_load_4d(st + h * C::HALF_BYTES + row_off, &tmap_k, fb, 0, c1, slot0,
+                                (int)phys, policy);
+                    tma_load_4d(st + (C::HALVES + h) * C::HALF_BYTES + row_off, &tmap_v, fb, 0,
+                                c1, slot0, (int)phys, policy);
+                }
+            }
+            cursor_next(cur, a.seq_lens, a.B, a.hkv, a.max_blocks, bs);
+        }
+        // Do not leave while copies this CTA issued may still land.
+        if (lane == 0) {
+            const int first = issued > S ? issued - S : 0;
+            for (int it = first; it < issued; ++it) {
+                if (!mbar_wait(smem_u32(&full_bar[it % S]), (uint32_t)(it / S) & 1u)) break;
+            }
+        }
+        return;
+    }
+
+    // ================================================================ consumers
+    const int mt = warp / C::TG;
+    const int tg = warp % C::TG;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int tw0 = tg * C::TW;
+    const int G = a.group;
+    const int row0 = mt * 16 + gid;      // group row of accumulator rows c0,c1
+    const int row1 = row0 + 8;           // group row of c2,c3
+    const bool row0_ok = row0 < G;
+    const bool row1_ok = C::ROWS16 && row1 < G;
+
+    uint32_t qa[D / 16][4];
+    float o[D / 8][4];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    bool seg_bad = false;
+    uint32_t comb_phase = 0;
+
+    // Lane-dependent parts of the ldmatrix addresses.
+    const int lm_mi = lane >> 3, lm_i = lane & 7;
+
+    for (int it = 0; it < n_tiles; ++it) {
+        const int s = it % S;
+        const uint32_t ph = (uint32_t)(it / S) & 1u;
+        if (!mbar_wait(smem_u32(&full_bar[s]), ph)) {
+            if (lane == 0) {
+                latch_error(a.err, PGD_ERR_TIMEOUT);
+                aborted = 1;
+            }
+            break;
+        }
+        if (aborted) break;
+        const StageDesc dsc = desc[s];
+        uint8_t* st = stage_base + s * C::STAGE_BYTES;
+        const uint32_t st_u = smem_u32(st);
+
+        if (dsc.flags & kSegStart) {
+            // New piece: load this warp's query rows as mma A fragments.
+            const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q) +
+                                      ((int64_t)dsc.b * a.hq + (int64_t)dsc.kvh * G) * D;
+            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(qg + (int64_t)row0 * D);
+            const uint32_t* q1 = reinterpret_cast<const uint32_t*>(qg + (int64_t)row1 * D);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const int c = ks * 8 + tig;  // 32-bit word index of columns 16ks + 2 tig
+                qa[ks][0] = row0_ok ? __ldg(q0 + c) : 0u;
+                qa[ks][1] = row1_ok ? __ldg(q1 + c) : 0u;
+                qa[ks][2] = row0_ok ? __ldg(q0 + c + 4) : 0u;
+                qa[ks][3] = row1_ok ? __ldg(q1 + c + 4) : 0u;
+            }
+#pragma unroll
+            for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+            seg_bad = false;
+        }
+        seg_bad |= (dsc.flags & kTileBad) != 0;
+
+        const int n_valid = dsc.n_valid;
+        const bool active = tw0 < n_valid;
+        const bool zeroed = active && n_valid < tw0 + C::TW;
+        if (zeroed) {
+            // Rows past the sequence end are tail slots or stale data: zero V
+            // there so that 0 * (NaN or Inf) never reaches the accumulators.
+            const int z0 = n_valid;
+            const int nz = tw0 + C::TW - z0;
+            for (int idx = lane; idx < nz * 8 * C::HALVES; idx += 32) {
+                const int r = z0 + idx / (8 * C::HALVES);
+                const int rem = idx % (8 * C::HALVES);
+                const int h = rem / 8, ch = rem % 8;
+                *reinterpret_cast<uint4*>(st + (C::HALVES + h) * C::HALF_BYTES + r * 128 +
+                                          ch * 16) = make_uint4(0, 0, 0, 0);
+            }
+            __syncwarp();
+        }
+
+        if (active) {
+            // ---- S = q K^T over this warp's TW tokens
+            float sc[C::TW / 8][4];
+#pragma unroll
+            for (int j = 0; j < C::TW / 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const int h = ks / 4;
+                const int kc = (ks % 4) * 2 + (lm_mi & 1);
+#pragma unroll
+                for (int np = 0; np < C::TW / 16; ++np) {
+                    const int tok = tw0 + np * 16 + (lm_mi >> 1) * 8 + lm_i;
+                    const uint32_t addr =
+                        st_u + h * C::HALF_BYTES + tok * 128 + ((kc ^ (tok & 7)) << 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(addr, b0, b1, b2, b3);
+                    mma_bf16(sc[2 * np], qa[ks], b0, b1);
+                    mma_bf16(sc[2 * np + 1], qa[ks], b2, b3);
+                }
+            }
+            // ---- mask, scale to base-2 units, running max
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < C::TW / 8; ++j) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int tok = tw0 + j * 8 + tig * 2 + e;
+                    const bool v = tok < n_valid;
+                    sc[j][e] = v ? sc[j][e] * a.scale_log2 : -INFINITY;
+                    sc[j][2 + e] = v ? sc[j][2 + e] * a.scale_log2 : -INFINITY;
+                    mx0 = fmaxf(mx0, sc[j][e]);
+                    mx1 = fmaxf(mx1, sc[j][2 + e]);
+                }
+            }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            if (C::ROWS16) {
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            }
+            const float mn0 = fmaxf(m0, mx0);
+            const float mn1 = C::ROWS16 ? fmaxf(m1, mx1) : 0.f;
+            const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+            const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float alpha0 = fast_exp2(m0 - base0);
+            const float alpha1 = C::ROWS16 ? fast_exp2(m1 - base1) : 1.f;
+            m0 = mn0;
+            if (C::ROWS16) m1 = mn1;
+            float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+            for (int j = 0; j < C::TW / 8; ++j) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    sc[j][e] = fast_exp2(sc[j][e] - base0);
+                    ps0 += sc[j][e];
+                    if (C::ROWS16) {
+                        sc[j][2 + e] = fast_exp2(sc[j][2 + e] - base1);
+                        ps1 += sc[j][2 + e];
+                    } else {
+                        sc[j][2 + e] = 0.f;
+                    }
+                }
+            }
+            l0 = l0 * alpha0 + ps0;
+            if (C::ROWS16) l1 = l1 * alpha1 + ps1;
+            if (__any_sync(0xffffffffu, alpha0 != 1.f || alpha1 != 1.f)) {
+#pragma unroll
+                for (int n = 0; n < D / 8; ++n) {
+                    o[n][0] *= alpha0;
+                    o[n][1] *= alpha0;
+                    o[n][2] *= alpha1;
+                    o[n][3] *= alpha1;
+                }
+            }
+            // ---- O += P V
+#pragma unroll
+            for (int kk = 0; kk < C::TW / 16; ++kk) {
+                uint32_t pa[4];
+                pa[0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
+                pa[1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
+                pa[2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+                pa[3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+                const int tok = tw0 + kk * 16 + (lm_mi & 1) * 8 + lm_i;
+#pragma unroll
+                for (int dp = 0; dp < D / 16; ++dp) {
+                    const int h = dp / 4;
+                    const int vc = (dp % 4) * 2 + (lm_mi >> 1);
+                    const uint32_t addr = st_u + (C::HALVES + h) * C::HALF_BYTES + tok * 128 +
+                                          ((vc ^ (tok & 7)) << 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(addr, b0, b1, b2, b3);
+                    mma_bf16(o[2 * dp], pa, b0, b1);
+                    mma_bf16(o[2 * dp + 1], pa, b2, b3);
+                }
+            }
+        }
+
+        // ---- release the stage
+        if (zeroed) fence_proxy_async();
+        __syncwarp();
+        mbar_arrive(smem_u32(&empty_bar[s]));
+
+        if (!(dsc.flags & kSegEnd)) continue;
+
+        // ================================================ end of a piece: combine
+        float lt0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
+        lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
+        float lt1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
+        lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
+        if (C::TG > 1) {
+            constexpr int RS = D + 2;  // row stride: D outputs, then m and l
+            if (tg > 0) {
+                float* cb = comb + ((tg - 1) * C::MT + mt) * C::ROWS * RS;
+#pragma unroll
+                for (int n = 0; n < D / 8; ++n) {
+                    *reinterpret_cast<float2*>(cb + gid * RS + n * 8 + tig * 2) =
+                        make_float2(o[n][0], o[n][1]);
+                    if (C::ROWS16)
+                        *reinterpret_cast<float2*>(cb + (gid + 8) * RS + n * 8 + tig * 2) =
+                            make_float2(o[n][2], o[n][3]);
+                }
+                if (tig == 0) {
+                    cb[gid * RS + D] = m0;
+                    cb[gid * RS + D + 1] = lt0;
+                    if (C::ROWS16) {
+                        cb[(gid + 8) * RS + D] = m1;
+                        cb[(gid + 8) * RS + D + 1] = lt1;
+                    }
+                }
+            }
+            mbar_arrive(smem_u32(&comb_bar));
+            if (!mbar_wait(smem_u32(&comb_bar), comb_phase)) {
+                if (lane == 0) {
+                    latch_error(a.err, PGD_ERR_TIMEOUT);
+                    aborted = 1;
+                }
+                break;
+            }
+            comb_phase ^= 1u;
+            if (tg == 0) {
+#pragma unroll 1
+                for (int t2 = 1; t2 < C::TG; ++t2) {
+                    const float* cb = comb + ((t2 - 1) * C::MT + mt) * C::ROWS * RS;
+                    const float om0 = cb[gid * RS + D], ol0 = cb[gid * RS + D + 1];
+                    const float nm0 = fmaxf(m0, om0);
+                    const float nb0 = nm0 == -INFINITY ? 0.f : nm0;
+                    const float sa0 = fast_exp2(m0 - nb0), sb0 = fast_exp2(om0 - nb0);
+                    m0 = nm0;
+                    lt0 = lt0 * sa0 + ol0 * sb0;
+                    float sa1 = 1.f, sb1 = 0.f;
+                    if (C::ROWS16) {
+                        const float om1 = cb[(gid + 8) * RS + D], ol1 = cb[(gid + 8) * RS + D + 1];
+                        const float nm1 = fmaxf(m1, om1);
+                        const float nb1 = nm1 == -INFINITY ? 0.f : nm1;
+                        sa1 = fast_exp2(m1 - nb1);
+                        sb1 = fast_exp2(om1 - nb1);
+                        m1 = nm1;
+                        lt1 = lt1 * sa1 + ol1 * sb1;
+                    }
+#pragma unroll
+                    for (int n = 0; n < D / 8; ++n) {
+                        const float2 u = *reinterpret_cast<const float2*>(cb + gid * RS + n * 8 +
+                                                                          tig * 2);
+                        o[n][0] = o[n][0] * sa0 + u.x * sb0;
+                        o[n][1] = o[n][1] * sa0 + u.y * sb0;
+                        if (C::ROWS16) {
+                            const float2 w = *reinterpret_cast<const float2*>(
+                                cb + (gid + 8) * RS + n * 8 + tig * 2);
+                            o[n][2] = o[n][2] * sa1 + w.x * sb1;
+                            o[n][3] = o[n][3] * sa1 + w.y * sb1;
+                        }
+                    }
+                }
+            }
+            mbar_arrive(smem_u32(&comb_bar));
+            if (!mbar_wait(smem_u32(&comb_bar), comb_phase)) {
+                if (lane == 0) {
+                    latch_error(a.err, PGD_ERR_TIMEOUT);
+                    aborted = 1;
+                }
+                break;
+            }
+            comb_phase ^= 1u;
+        }
+        if (tg != 0) continue;
+
+        // ---- write: whole run -> out (bf16); split run -> partial (fp32) + lse
+        const float inv0 = seg_bad ? NAN : 1.f / lt0;
+        const float inv1 = seg_bad ? NAN : 1.f / lt1;
+        if (!(dsc.flags & kSegPartial)) {
+            __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) +
+                                ((int64_t)dsc.b * a.hq + (int64_t)dsc.kvh * G) * D;
+#pragma unroll
+            for (int n = 0; n < D / 8; ++n) {
+                if (row0_ok)
+                    *reinterpret_cast<uint32_t*>(ob + (int64_t)row0 * D + n * 8 + tig * 2) =
+                        pack_bf16(o[n][0] * inv0, o[n][1] * inv0);
+                if (row1_ok)
+                    *reinterpret_cast<uint32_t*>(ob + (int64_t)row1 * D + n * 8 + tig * 2) =
+                        pack_bf16(o[n][2] * inv1, o[n][3] * inv1);
+            }
+        } else {
+            const int64_t slot = (int64_t)blockIdx.x * 2 + ((dsc.flags & kSegSlot1) ? 1 : 0);
+            float* po = a.part_o + slot * G * D;
+#pragma unroll
+            for (int n = 0; n < D / 8; ++n) {
+                if (row0_ok)
+                    *reinterpret_cast<float2*>(po + (int64_t)row0 * D + n * 8 + tig * 2) =
+                        make_float2(o[n][0] * inv0, o[n][1] * inv0);
+                if (row1_ok)
+                    *reinterpret_cast<float2*>(po + (int64_t)row1 * D + n * 8 + tig * 2) =
+                        make_float2(o[n][2] * inv1, o[n][3] * inv1);
+            }
+            if (tig == 0) {
+                if (row0_ok) a.part_lse[slot * G + row0] = seg_bad ? 0.f : m0 + fast_log2(lt0);
+                if (row1_ok) a.part_lse[slot * G + row1] = seg_bad ? 0.f : m1 + fast_log2(lt1);
+            }
+            // Publish the partial, count it; the warp that brings the run's
+            // count to its number of pieces merges them (log-sum-exp) and
+            // resets the counter, so no second kernel and no waiting.
+            __threadfence();
+            __syncwarp();
+            const int64_t t0 = dsc.run_start;
+            const int64_t N = ss.n_total, P = a.num_parts;
+            const int64_t c0 = span_owner(t0, N, P), c1 = span_owner(t0 + dsc.n_b - 1, N, P);
+            int last = 0;
+            if (lane == 0) {
+                int pieces = (int)(c1 - c0 + 1);
+                if (P > N) {
+                    pieces = 0;
+                    for (int64_t c = c0; c <= c1; ++c)
+                        pieces += span_begin(c, N, P) != span_begin(c + 1, N, P);
+                }
+                int* ctr = a.counters + ((int64_t)dsc.b * a.hkv + dsc.kvh) * C::MT + mt;
+                last = atomicAdd(ctr, 1) == pieces - 1;
+                if (last) atomicExch(ctr, 0);
+            }
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (!last) continue;
+            __threadfence();
+            float M0 = -INFINITY, M1 = -INFINITY, W0 = 0.f, W1 = 0.f;
+#pragma unroll
+            for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+            for (int64_t c = c0; c <= c1; ++c) {
+                const int64_t sb = span_begin(c, N, P);
+                if (sb == span_begin(c + 1, N, P)) continue;
+                const int64_t sl = c * 2 + (sb < t0 ? 1 : 0);
+                const float* pc = a.part_o + sl * G * D;
+                const float* lc = a.part_lse + sl * G;
+                const float e0 = row0_ok ? __ldcg(lc + row0) : 0.f;
+                const float e1 = row1_ok ? __ldcg(lc + row1) : 0.f;
+                const float n0 = fmaxf(M0, e0), n1 = fmaxf(M1, e1);
+                const float a0 = fast_exp2(M0 - n0), b0 = fast_exp2(e0 - n0);
+                const float a1 = fast_exp2(M1 - n1), b1 = fast_exp2(e1 - n1);
+                M0 = n0;
+                M1 = n1;
+                W0 = W0 * a0 + b0;
+                W1 = W1 * a1 + b1;
+#pragma unroll
+                for (int n = 0; n < D / 8; ++n) {
+                    if (row0_ok) {
+                        const float2 u = __ldcg(reinterpret_cast<const float2*>(
+                            pc + (int64_t)row0 * D + n * 8 + tig * 2));
+                        o[n][0] = o[n][0] * a0 + u.x * b0;
+                        o[n][1] = o[n][1] * a0 + u.y * b0;
+                    }
+                    if (row1_ok) {
+                        const float2 u = __ldcg(reinterpret_cast<const float2*>(
+                            pc + (int64_t)row1 * D + n * 8 + tig * 2));
+                        o[n][2] = o[n][2] * a1 + u.x * b1;
+                        o[n][3] = o[n][3] * a1 + u.y * b1;
+                    }
+                }
+            }
+            const float w0 = 1.f / W0, w1 = 1.f / W1;
+            __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) +
+                                ((int64_t)dsc.b * a.hq + (int64_t)dsc.kvh * G) * D;
+#pragma unroll
+            for (int n = 0; n < D / 8; ++n) {
+                if (row0_ok)
+                    *reinterpret_cast<uint32_t*>(ob + (int64_t)row0 * D + n * 8 + tig * 2) =
+                        pack_bf16(o[n][0] * w0, o[n][1] * w0);
+                if (row1_ok)
+                    *reinterpret_cast<uint32_t*>(ob + (int64_t)row1 * D + n * 8 + tig * 2) =
+                        pack_bf16(o[n][2] * w1, o[n][3] * w1);
+            }
+        }
+    }
+}
+
+template <class C>
+cudaError_t launch_cfg(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
+    static bool attr_done = false;  // per instantiation; harmless if raced
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(decode_tma_kernel<C>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    decode_tma_kernel<C><<<a.num_parts, C::THREADS, C::SMEM_BYTES, s>>>(p.tmap_k, p.tmap_v, a);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
+    const int G = a.group;
+    if (G <= 8) return launch_cfg<Cfg<D, 1, 4, false>>(a, p, s);
+    if (G <= 16) return launch_cfg<Cfg<D, 1, 4, true>>(a, p, s);
+    if (G <= 32) return launch_cfg<Cfg<D, 2, 2, true>>(a, p, s);
+    if (G <= 48) return launch_cfg<Cfg<D, 3, 2, true>>(a, p, s);
+    return launch_cfg<Cfg<D, 4, 2, true>>(a, p, s);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_tma(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
+    if (a.d == 64) return launch_d<64>(a, p, s);
+    return launch_d<128>(a, p, s);
+}
+
+}  // namespace pgd

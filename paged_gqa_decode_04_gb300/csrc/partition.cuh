@@ -1,0 +1,170 @@
+// Device-side work partition shared by the decode kernels and the merge kernel.
+//
+// The KV work of one call is the sequence of 64-token tiles of every
+// (sequence b, KV head kvh) pair, in the order b-major, then kvh, then tile:
+//
+//     flat(b, kvh, i) = tile_base[b] + kvh * n_b + i,   n_b = ceil(L_b / 64)
+//
+// CTA c of P takes the span [floor(c N / P), floor((c+1) N / P)) of the N
+// tiles, so every CTA gets the same amount of KV bytes (to one tile) whatever
+// the length mix.  A (b, kvh) run that lies inside one span is finished by that
+// CTA; a run cut by span boundaries leaves one partial result per piece, in
+// slot 0 of a CTA (the piece that starts the CTA's span) or slot 1 (the piece
+// that ends it), and the merge kernel combines them with a log-sum-exp.
+// This is the split-KV scheme of FlashDecoding ("Modern LLM Inference ...",
+// section 8.3 lists FlashDecoding kernels) with the splits placed by work
+// rather than per sequence.
+#pragma once
+
+#include <stdint.h>
+
+#include "pgd_internal.h"
+
+namespace pgd {
+
+__device__ __forceinline__ bool seq_len_ok(int L, int max_blocks, int block_size) {
+    return L >= 0 && (int64_t)L <= (int64_t)max_blocks * block_size;
+}
+
+__device__ __forceinline__ int tiles_of(int L, int max_blocks, int block_size) {
+    return seq_len_ok(L, max_blocks, block_size) ? (L + kTileTokens - 1) / kTileTokens : 0;
+}
+
+__device__ __forceinline__ int64_t span_begin(int64_t c, int64_t N, int64_t P) {
+    return (c * N) / P;
+}
+
+// CTA whose span holds flat tile x (N > 0).  When P > N some spans are empty;
+// the owners of consecutive tiles can then skip CTAs, which own nothing.
+__device__ __forceinline__ int64_t span_owner(int64_t x, int64_t N, int64_t P) {
+    return ((x + 1) * P - 1) / N;
+}
+
+__device__ __forceinline__ void latch_error(int* err, int code) {
+    atomicCAS(err, 0, code);
+}
+
+// Start of this CTA's span, found with a block-wide scan over the sequences.
+struct SpanStart {
+    int64_t n_total;   // N
+    int64_t r0, r1;    // this CTA's span
+    int b;             // sequence holding r0 (valid when r0 < r1)
+    int64_t b_base;    // tile_base[b]
+};
+
+// Every thread of the block must call this.  `scratch` is >= blockDim.x int64
+// of shared memory, `out` a shared SpanStart.  CTA 0 also writes
+// tile_base[0..B] to global memory for the merge kernel.
+__device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int B, int hkv,
+                                       int max_blocks, int block_size, int64_t parts,
+                                       int64_t* scratch, SpanStart* out,
+                                       int64_t* __restrict__ tile_base_out) {
+    const int nt = blockDim.x;
+    const int tid = threadIdx.x;
+    const int per = (B + nt - 1) / nt;
+    const int b_lo = min(B, tid * per);
+    const int b_hi = min(B, b_lo + per);
+    int64_t local = 0;
+    for (int b = b_lo; b < b_hi; ++b) local += (int64_t)hkv * tiles_of(seq_lens[b], max_blocks, block_size);
+    scratch[tid] = local;
+    __syncthreads();
+    if (tid == 0) {  // exclusive scan of per-thread sums (nt is small)
+        int64_t run = 0;
+        for (int i = 0; i < nt; ++i) {
+            int64_t v = scratch[i];
+            scratch[i] = run;
+            run += v;
+        }
+        out->n_total = run;
+        out->r0 = span_begin(blockIdx.x, run, parts);
+        out->r1 = span_begin(blockIdx.x + 1, run, parts);
+        out->b = -1;
+        out->b_base = 0;
+    }
+    __syncthreads();
+    const int64_t r0 = out->r0;
+    int64_t run = scratch[tid];
+    for (int b = b_lo; b < b_hi; ++b) {
+        int64_t n = (int64_t)hkv * tiles_of(seq_lens[b], max_blocks, block_size);
+        if (blockIdx.x == 0) tile_base_out[b] = run;
+        if (r0 >= run && r0 < run + n) {
+            out->b = b;
+            out->b_base = run;
+        }
+        run += n;
+    }
+    if (blockIdx.x == 0 && tid == nt - 1) tile_base_out[B] = out->n_total;
+    __syncthreads();
+}
+
+// Cursor over the (b, kvh, tile) sequence of one span.
+struct TileCursor {
+    int b, kvh, i, n_b;      // current position: tile i of n_b of (b, kvh)
+    int64_t run_start;       // flat index of tile 0 of (b, kvh)
+};
+
+__device__ inline TileCursor cursor_at(const SpanStart& s, const int32_t* seq_lens, int hkv,
+                                       int max_blocks, int block_size) {
+    TileCursor c;
+    c.b = s.b;
+    c.n_b = tiles_of(seq_lens[s.b], max_blocks, block_size);
+    int64_t off = s.r0 - s.b_base;
+    c.kvh = (int)(off / c.n_b);
+    c.i = (int)(off % c.n_b);
+    c.run_start = s.b_base + (int64_t)c.kvh * c.n_b;
+    return c;
+}
+
+__device__ inline void cursor_next(TileCursor& c, const int32_t* seq_lens, int B, int hkv,
+                                   int max_blocks, int block_size) {
+    if (++c.i < c.n_b) return;
+    c.run_start += c.n_b;
+    c.i = 0;
+    if (++c.kvh < hkv) return;
+    c.kvh = 0;
+    int nb = 0;
+    while (++c.b < B) {
+        nb = tiles_of(seq_lens[c.b], max_blocks, block_size);
+        if (nb > 0) break;
+    }
+    c.n_b = nb;
+}
+
+// Segment flags for the piece of (b, kvh) a CTA holds.
+enum : int {
+    kSegStart = 1,    // first tile of this CTA's piece of (b, kvh)
+    kSegEnd = 2,      // last tile of the piece
+    kSegPartial = 4,  // piece is not the whole run: write a partial result
+    kSegSlot1 = 8,    // partial goes to slot 1 (else slot 0)
+    kTileBad = 16     // a block id of this tile was out of range
+};
+
+// Flags of tile x of run [run_start, run_start + n_b) inside span [r0, r1).
+__device__ __forceinline__ int segment_flags(int64_t x, int64_t run_start, int n_b, int64_t r0,
+                                             int64_t r1) {
+    const int64_t run_end = run_start + n_b;
+    const int64_t s0 = run_start > r0 ? run_start : r0;
+    const int64_t s1 = run_end < r1 ? run_end : r1;
+    int f = 0;
+    if (x == s0) f |= kSegStart;
+    if (x == s1 - 1) f |= kSegEnd;
+    if (s0 != run_start || s1 != run_end) {
+        f |= kSegPartial;
+        if (s0 != r0) f |= kSegSlot1;
+    }
+    return f;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float fast_log2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+}  // namespace pgd

@@ -1,0 +1,72 @@
+// Internal declarations shared by the C-ABI layer (api.cpp) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "paged_gqa.h"
+
+namespace pgd {
+
+// Tokens per tile: the unit of work that is split across CTAs and the unit a
+// pipeline stage holds.
+constexpr int kTileTokens = 64;
+
+// Largest query-head group the kernels handle (4 m16 row tiles).
+constexpr int kMaxGroup = 64;
+
+struct Pool {
+    const void* k;
+    const void* v;
+    int64_t num_blocks;
+    int block_size;
+    int hkv;
+    int d;
+    int dtype;
+    int device;
+    int num_sms;
+    int* err;              // device error word (latched pgd_status)
+    bool has_tmap;         // bfloat16 TMA descriptors encoded
+    CUtensorMap tmap_k;    // 4-D view [d_lo 64, Hkv*D/64, block_size, num_blocks]
+    CUtensorMap tmap_v;
+};
+
+// Everything a decode launch needs, resolved on the host.
+struct DecodeArgs {
+    const void* q;
+    const void* k_pool;
+    const void* v_pool;
+    void* out;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    int B;
+    int hq;
+    int hkv;
+    int group;             // G = Hq / Hkv
+    int d;
+    int block_size;
+    int max_blocks;
+    int64_t num_blocks;
+    float scale_log2;      // scale * log2(e): logits kept in base-2 units
+    int num_parts;         // CTAs of the decode grid (spans of the tile sequence)
+    int* err;
+    // workspace carve-up
+    int* counters;         // [B][Hkv][m-tiles] pieces finished per split run (kept zero between calls)
+    int64_t* tile_base;    // [B + 1] first flat tile of each sequence
+    float* part_o;         // [num_parts][2][group][d] normalised partial outputs
+    float* part_lse;       // [num_parts][2][group]    partial log2-sum-exp
+};
+
+// Workspace layout for (B, G, D, parts); returns total bytes and fills offsets.
+struct WorkspaceLayout {
+    size_t counters_off, tile_base_off, part_lse_off, part_o_off, total;
+};
+WorkspaceLayout workspace_layout(int B, int hkv, int group, int d, int parts);
+
+// Kernel launchers (return a cudaError_t from the launch).
+cudaError_t launch_decode_simple(const DecodeArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_decode_tma(const DecodeArgs& a, const Pool& p, cudaStream_t s);
+cudaError_t launch_merge(const DecodeArgs& a, int dtype, cudaStream_t s);
+
+}  // namespace pgd

@@ -1,0 +1,52 @@
+"""Helpers for the GPU parity tests: run the CUDA path, run the oracle, compare."""
+import numpy as np
+import torch
+
+import gen
+import oracle
+import paged_gqa_decode_04_gb300 as pgd
+
+# Tolerances against the float64 oracle (bf16 KV with fp32 accumulation; fp32 KV).
+BF16_MAX, BF16_MEAN = 1e-2, 1e-3
+F32_MAX, F32_MEAN = 1e-5, 1e-5
+
+
+def tol(dtype):
+    return (F32_MAX, F32_MEAN) if dtype in ("f32", torch.float32) else (BF16_MAX, BF16_MEAN)
+
+
+def run_cuda(w, num_splits=0, stream=None, check_error=True):
+    pool = pgd.PagedKVPool(w.k_pool, w.v_pool)
+    try:
+        out = pgd.paged_gqa_decode(pool, w.q, w.block_table, w.seq_lens, w.scale,
+                                   num_splits=num_splits, stream=stream)
+        status = pgd.paged_gqa_get_error(pool, stream)
+    finally:
+        pool.close()
+    if check_error:
+        assert status == 0, pgd.strerror(status)
+    return out, status
+
+
+def host(t):
+    return gen.to_numpy_bits(t)
+
+
+def run_oracle(w, table=None, lens=None):
+    table = w.table_np if table is None else table
+    lens = w.lens_np if lens is None else lens
+    return oracle.decode_f64(host(w.q), host(w.k_pool), host(w.v_pool), table, lens, w.scale)
+
+
+def errors(got, want):
+    g = got.detach().float().cpu().numpy().astype(np.float64)
+    e = np.abs(g - want)
+    return g, float(e.max()), float(e.mean())
+
+
+def assert_close(got, want, dtype, what=""):
+    g, emax, emean = errors(got, want)
+    tmax, tmean = tol(dtype)
+    assert np.isfinite(g).all(), "%s: non-finite output" % what
+    assert emax <= tmax and emean <= tmean, "%s: max %.3g mean %.3g" % (what, emax, emean)
+    return emax, emean

@@ -1,0 +1,72 @@
+"""The C ABI on a machine without a GPU: the library loads, exports every
+function the header declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+
+import pytest
+
+import paged_gqa_decode_04_gb300 as pgd
+from paged_gqa_decode_04_gb300 import _lib
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    return _lib.load()
+
+
+def test_exports_every_declared_function(lib):
+    names = _lib.declared_functions()
+    assert set(names) >= {"paged_kv_pool_create", "paged_kv_pool_destroy", "paged_gqa_decode",
+                          "paged_gqa_workspace_size", "paged_gqa_get_error",
+                          "paged_gqa_strerror", "paged_gqa_auto_splits"}
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_strerror_names_every_status(lib):
+    for code, name in _lib.STATUS_NAMES.items():
+        s = pgd.strerror(code)
+        assert s and s != "unknown status", (code, name)
+    assert pgd.strerror(12345) == "unknown status"
+
+
+def _create(lib, k, v, nb=10, bs=16, hkv=8, d=128, dtype=1):
+    h = ctypes.c_void_p()
+    rc = lib.paged_kv_pool_create(ctypes.byref(h), k, v, nb, bs, hkv, d, dtype)
+    return rc, h
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(k=None, v=None), _lib.PGD_ERR_ARG),
+    (dict(k=256, v=256, nb=0), _lib.PGD_ERR_ARG),
+    (dict(k=256, v=256, hkv=0), _lib.PGD_ERR_ARG),
+    (dict(k=256, v=256, d=96), _lib.PGD_ERR_SHAPE),
+    (dict(k=256, v=256, bs=12), _lib.PGD_ERR_SHAPE),      # bf16 needs a power of two
+    (dict(k=256, v=256, bs=4), _lib.PGD_ERR_SHAPE),       # bf16 needs >= 8
+    (dict(k=256, v=256, bs=2048, dtype=0), _lib.PGD_ERR_SHAPE),
+    (dict(k=256, v=256, dtype=7), _lib.PGD_ERR_DTYPE),
+    (dict(k=264 + 1, v=256), _lib.PGD_ERR_ALIGN),
+])
+def test_pool_create_rejects(lib, args, code):
+    rc, h = _create(lib, **args)
+    assert rc == code
+    assert h.value is None
+
+
+def test_null_handles_rejected(lib):
+    n = ctypes.c_size_t()
+    assert lib.paged_gqa_workspace_size(None, 1, 8, 0, ctypes.byref(n)) == _lib.PGD_ERR_ARG
+    assert lib.paged_gqa_decode(None, None, 1, 8, None, 1, None, 1.0, None, None, 0, 0,
+                                None) == _lib.PGD_ERR_ARG
+    assert lib.paged_gqa_get_error(None, None) == _lib.PGD_ERR_ARG
+    assert lib.paged_kv_pool_destroy(None) == _lib.PGD_OK
+    k = ctypes.c_int()
+    assert lib.paged_gqa_auto_splits(None, ctypes.byref(k)) == _lib.PGD_ERR_ARG
+
+
+def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        _lib.load(str(tmp_path / "missing.so"))

@@ -28,3 +28,27 @@ def test_oracle_reproduces_stored_answer():
     got, rc = oracle.decode_f64(q, k, v, t, L, scale)
     assert rc == 0
     assert np.array_equal(got, want)
+
+
+def test_page_numbers_pin_host_accounting():
+    from paged_gqa_decode_04_gb300 import accounting as acc
+
+    with open(os.path.join(HERE, "golden", "pages_numbers.json")) as f:
+        entries = {e["id"]: e for e in json.load(f)["entries"]}
+    e = entries["contiguous_reservation_waste"]
+    assert acc.contiguous_waste(e["reserved_tokens"], e["generated_tokens"]) == e["wasted_slots"]
+    e = entries["expected_vs_generated_waste"]
+    assert acc.contiguous_waste(e["reserved_tokens"], e["generated_tokens"]) == e["wasted_slots"]
+    e = entries["gqa_reduction_factor"]
+    assert acc.gqa_reduction_factor(e["query_heads"], e["kv_heads"]) == e["reduction_factor"]
+    # the same factor shows up in the algorithmic KV bytes of a step
+    lens = [100, 2000, 37]
+    mha = acc.algorithmic_bytes(lens, 40, 40, 128, 16, 2) - 2 * 3 * 40 * 128 * 2
+    gqa = acc.algorithmic_bytes(lens, 40, 8, 128, 16, 2) - 2 * 3 * 40 * 128 * 2
+    pages_words = 4 * (3 + sum(-(-L // 16) for L in lens))
+    assert (mha - pages_words) == e["reduction_factor"] * (gqa - pages_words)
+    e = entries["default_block_tokens"]
+    # with paging the waste of the 2048-slot example drops below one block
+    assert acc.paged_waste(10, e["block_size"]) == 6 < e["block_size"]
+    e = entries["selective_batching_flatten"]
+    assert acc.flattened_tokens(e["lengths"]) == e["flattened_tokens"]
