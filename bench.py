@@ -159,6 +159,16 @@ def max_over_ranks(x, world, device):
     return float(t.item())
 
 
+def replica_seed(config, rank):
+    """Each rank runs its own replica of the workload, drawn with seed + rank."""
+    return gen.CONFIGS[config]["seed"] + rank
+
+
+def whole_job_gbs(nbytes, t_ms, world):
+    """Bytes all ranks moved (each its own replica) over the slowest rank's time."""
+    return world * nbytes / (t_ms * 1e-3) / 1e9
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -229,7 +239,7 @@ def run_ours(args, world, rank, local):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = gen.make(args.config, device=dev, seed=gen.CONFIGS[args.config]["seed"] + rank)
+    w = gen.make(args.config, device=dev, seed=replica_seed(args.config, rank))
     elt = accounting.ELT[w.dtype]
     nbytes = accounting.algorithmic_bytes(w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt)
     pool = pgd.PagedKVPool(w.k_pool, w.v_pool)
@@ -321,7 +331,7 @@ def run_ours(args, world, rank, local):
     if rank != 0:
         return
     peak, peak_src = peak_hbm()
-    value = world * nbytes / (t_ms * 1e-3) / 1e9
+    value = whole_job_gbs(nbytes, t_ms, world)
     per_gpu = nbytes / (t_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,

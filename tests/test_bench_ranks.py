@@ -1,0 +1,54 @@
+"""The benchmark's multi-rank host logic on CPU with gloo, world size 2:
+rendezvous, barrier, max-over-ranks timing, distinct per-rank workloads and the
+whole-job value.  (Every box here has one GPU; the GPU ranks run the same code
+over NCCL.)"""
+import os
+import socket
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, out_dir):
+    os.environ.update({"RANK": str(rank), "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank),
+                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    import bench
+    import gen
+
+    w_, r_, l_ = bench.dist_setup()
+    assert (w_, r_) == (world, rank)
+    t = bench.max_over_ranks(1.0 + rank, world, torch.device("cpu"))
+    bench.barrier(world)
+    seed = bench.replica_seed("llama3_8b", rank)
+    wl = gen.make("llama3_8b", B=4, lens=("uniform", 1, 64), max_len=64, seed=seed)
+    with open(os.path.join(out_dir, "r%d.txt" % rank), "w") as f:
+        f.write("%r %d %s\n" % (t, seed, ",".join(map(str, wl.lens_np.tolist()))))
+    import torch.distributed as dist
+
+    dist.destroy_process_group()
+
+
+@pytest.mark.timeout(120)
+def test_two_gloo_ranks(tmp_path):
+    world = 2
+    mp.start_processes(_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world,
+                       join=True, start_method="spawn")
+    rows = [open(tmp_path / ("r%d.txt" % r)).read().split() for r in range(world)]
+    assert all(float(r[0]) == 2.0 for r in rows)         # max over ranks
+    assert rows[0][1] != rows[1][1]                       # distinct replica seeds
+    assert rows[0][2] != rows[1][2]                       # hence distinct workloads
+
+
+def test_whole_job_value():
+    import bench
+
+    assert bench.whole_job_gbs(nbytes=1e9, t_ms=2.0, world=4) == pytest.approx(2000.0)
