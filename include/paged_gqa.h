@@ -76,7 +76,8 @@ enum pgd_status {
     PGD_ERR_BLOCK_ID = 7,    /* device: a block id outside [0, num_blocks) (latched) */
     PGD_ERR_SEQ_LEN = 8,     /* device: a length outside [0, max_blocks*block_size] (latched) */
     PGD_ERR_UNSUPPORTED = 9, /* valid request this build does not implement */
-    PGD_ERR_TIMEOUT = 10     /* device: a pipeline wait gave up (latched) */
+    PGD_ERR_TIMEOUT = 10,    /* device: a pipeline wait gave up (latched) */
+    PGD_ERR_TOO_LARGE = 11   /* paged_gqa_decode_noalloc: scratch need above its fixed size */
 };
 
 /*
@@ -143,6 +144,33 @@ int paged_gqa_auto_splits(pgd_pool_t pool, int *num_splits);
 
 /* Static, human-readable name of a pgd_status. */
 const char *paged_gqa_strerror(int status);
+
+/*
+ * paged_gqa_decode without a workspace argument, for callers that cannot
+ * allocate device memory: a plugin inside a host runtime that owns all device
+ * memory and offers it no allocator, or a latency-critical path that must not
+ * call cudaMalloc / cudaFree because they can synchronise the device.  (The
+ * pages describe no such entry point; it is a property of this library.)
+ *
+ * Same arguments, semantics and errors as paged_gqa_decode, minus workspace.
+ * The split-KV scratch is a fixed array of paged_gqa_noalloc_scratch_bytes()
+ * bytes (16 MiB) of static device memory in this library, reserved on every
+ * device that loads it until the process exits.  Requests whose workspace
+ * (paged_gqa_workspace_size) exceeds that return PGD_ERR_TOO_LARGE before
+ * anything is enqueued.  Nothing is allocated: the first call on a device
+ * looks up the array's device address with that device made current (make
+ * that first call before any stream capture), and every call clears the
+ * array's counters with cudaMemsetAsync on `stream` before the kernel.
+ * All calls share the one array: calls that may overlap on the GPU (on
+ * different streams, or from several threads) race on it and must be
+ * serialised by the caller.
+ */
+int paged_gqa_decode_noalloc(pgd_pool_t pool, const void *q, int B, int Hq,
+                             const int32_t *block_table, int max_blocks, const int32_t *seq_lens,
+                             float scale, void *out, int num_splits, void *stream);
+
+/* Size in bytes of the fixed scratch array paged_gqa_decode_noalloc uses. */
+size_t paged_gqa_noalloc_scratch_bytes(void);
 
 #ifdef __cplusplus
 }

@@ -16,7 +16,8 @@ from ._lib import PagedGQAError, STATUS_NAMES, strerror  # noqa: F401
 __all__ = [
     "PagedKVPool", "PagedGQAError", "paged_kv_pool_create", "paged_kv_pool_destroy",
     "paged_gqa_workspace_size", "paged_gqa_decode", "paged_gqa_get_error",
-    "paged_gqa_auto_splits", "strerror", "decode",
+    "paged_gqa_auto_splits", "paged_gqa_decode_noalloc", "paged_gqa_noalloc_scratch_bytes",
+    "strerror", "decode",
 ]
 
 _DTYPES = {torch.float32: _lib.PGD_F32, torch.bfloat16: _lib.PGD_BF16}
@@ -142,6 +143,29 @@ def paged_gqa_decode(pool, q, block_table, seq_lens, scale, out=None, workspace=
                                 out.data_ptr(), workspace.data_ptr(), workspace.numel(),
                                 int(num_splits), _stream_handle(stream)), "paged_gqa_decode")
     return out
+
+
+def paged_gqa_decode_noalloc(pool, q, block_table, seq_lens, scale, out, num_splits=0,
+                             stream=None):
+    """paged_gqa_decode for callers that cannot allocate device memory.
+
+    No workspace: the split-KV scratch is the library's fixed static device
+    array (paged_gqa_noalloc_scratch_bytes()), shared by every call, so calls
+    that may overlap on the GPU must be serialised by the caller.  `out` must
+    be given (nothing is allocated here either).  Raises PagedGQAError with
+    PGD_ERR_TOO_LARGE when the request needs more scratch than the array holds.
+    """
+    lib = _lib.load()
+    B, Hq, _ = q.shape
+    _check(lib.paged_gqa_decode_noalloc(pool.handle, q.data_ptr(), B, Hq, block_table.data_ptr(),
+                                        block_table.shape[1], seq_lens.data_ptr(), float(scale),
+                                        out.data_ptr(), int(num_splits), _stream_handle(stream)),
+           "paged_gqa_decode_noalloc")
+    return out
+
+
+def paged_gqa_noalloc_scratch_bytes():
+    return int(_lib.load().paged_gqa_noalloc_scratch_bytes())
 
 
 def paged_gqa_get_error(pool, stream=None):

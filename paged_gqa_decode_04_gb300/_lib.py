@@ -18,7 +18,7 @@ PGD_BF16 = 1
 STATUS_NAMES = {
     0: "PGD_OK", 1: "PGD_ERR_ARG", 2: "PGD_ERR_SHAPE", 3: "PGD_ERR_DTYPE", 4: "PGD_ERR_ALIGN",
     5: "PGD_ERR_WORKSPACE", 6: "PGD_ERR_CUDA", 7: "PGD_ERR_BLOCK_ID", 8: "PGD_ERR_SEQ_LEN",
-    9: "PGD_ERR_UNSUPPORTED", 10: "PGD_ERR_TIMEOUT",
+    9: "PGD_ERR_UNSUPPORTED", 10: "PGD_ERR_TIMEOUT", 11: "PGD_ERR_TOO_LARGE",
 }
 globals().update({v: k for k, v in STATUS_NAMES.items()})
 
@@ -58,6 +58,11 @@ def load(path=LIB_PATH):
     lib.paged_gqa_auto_splits.restype = i32
     lib.paged_gqa_strerror.argtypes = [i32]
     lib.paged_gqa_strerror.restype = ctypes.c_char_p
+    lib.paged_gqa_decode_noalloc.argtypes = [vp, vp, i32, i32, vp, i32, vp, ctypes.c_float, vp,
+                                             i32, vp]
+    lib.paged_gqa_decode_noalloc.restype = i32
+    lib.paged_gqa_noalloc_scratch_bytes.argtypes = []
+    lib.paged_gqa_noalloc_scratch_bytes.restype = sz
     _lib = lib
     return lib
 

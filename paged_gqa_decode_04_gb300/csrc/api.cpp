@@ -75,6 +75,8 @@ int resolve_parts(const Pool& p, int num_splits) {
 
 }  // namespace
 
+const Pool& pool_desc(pgd_pool_t h) { return h->p; }
+
 WorkspaceLayout workspace_layout(int B, int hkv, int group, int d, int parts) {
     WorkspaceLayout w;
     const int mtiles = (group + 15) / 16;
@@ -262,6 +264,8 @@ const char* paged_gqa_strerror(int status) {
         case PGD_ERR_SEQ_LEN: return "sequence length out of range";
         case PGD_ERR_UNSUPPORTED: return "unsupported request";
         case PGD_ERR_TIMEOUT: return "device pipeline wait timed out";
+        case PGD_ERR_TOO_LARGE:
+            return "request needs more scratch than the fixed no-alloc scratch array holds";
         default: return "unknown status";
     }
 }

@@ -64,6 +64,9 @@ struct WorkspaceLayout {
 };
 WorkspaceLayout workspace_layout(int B, int hkv, int group, int d, int parts);
 
+// The description behind a pool handle.
+const Pool& pool_desc(pgd_pool_t h);
+
 // Kernel launchers (return a cudaError_t from the launch).
 cudaError_t launch_decode_simple(const DecodeArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_decode_tma(const DecodeArgs& a, const Pool& p, cudaStream_t s);
