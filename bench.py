@@ -37,7 +37,7 @@ from paged_gqa_decode_04_gb300 import accounting  # noqa: E402
 METRIC = "paged GQA decode KV GB/s and % of GB300 HBM peak; tokens/s per layer"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SRC = os.path.join(ROOT, "paged_gqa_decode_04_gb300", "csrc", "decode_tma.cu")
+KERNEL_SRC = os.path.join(ROOT, "paged_gqa_decode_04_gb300", "csrc", "decode_tma.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 

@@ -51,17 +51,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 4-D view of a bf16 pool [num_blocks, bs, Hkv, D] as
-// [d_lo = 64, head-half = Hkv*D/64, slot = bs, block = num_blocks]; one box is
-// one 128-byte half head row for min(bs, 64) consecutive slots of one block.
+// 4-D view of a bf16 pool [num_blocks, bs, Hkv, D] listed as
+// (d_lo = 64, slot = bs, head-half = Hkv*D/64, block = num_blocks), so that a
+// box (64, rows, hg*D/64, 1) -- `rows` slots of one block for hg consecutive
+// KV heads -- lands in shared memory head-half-major: [head-half][slot][64].
 bool encode_pool_map(CUtensorMap* map, const void* base, int64_t num_blocks, int bs, int hkv,
-                     int d) {
+                     int d, int hg) {
     auto fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t row_bytes = (cuuint64_t)hkv * d * 2;
-    cuuint64_t dims[4] = {64, (cuuint64_t)hkv * (d / 64), (cuuint64_t)bs, (cuuint64_t)num_blocks};
-    cuuint64_t strides[3] = {128, row_bytes, row_bytes * bs};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)(bs < kTileTokens ? bs : kTileTokens), 1};
+    const cuuint64_t row_bytes = (cuuint64_t)hkv * d * 2;  // one slot, all heads
+    const int tile = 128 / hg;
+    cuuint64_t dims[4] = {64, (cuuint64_t)bs, (cuuint64_t)hkv * (d / 64), (cuuint64_t)num_blocks};
+    cuuint64_t strides[3] = {row_bytes, 128, row_bytes * bs};
+    cuuint32_t box[4] = {64, (cuuint32_t)(bs < tile ? bs : tile), (cuuint32_t)(hg * (d / 64)), 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -77,14 +79,24 @@ int resolve_parts(const Pool& p, int num_splits) {
 
 const Pool& pool_desc(pgd_pool_t h) { return h->p; }
 
-WorkspaceLayout workspace_layout(int B, int hkv, int group, int d, int parts) {
+int choose_hg(const Pool& p, int group) {
+    if (p.dtype != PGD_BF16) return 1;
+    const int mt = (group + 15) / 16;
+    const int cap = mt == 1 ? 8 : mt == 2 ? 4 : 2;  // at most 8 consumer warps
+    int hg = 8;
+    while (hg > 1 && (p.hkv % hg != 0 || hg > cap)) hg /= 2;
+    return hg;
+}
+
+WorkspaceLayout workspace_layout(int B, int hkv, int group, int hg, int d, int parts) {
     WorkspaceLayout w;
     const int mtiles = (group + 15) / 16;
+    const size_t rows = (size_t)hg * group;  // rows of one partial result
     w.counters_off = 0;
     w.tile_base_off = round_up((size_t)B * hkv * mtiles * sizeof(int), 256);
     w.part_lse_off = w.tile_base_off + round_up((size_t)(B + 1) * sizeof(int64_t), 256);
-    w.part_o_off = w.part_lse_off + round_up((size_t)parts * 2 * group * sizeof(float), 256);
-    w.total = w.part_o_off + round_up((size_t)parts * 2 * group * d * sizeof(float), 256);
+    w.part_o_off = w.part_lse_off + round_up((size_t)parts * 2 * rows * sizeof(float), 256);
+    w.total = w.part_o_off + round_up((size_t)parts * 2 * rows * d * sizeof(float), 256);
     return w;
 }
 
@@ -134,13 +146,19 @@ int paged_kv_pool_create(pgd_pool_t* out, const void* k_pool, const void* v_pool
         return PGD_ERR_CUDA;
     }
     if (dtype == PGD_BF16) {
-        if (!encode_pool_map(&p.tmap_k, k_pool, num_blocks, block_size, num_kv_heads, head_dim) ||
-            !encode_pool_map(&p.tmap_v, v_pool, num_blocks, block_size, num_kv_heads, head_dim)) {
-            cudaFree(p.err);
-            delete h;
-            return PGD_ERR_CUDA;
+        for (int i = 0; i < 4; ++i) {
+            const int hg = 1 << i;
+            if (num_kv_heads % hg != 0) continue;
+            if (!encode_pool_map(&p.tmap_k[i], k_pool, num_blocks, block_size, num_kv_heads,
+                                 head_dim, hg) ||
+                !encode_pool_map(&p.tmap_v[i], v_pool, num_blocks, block_size, num_kv_heads,
+                                 head_dim, hg)) {
+                cudaFree(p.err);
+                delete h;
+                return PGD_ERR_CUDA;
+            }
+            p.tmap_ok[i] = true;
         }
-        p.has_tmap = true;
     }
     *out = h;
     return PGD_OK;
@@ -168,7 +186,8 @@ int paged_gqa_workspace_size(pgd_pool_t pool, int B, int Hq, int num_splits, siz
         return PGD_ERR_ARG;
     const Pool& p = pool->p;
     if (Hq % p.hkv != 0 || Hq / p.hkv > kMaxGroup) return PGD_ERR_SHAPE;
-    *bytes = workspace_layout(B, p.hkv, Hq / p.hkv, p.d, resolve_parts(p, num_splits)).total;
+    const int G = Hq / p.hkv;
+    *bytes = workspace_layout(B, p.hkv, G, choose_hg(p, G), p.d, resolve_parts(p, num_splits)).total;
     return PGD_OK;
 }
 
@@ -196,7 +215,8 @@ int paged_gqa_decode(pgd_pool_t pool, const void* q, int B, int Hq, const int32_
         !aligned(seq_lens, 4))
         return PGD_ERR_ALIGN;
     const int parts = resolve_parts(p, num_splits);
-    const WorkspaceLayout wl = workspace_layout(B, p.hkv, G, p.d, parts);
+    const int hg = choose_hg(p, G);
+    const WorkspaceLayout wl = workspace_layout(B, p.hkv, G, hg, p.d, parts);
     if (!aligned(workspace, 256) || workspace_bytes < wl.total) return PGD_ERR_WORKSPACE;
 
     DeviceGuard g(p.device);
@@ -220,6 +240,9 @@ int paged_gqa_decode(pgd_pool_t pool, const void* q, int B, int Hq, const int32_
     a.num_blocks = p.num_blocks;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.num_parts = parts;
+    a.hg = hg;
+    a.units = p.hkv / hg;
+    a.tile_tokens = p.dtype == PGD_BF16 ? 128 / hg : kSimpleTileTokens;
     a.err = p.err;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     a.counters = reinterpret_cast<int*>(ws + wl.counters_off);

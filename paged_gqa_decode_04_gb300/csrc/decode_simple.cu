@@ -46,8 +46,8 @@ __global__ void __launch_bounds__(kSimpleThreads) decode_simple_kernel(DecodeArg
     constexpr int DPL = D / 32;  // head-dim elements per lane
     __shared__ int64_t scratch[kSimpleThreads];
     __shared__ SpanStart ss;
-    find_span_start(a.seq_lens, a.B, a.hkv, a.max_blocks, a.block_size, a.num_parts, scratch,
-                    &ss, a.tile_base);
+    find_span_start(a.seq_lens, a.B, a.units, a.tile_tokens, a.max_blocks, a.block_size,
+                    a.num_parts, scratch, &ss, a.tile_base);
     if (ss.r0 >= ss.r1) return;
 
     const int warp = threadIdx.x / 32;
@@ -58,7 +58,8 @@ __global__ void __launch_bounds__(kSimpleThreads) decode_simple_kernel(DecodeArg
     T* __restrict__ out = static_cast<T*>(a.out);
     const int G = a.group;
 
-    TileCursor cur = cursor_at(ss, a.seq_lens, a.hkv, a.max_blocks, a.block_size);
+    TileCursor cur = cursor_at(ss, a.seq_lens, a.units, a.tile_tokens, a.max_blocks,
+                               a.block_size);
     int64_t x = ss.r0;
     while (x < ss.r1) {
         const int64_t run_end = cur.run_start + cur.n_b;
@@ -66,9 +67,9 @@ __global__ void __launch_bounds__(kSimpleThreads) decode_simple_kernel(DecodeArg
         const int flags = segment_flags(x, cur.run_start, cur.n_b, ss.r0, ss.r1);
         const int L = a.seq_lens[cur.b];
         const int i_end = (int)(piece_end - cur.run_start);
-        const int t_begin = cur.i * kTileTokens;
-        const int t_end = min(L, i_end * kTileTokens);
-        const int b = cur.b, kvh = cur.kvh;
+        const int t_begin = cur.i * a.tile_tokens;
+        const int t_end = min(L, i_end * a.tile_tokens);
+        const int b = cur.b, kvh = cur.unit;  // one KV head per unit here
 
         for (int j = warp; j < G; j += kSimpleWarps) {
             const int h = kvh * G + j;
@@ -121,7 +122,7 @@ __global__ void __launch_bounds__(kSimpleThreads) decode_simple_kernel(DecodeArg
         // advance past this piece
         x = piece_end;
         cur.i = i_end - 1;
-        cursor_next(cur, a.seq_lens, a.B, a.hkv, a.max_blocks, a.block_size);
+        cursor_next(cur, a.seq_lens, a.B, a.units, a.tile_tokens, a.max_blocks, a.block_size);
     }
 }
 

@@ -1,42 +1,55 @@
 // bfloat16 paged GQA decode: TMA page staging, mbarrier pipeline, tensor-core
-// tile products, online softmax.  sm_103a.
+// tile products, online softmax.  sm_103a.  Included by decode_tma_d64.cu and
+// decode_tma_d128.cu, which instantiate it for one head dimension each.
 //
 // Decode attention reads every cached K/V byte once and does G multiply-adds
 // per element, far below the tensor cores' ridge point, so the kernel is built
-// around keeping HBM busy (the pages: "Moving KV tensors from global memory to
-// the compute cores takes significantly longer than the actual matrix
-// multiplication", "Advanced Optimizations: MQA, GQA, and PagedAttention",
-// section "The Memory Bandwidth Bottleneck").
+// around keeping HBM busy (the pages: moving KV tensors from global memory to
+// the compute cores takes far longer than the matrix products, "Advanced
+// Optimizations: MQA, GQA, and PagedAttention", section "The Memory Bandwidth
+// Bottleneck").
 //
-// Structure of a CTA (one per span of the 64-token tile sequence, see
-// partition.cuh; the grid is one CTA per SM):
-//   * warp NC (producer): walks the span's tiles, reads the tile's block ids
-//     from the block table, and for each 16..64-row page slice issues
-//     cp.async.bulk.tensor loads of K and V ([rows, 64] bf16 boxes, 128-byte
-//     swizzle) into a ring of pipeline stages, each guarded by a "full"
-//     mbarrier (transaction bytes) and an "empty" mbarrier (consumer release).
-//     Reading the pages inside the attention kernel is the block-read +
-//     attention fusion of "Modern LLM Inference ...", section 8.3.
-//   * warps 0..NC-1 (consumers): warp (mt, tg) owns query rows
-//     [16 mt, 16 mt + 16) of the KV head's group and tokens
-//     [tg TW, (tg+1) TW) of every tile.  S = q K^T and O += P V run on
+// Unit of work.  A pool block [block_size, Hkv, D] is contiguous, all KV heads
+// of a token side by side.  A CTA therefore works on a group of HG KV heads at
+// once (HG = 8 for Llama-style GQA) and one TMA box fetches a page slice for
+// the whole group: [rows, HG heads, 128 bytes x D/64] — at Hkv = 8, D = 128,
+// block_size = 16 that is the entire 32 KB block, one contiguous read.  The
+// tensor map lists the pool's dimensions as (d_lo 64, slot, head-half, block)
+// so the box lands in shared memory head-major, [head-half][slot][64], which
+// keeps the 128-byte swizzle conflict-free for ldmatrix over tokens.
+//
+// Structure of a CTA (one per span of the tile sequence, see partition.cuh;
+// the grid is one CTA per SM):
+//   * warp NC (producer): walks the span's tiles (T = 128 / HG tokens of one
+//     (sequence, head group)), keeps a 32-entry window of block ids in
+//     registers (plus the next window in flight), and issues one
+//     cp.async.bulk.tensor per page for K and one for V into a ring of stages
+//     guarded by "full" (transaction bytes) and "empty" mbarriers.  Reading the
+//     pages inside the attention kernel is the block-read + attention fusion
+//     of "Modern LLM Inference ...", section 8.3.
+//   * warps 0..NC-1 (consumers): warp (hgi, mt, tg) owns KV head hgi of the
+//     group, query rows [16 mt, 16 mt + 16) of that head's G-row group and
+//     tokens [tg TW, (tg+1) TW) of every tile.  S = q K^T and O += P V run on
 //     mma.sync m16n8k16 (bf16 in, fp32 accumulate) fed by ldmatrix from the
 //     swizzled stage; the running max / sum softmax runs on the fp32
-//     accumulators in base-2 units.  At the end of a piece the token groups
-//     are combined through shared memory and the tg == 0 warps write the
-//     output row (whole run) or a normalised partial + log-sum-exp (split run).
+//     accumulators in base-2 units.  When TG > 1 the token groups of a head
+//     combine through shared memory at the end of a piece; the tg == 0 warps
+//     then write the output rows (whole run) or a normalised partial and its
+//     log2-sum-exp (split run); the warp that completes a split run's count
+//     merges its pieces.
 //
 // Every wait is bounded (kWaitNs); a wait that gives up latches
 // PGD_ERR_TIMEOUT, marks the CTA aborted and lets every warp leave.
+#pragma once
+
 #include <cuda_bf16.h>
 #include <math.h>
 
 #include "partition.cuh"
 
 namespace pgd {
-namespace {
+namespace tma {
 
-constexpr int T = kTileTokens;          // tokens per tile / stage
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
 constexpr int kSmemBudget = 227 * 1024;
 
@@ -141,20 +154,23 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // ----------------------------------------------------------------- configuration
-template <int D_, int MT_, int TG_, bool ROWS16_>
+template <int D_, int HG_, int MT_, int TG_, bool ROWS16_>
 struct Cfg {
     static constexpr int D = D_;
-    static constexpr int MT = MT_;            // m16 row tiles of the query group
+    static constexpr int HG = HG_;            // KV heads per unit of work
+    static constexpr int MT = MT_;            // m16 row tiles of one head's query group
     static constexpr int TG = TG_;            // token groups per tile
     static constexpr bool ROWS16 = ROWS16_;   // rows 8..15 of an m-tile in use
-    static constexpr int NC = MT * TG;        // consumer warps
+    static constexpr int HALVES = D / 64;     // 128-byte halves of a head row
+    static constexpr int HH = HG * HALVES;    // head-halves per tile
+    static constexpr int T = 128 / HG;        // tokens per tile
+    static constexpr int NC = HG * MT * TG;   // consumer warps
     static constexpr int THREADS = (NC + 1) * 32;
     static constexpr int TW = T / TG;         // tokens per consumer warp per tile
-    static constexpr int HALVES = D / 64;     // 128-byte halves of a head row
-    static constexpr int HALF_BYTES = T * 128;
-    static constexpr int STAGE_BYTES = 2 * HALVES * HALF_BYTES;  // K then V
+    static constexpr int TENSOR_BYTES = HH * T * 128;   // K (or V) bytes of a stage
+    static constexpr int STAGE_BYTES = 2 * TENSOR_BYTES;
     static constexpr int ROWS = ROWS16 ? 16 : 8;
-    static constexpr int COMB_FLOATS = (TG - 1) * MT * ROWS * (D + 2);
+    static constexpr int COMB_FLOATS = (TG - 1) * HG * MT * ROWS * (D + 2);
     static constexpr int COMB_BYTES = COMB_FLOATS * 4;
     static constexpr int STATIC_RESERVE = 4096;  // static smem + alignment slack
     static constexpr int STAGES_FIT = (kSmemBudget - STATIC_RESERVE - COMB_BYTES) / STAGE_BYTES;
@@ -163,12 +179,13 @@ struct Cfg {
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + COMB_BYTES;
     static_assert(STAGES >= 2, "pipeline needs at least two stages");
     static_assert(TW % 16 == 0, "a warp's token slice must be whole k16 steps");
+    static_assert(THREADS <= 288, "at most 8 consumer warps");
 };
 
 // What the producer tells the consumers about the tile in a stage.
 struct StageDesc {
-    int64_t run_start;  // flat index of tile 0 of the (b, kvh) run
-    int b, kvh, n_valid, flags;
+    int64_t run_start;  // flat index of tile 0 of the (b, unit) run
+    int b, unit, n_valid, flags;
     int n_b;            // tiles of the run
     int pad;
 };
@@ -180,6 +197,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                       const __grid_constant__ CUtensorMap tmap_v, DecodeArgs a) {
     constexpr int S = C::STAGES;
     constexpr int D = C::D;
+    constexpr int T = C::T;
     extern __shared__ uint8_t dyn_smem[];
     __shared__ int64_t scratch[C::THREADS];
     __shared__ SpanStart ss;
@@ -195,6 +213,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
+    const int bs = a.block_size;
+    // page geometry of a tile: R rows per box, T / R boxes (pages) per tile
+    const int R = bs < T ? bs : T;
+    const int log_r = __ffs(R) - 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -205,14 +227,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         aborted = 0;
         fence_barrier_init();
     }
-    find_span_start(a.seq_lens, a.B, a.hkv, a.max_blocks, a.block_size, a.num_parts, scratch,
-                    &ss, a.tile_base);  // ends with __syncthreads
+    find_span_start(a.seq_lens, a.B, a.units, T, a.max_blocks, bs, a.num_parts, scratch, &ss,
+                    a.tile_base);  // ends with __syncthreads
 
     // Sequences that own no tiles: length 0 gives zeros, an out-of-range length
     // gives NaN and latches PGD_ERR_SEQ_LEN.  CTA b % P writes sequence b.
     for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
         const int L = a.seq_lens[b];
-        if (L != 0 && seq_len_ok(L, a.max_blocks, a.block_size)) continue;
+        if (L != 0 && seq_len_ok(L, a.max_blocks, bs)) continue;
         if (L != 0 && threadIdx.x == 0) latch_error(a.err, PGD_ERR_SEQ_LEN);
         const __nv_bfloat16 fill = __float2bfloat16_rn(L == 0 ? 0.f : NAN);
         __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) + (int64_t)b * a.hq * D;
@@ -221,14 +243,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (ss.r0 >= ss.r1) return;
     const int64_t r0 = ss.r0, r1 = ss.r1;
     const int n_tiles = (int)(r1 - r0);
-    const int bs = a.block_size;
 
     if (warp == C::NC) {
         // ============================================================ producer
-        const int box_rows = bs < T ? bs : T;
-        const uint32_t box_bytes = (uint32_t)box_rows * 128u;
-        TileCursor cur = cursor_at(ss, a.seq_lens, a.hkv, a.max_blocks, bs);
+        TileCursor cur = cursor_at(ss, a.seq_lens, a.units, T, a.max_blocks, bs);
         const uint64_t policy = policy_evict_first();
+        const uint32_t box_bytes = (uint32_t)(C::HH * R * 128);
         // Block-id window: lane l holds block_table[win_b][win_lb + l]; the next
         // 32 entries are loaded ahead into nxt_id so that walking a run meets
         // the table's latency once per window, not once per tile.
@@ -282,25 +302,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (aborted) break;
             const uint32_t fb = smem_u32(&full_bar[s]);
             if (lane == 0) {
-                desc[s] = StageDesc{cur.run_start, cur.b, cur.kvh, n_valid, flags, cur.n_b, 0};
-                mbar_arrive_expect_tx(fb, (uint32_t)nok * box_bytes * 2u * C::HALVES);
+                desc[s] = StageDesc{cur.run_start, cur.b, cur.unit, n_valid, flags, cur.n_b, 0};
+                mbar_arrive_expect_tx(fb, (uint32_t)nok * box_bytes * 2u);
                 if (bad) latch_error(a.err, PGD_ERR_BLOCK_ID);
             }
             ++issued;
             __syncwarp();
             if (ok) {
-                const uint32_t st = smem_u32(stage_base + s * C::STAGE_BYTES);
-                const uint32_t row_off = (uint32_t)(lane * box_rows) * 128u;
-#pragma unroll
-                for (int h = 0; h < C::HALVES; ++h) {
-                    const int c1 = cur.kvh * C::HALVES + h;
-                    tma_load_4d(st + h * C::HALF_BYTES + row_off, &tmap_k, fb, 0, c1, slot0,
-                                (int)phys, policy);
-                    tma_load_4d(st + (C::HALVES + h) * C::HALF_BYTES + row_off, &tmap_v, fb, 0,
-                                c1, slot0, (int)phys, policy);
-                }
+                // page `lane` of the tile: K box then V box, all HG heads
+                const uint32_t dst = smem_u32(stage_base + s * C::STAGE_BYTES) + lane * box_bytes;
+                const int hh0 = cur.unit * C::HH;
+                tma_load_4d(dst, &tmap_k, fb, 0, slot0, hh0, (int)phys, policy);
+                tma_load_4d(dst + C::TENSOR_BYTES, &tmap_v, fb, 0, slot0, hh0, (int)phys, policy);
             }
-            cursor_next(cur, a.seq_lens, a.B, a.hkv, a.max_blocks, bs);
+            cursor_next(cur, a.seq_lens, a.B, a.units, T, a.max_blocks, bs);
         }
         // Do not leave while copies this CTA issued may still land.
         if (lane == 0) {
@@ -313,8 +328,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
 
     // ================================================================ consumers
-    const int mt = warp / C::TG;
     const int tg = warp % C::TG;
+    const int mt = (warp / C::TG) % C::MT;
+    const int hgi = warp / (C::TG * C::MT);
     const int gid = lane >> 2, tig = lane & 3;
     const int tw0 = tg * C::TW;
     const int G = a.group;
@@ -322,6 +338,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int row1 = row0 + 8;           // group row of c2,c3
     const bool row0_ok = row0 < G;
     const bool row1_ok = C::ROWS16 && row1 < G;
+    const int piece_rows = C::HG * G;    // rows of a partial result
+    const int hh_mine = hgi * C::HALVES; // my head's first head-half in a page box
 
     uint32_t qa[D / 16][4];
     float o[D / 8][4];
@@ -331,6 +349,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
     // Lane-dependent parts of the ldmatrix addresses.
     const int lm_mi = lane >> 3, lm_i = lane & 7;
+    // byte offset of (token t, head-half h of my head) row in a tensor of a stage
+    auto row_off = [&](int t, int h) -> uint32_t {
+        const int p = t >> log_r, r = t & (R - 1);
+        return (uint32_t)(((p * C::HH + hh_mine + h) * R + r) * 128);
+    };
 
     for (int it = 0; it < n_tiles; ++it) {
         const int s = it % S;
@@ -345,12 +368,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (aborted) break;
         const StageDesc dsc = desc[s];
         uint8_t* st = stage_base + s * C::STAGE_BYTES;
-        const uint32_t st_u = smem_u32(st);
+        const uint32_t k_u = smem_u32(st);
+        const uint32_t v_u = k_u + C::TENSOR_BYTES;
+        const int kvh = dsc.unit * C::HG + hgi;
 
         if (dsc.flags & kSegStart) {
             // New piece: load this warp's query rows as mma A fragments.
             const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q) +
-                                      ((int64_t)dsc.b * a.hq + (int64_t)dsc.kvh * G) * D;
+                                      ((int64_t)dsc.b * a.hq + (int64_t)kvh * G) * D;
             const uint32_t* q0 = reinterpret_cast<const uint32_t*>(qg + (int64_t)row0 * D);
             const uint32_t* q1 = reinterpret_cast<const uint32_t*>(qg + (int64_t)row1 * D);
 #pragma unroll
@@ -375,14 +400,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (zeroed) {
             // Rows past the sequence end are tail slots or stale data: zero V
             // there so that 0 * (NaN or Inf) never reaches the accumulators.
-            const int z0 = n_valid;
-            const int nz = tw0 + C::TW - z0;
+            const int nz = tw0 + C::TW - n_valid;
             for (int idx = lane; idx < nz * 8 * C::HALVES; idx += 32) {
-                const int r = z0 + idx / (8 * C::HALVES);
+                const int t = n_valid + idx / (8 * C::HALVES);
                 const int rem = idx % (8 * C::HALVES);
-                const int h = rem / 8, ch = rem % 8;
-                *reinterpret_cast<uint4*>(st + (C::HALVES + h) * C::HALF_BYTES + r * 128 +
-                                          ch * 16) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(st + C::TENSOR_BYTES + row_off(t, rem / 8) +
+                                          (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
             }
             __syncwarp();
         }
@@ -399,10 +422,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
                 for (int np = 0; np < C::TW / 16; ++np) {
                     const int tok = tw0 + np * 16 + (lm_mi >> 1) * 8 + lm_i;
-                    const uint32_t addr =
-                        st_u + h * C::HALF_BYTES + tok * 128 + ((kc ^ (tok & 7)) << 4);
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4(addr, b0, b1, b2, b3);
+                    ldsm_x4(k_u + row_off(tok, h) + ((kc ^ lm_i) << 4), b0, b1, b2, b3);
                     mma_bf16(sc[2 * np], qa[ks], b0, b1);
                     mma_bf16(sc[2 * np + 1], qa[ks], b2, b3);
                 }
@@ -474,10 +495,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 for (int dp = 0; dp < D / 16; ++dp) {
                     const int h = dp / 4;
                     const int vc = (dp % 4) * 2 + (lm_mi >> 1);
-                    const uint32_t addr = st_u + (C::HALVES + h) * C::HALF_BYTES + tok * 128 +
-                                          ((vc ^ (tok & 7)) << 4);
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(addr, b0, b1, b2, b3);
+                    ldsm_x4_t(v_u + row_off(tok, h) + ((vc ^ lm_i) << 4), b0, b1, b2, b3);
                     mma_bf16(o[2 * dp], pa, b0, b1);
                     mma_bf16(o[2 * dp + 1], pa, b2, b3);
                 }
@@ -498,8 +517,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
         if (C::TG > 1) {
             constexpr int RS = D + 2;  // row stride: D outputs, then m and l
+            const int grp = hgi * C::MT + mt;
             if (tg > 0) {
-                float* cb = comb + ((tg - 1) * C::MT + mt) * C::ROWS * RS;
+                float* cb = comb + ((tg - 1) * C::HG * C::MT + grp) * C::ROWS * RS;
 #pragma unroll
                 for (int n = 0; n < D / 8; ++n) {
                     *reinterpret_cast<float2*>(cb + gid * RS + n * 8 + tig * 2) =
@@ -529,7 +549,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (tg == 0) {
 #pragma unroll 1
                 for (int t2 = 1; t2 < C::TG; ++t2) {
-                    const float* cb = comb + ((t2 - 1) * C::MT + mt) * C::ROWS * RS;
+                    const float* cb = comb + ((t2 - 1) * C::HG * C::MT + grp) * C::ROWS * RS;
                     const float om0 = cb[gid * RS + D], ol0 = cb[gid * RS + D + 1];
                     const float nm0 = fmaxf(m0, om0);
                     const float nb0 = nm0 == -INFINITY ? 0.f : nm0;
@@ -576,9 +596,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // ---- write: whole run -> out (bf16); split run -> partial (fp32) + lse
         const float inv0 = seg_bad ? NAN : 1.f / lt0;
         const float inv1 = seg_bad ? NAN : 1.f / lt1;
+        __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) +
+                            ((int64_t)dsc.b * a.hq + (int64_t)kvh * G) * D;
         if (!(dsc.flags & kSegPartial)) {
-            __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) +
-                                ((int64_t)dsc.b * a.hq + (int64_t)dsc.kvh * G) * D;
 #pragma unroll
             for (int n = 0; n < D / 8; ++n) {
                 if (row0_ok)
@@ -588,98 +608,101 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     *reinterpret_cast<uint32_t*>(ob + (int64_t)row1 * D + n * 8 + tig * 2) =
                         pack_bf16(o[n][2] * inv1, o[n][3] * inv1);
             }
-        } else {
-            const int64_t slot = (int64_t)blockIdx.x * 2 + ((dsc.flags & kSegSlot1) ? 1 : 0);
-            float* po = a.part_o + slot * G * D;
+            continue;
+        }
+        const int64_t slot = (int64_t)blockIdx.x * 2 + ((dsc.flags & kSegSlot1) ? 1 : 0);
+        const int prow0 = hgi * G + row0, prow1 = hgi * G + row1;  // rows of the piece
+        {
+            float* po = a.part_o + slot * piece_rows * D;
 #pragma unroll
             for (int n = 0; n < D / 8; ++n) {
                 if (row0_ok)
-                    *reinterpret_cast<float2*>(po + (int64_t)row0 * D + n * 8 + tig * 2) =
+                    *reinterpret_cast<float2*>(po + (int64_t)prow0 * D + n * 8 + tig * 2) =
                         make_float2(o[n][0] * inv0, o[n][1] * inv0);
                 if (row1_ok)
-                    *reinterpret_cast<float2*>(po + (int64_t)row1 * D + n * 8 + tig * 2) =
+                    *reinterpret_cast<float2*>(po + (int64_t)prow1 * D + n * 8 + tig * 2) =
                         make_float2(o[n][2] * inv1, o[n][3] * inv1);
             }
             if (tig == 0) {
-                if (row0_ok) a.part_lse[slot * G + row0] = seg_bad ? 0.f : m0 + fast_log2(lt0);
-                if (row1_ok) a.part_lse[slot * G + row1] = seg_bad ? 0.f : m1 + fast_log2(lt1);
+                float* pl = a.part_lse + slot * piece_rows;
+                if (row0_ok) pl[prow0] = seg_bad ? 0.f : m0 + fast_log2(lt0);
+                if (row1_ok) pl[prow1] = seg_bad ? 0.f : m1 + fast_log2(lt1);
             }
-            // Publish the partial, count it; the warp that brings the run's
-            // count to its number of pieces merges them (log-sum-exp) and
-            // resets the counter, so no second kernel and no waiting.
-            __threadfence();
-            __syncwarp();
-            const int64_t t0 = dsc.run_start;
-            const int64_t N = ss.n_total, P = a.num_parts;
-            const int64_t c0 = span_owner(t0, N, P), c1 = span_owner(t0 + dsc.n_b - 1, N, P);
-            int last = 0;
-            if (lane == 0) {
-                int pieces = (int)(c1 - c0 + 1);
-                if (P > N) {
-                    pieces = 0;
-                    for (int64_t c = c0; c <= c1; ++c)
-                        pieces += span_begin(c, N, P) != span_begin(c + 1, N, P);
-                }
-                int* ctr = a.counters + ((int64_t)dsc.b * a.hkv + dsc.kvh) * C::MT + mt;
-                last = atomicAdd(ctr, 1) == pieces - 1;
-                if (last) atomicExch(ctr, 0);
+        }
+        // Publish the partial, count it; the warp that brings the run's count
+        // to its number of pieces merges them (log-sum-exp) and resets the
+        // counter, so no second kernel and no waiting.
+        __threadfence();
+        __syncwarp();
+        const int64_t t0 = dsc.run_start;
+        const int64_t N = ss.n_total, P = a.num_parts;
+        const int64_t c0 = span_owner(t0, N, P), c1 = span_owner(t0 + dsc.n_b - 1, N, P);
+        int last = 0;
+        if (lane == 0) {
+            int pieces = (int)(c1 - c0 + 1);
+            if (P > N) {
+                pieces = 0;
+                for (int64_t c = c0; c <= c1; ++c)
+                    pieces += span_begin(c, N, P) != span_begin(c + 1, N, P);
             }
-            last = __shfl_sync(0xffffffffu, last, 0);
-            if (!last) continue;
-            __threadfence();
-            float M0 = -INFINITY, M1 = -INFINITY, W0 = 0.f, W1 = 0.f;
+            int* ctr = a.counters + ((int64_t)dsc.b * a.hkv + kvh) * C::MT + mt;
+            last = atomicAdd(ctr, 1) == pieces - 1;
+            if (last) atomicExch(ctr, 0);
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (!last) continue;
+        __threadfence();
+        float M0 = -INFINITY, M1 = -INFINITY, W0 = 0.f, W1 = 0.f;
 #pragma unroll
-            for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-            for (int64_t c = c0; c <= c1; ++c) {
-                const int64_t sb = span_begin(c, N, P);
-                if (sb == span_begin(c + 1, N, P)) continue;
-                const int64_t sl = c * 2 + (sb < t0 ? 1 : 0);
-                const float* pc = a.part_o + sl * G * D;
-                const float* lc = a.part_lse + sl * G;
-                const float e0 = row0_ok ? __ldcg(lc + row0) : 0.f;
-                const float e1 = row1_ok ? __ldcg(lc + row1) : 0.f;
-                const float n0 = fmaxf(M0, e0), n1 = fmaxf(M1, e1);
-                const float a0 = fast_exp2(M0 - n0), b0 = fast_exp2(e0 - n0);
-                const float a1 = fast_exp2(M1 - n1), b1 = fast_exp2(e1 - n1);
-                M0 = n0;
-                M1 = n1;
-                W0 = W0 * a0 + b0;
-                W1 = W1 * a1 + b1;
-#pragma unroll
-                for (int n = 0; n < D / 8; ++n) {
-                    if (row0_ok) {
-                        const float2 u = __ldcg(reinterpret_cast<const float2*>(
-                            pc + (int64_t)row0 * D + n * 8 + tig * 2));
-                        o[n][0] = o[n][0] * a0 + u.x * b0;
-                        o[n][1] = o[n][1] * a0 + u.y * b0;
-                    }
-                    if (row1_ok) {
-                        const float2 u = __ldcg(reinterpret_cast<const float2*>(
-                            pc + (int64_t)row1 * D + n * 8 + tig * 2));
-                        o[n][2] = o[n][2] * a1 + u.x * b1;
-                        o[n][3] = o[n][3] * a1 + u.y * b1;
-                    }
-                }
-            }
-            const float w0 = 1.f / W0, w1 = 1.f / W1;
-            __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) +
-                                ((int64_t)dsc.b * a.hq + (int64_t)dsc.kvh * G) * D;
+        for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        for (int64_t c = c0; c <= c1; ++c) {
+            const int64_t sb = span_begin(c, N, P);
+            if (sb == span_begin(c + 1, N, P)) continue;
+            const int64_t sl = c * 2 + (sb < t0 ? 1 : 0);
+            const float* pc = a.part_o + sl * piece_rows * D;
+            const float* lc = a.part_lse + sl * piece_rows;
+            const float e0 = row0_ok ? __ldcg(lc + prow0) : 0.f;
+            const float e1 = row1_ok ? __ldcg(lc + prow1) : 0.f;
+            const float n0 = fmaxf(M0, e0), n1 = fmaxf(M1, e1);
+            const float a0 = fast_exp2(M0 - n0), b0 = fast_exp2(e0 - n0);
+            const float a1 = fast_exp2(M1 - n1), b1 = fast_exp2(e1 - n1);
+            M0 = n0;
+            M1 = n1;
+            W0 = W0 * a0 + b0;
+            W1 = W1 * a1 + b1;
 #pragma unroll
             for (int n = 0; n < D / 8; ++n) {
-                if (row0_ok)
-                    *reinterpret_cast<uint32_t*>(ob + (int64_t)row0 * D + n * 8 + tig * 2) =
-                        pack_bf16(o[n][0] * w0, o[n][1] * w0);
-                if (row1_ok)
-                    *reinterpret_cast<uint32_t*>(ob + (int64_t)row1 * D + n * 8 + tig * 2) =
-                        pack_bf16(o[n][2] * w1, o[n][3] * w1);
+                if (row0_ok) {
+                    const float2 u = __ldcg(
+                        reinterpret_cast<const float2*>(pc + (int64_t)prow0 * D + n * 8 + tig * 2));
+                    o[n][0] = o[n][0] * a0 + u.x * b0;
+                    o[n][1] = o[n][1] * a0 + u.y * b0;
+                }
+                if (row1_ok) {
+                    const float2 u = __ldcg(
+                        reinterpret_cast<const float2*>(pc + (int64_t)prow1 * D + n * 8 + tig * 2));
+                    o[n][2] = o[n][2] * a1 + u.x * b1;
+                    o[n][3] = o[n][3] * a1 + u.y * b1;
+                }
             }
+        }
+        const float w0 = 1.f / W0, w1 = 1.f / W1;
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) {
+            if (row0_ok)
+                *reinterpret_cast<uint32_t*>(ob + (int64_t)row0 * D + n * 8 + tig * 2) =
+                    pack_bf16(o[n][0] * w0, o[n][1] * w0);
+            if (row1_ok)
+                *reinterpret_cast<uint32_t*>(ob + (int64_t)row1 * D + n * 8 + tig * 2) =
+                    pack_bf16(o[n][2] * w1, o[n][3] * w1);
         }
     }
 }
 
 template <class C>
-cudaError_t launch_cfg(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
-    static bool attr_done = false;  // per instantiation; harmless if raced
+cudaError_t launch_cfg(const DecodeArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
+                       cudaStream_t s) {
+    static bool attr_done = false;  // per instantiation; a repeated set is harmless
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(decode_tma_kernel<C>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -687,25 +710,48 @@ cudaError_t launch_cfg(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    decode_tma_kernel<C><<<a.num_parts, C::THREADS, C::SMEM_BYTES, s>>>(p.tmap_k, p.tmap_v, a);
+    decode_tma_kernel<C><<<a.num_parts, C::THREADS, C::SMEM_BYTES, s>>>(mk, mv, a);
     return cudaGetLastError();
 }
 
+// Token groups per tile for (HG, MT): up to 8 consumer warps, >= 16 tokens each.
+constexpr int token_groups(int hg, int mt) {
+    const int by_tokens = (128 / hg) / 16;
+    const int by_warps = 8 / (hg * mt) > 0 ? 8 / (hg * mt) : 1;
+    return by_tokens < by_warps ? by_tokens : by_warps;
+}
+
+template <int D, int HG, int MT, bool R16>
+cudaError_t launch_hg(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
+    constexpr int TG = token_groups(HG, MT);
+    const int idx = HG == 1 ? 0 : HG == 2 ? 1 : HG == 4 ? 2 : 3;
+    return launch_cfg<Cfg<D, HG, MT, TG, R16>>(a, p.tmap_k[idx], p.tmap_v[idx], s);
+}
+
+template <int D, int MT, bool R16>
+cudaError_t launch_mt(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
+    switch (a.hg) {
+        case 1: return launch_hg<D, 1, MT, R16>(a, p, s);
+        case 2: return launch_hg<D, 2, MT, R16>(a, p, s);
+        case 4:
+            if constexpr (MT <= 2) return launch_hg<D, 4, MT, R16>(a, p, s);
+            break;
+        case 8:
+            if constexpr (MT == 1) return launch_hg<D, 8, MT, R16>(a, p, s);
+            break;
+    }
+    return cudaErrorInvalidValue;
+}
+
 template <int D>
-cudaError_t launch_d(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
+cudaError_t launch_tma_d(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
     const int G = a.group;
-    if (G <= 8) return launch_cfg<Cfg<D, 1, 4, false>>(a, p, s);
-    if (G <= 16) return launch_cfg<Cfg<D, 1, 4, true>>(a, p, s);
-    if (G <= 32) return launch_cfg<Cfg<D, 2, 2, true>>(a, p, s);
-    if (G <= 48) return launch_cfg<Cfg<D, 3, 2, true>>(a, p, s);
-    return launch_cfg<Cfg<D, 4, 2, true>>(a, p, s);
+    if (G <= 8) return launch_mt<D, 1, false>(a, p, s);
+    if (G <= 16) return launch_mt<D, 1, true>(a, p, s);
+    if (G <= 32) return launch_mt<D, 2, true>(a, p, s);
+    if (G <= 48) return launch_mt<D, 3, true>(a, p, s);
+    return launch_mt<D, 4, true>(a, p, s);
 }
 
-}  // namespace
-
-cudaError_t launch_decode_tma(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
-    if (a.d == 64) return launch_d<64>(a, p, s);
-    return launch_d<128>(a, p, s);
-}
-
+}  // namespace tma
 }  // namespace pgd

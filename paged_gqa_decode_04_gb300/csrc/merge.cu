@@ -12,9 +12,11 @@
 // "Modern LLM Inference ...", section 8.3); it keeps the softmax exact, as the
 // same notes say of FlashAttention's online softmax.
 //
-// One CTA per sequence.  Runs that were not split are left alone (the decode
-// kernel wrote them), sequences of length 0 get zeros, and sequences whose
-// length is out of range get NaN and latch PGD_ERR_SEQ_LEN.
+// One CTA per sequence; used after the CUDA-core kernel, whose units are single
+// KV heads (a run is one (sequence, KV head) pair).  Runs that were not split
+// are left alone (the decode kernel wrote them), sequences of length 0 get
+// zeros, and sequences whose length is out of range get NaN and latch
+// PGD_ERR_SEQ_LEN.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -51,7 +53,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeArgs a) {
 
     const int64_t N = a.tile_base[a.B];
     const int64_t P = a.num_parts;
-    const int n_b = tiles_of(L, a.max_blocks, a.block_size);
+    const int n_b = tiles_of(L, a.max_blocks, a.block_size, a.tile_tokens);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int nwarps = blockDim.x / 32;
 

@@ -1,13 +1,17 @@
 // Device-side work partition shared by the decode kernels and the merge kernel.
 //
-// The KV work of one call is the sequence of 64-token tiles of every
-// (sequence b, KV head kvh) pair, in the order b-major, then kvh, then tile:
+// The KV work of one call is the sequence of T-token tiles of every
+// (sequence b, unit u) pair, in the order b-major, then unit, then tile:
 //
-//     flat(b, kvh, i) = tile_base[b] + kvh * n_b + i,   n_b = ceil(L_b / 64)
+//     flat(b, u, i) = tile_base[b] + u * n_b + i,   n_b = ceil(L_b / T)
 //
+// A unit is a group of HG consecutive KV heads that one tile covers together
+// (HG = 1 for the CUDA-core kernel, up to 8 for the TMA kernel, which reads a
+// page slice for all heads of the group in one copy); a sequence has
+// Hkv / HG units.
 // CTA c of P takes the span [floor(c N / P), floor((c+1) N / P)) of the N
 // tiles, so every CTA gets the same amount of KV bytes (to one tile) whatever
-// the length mix.  A (b, kvh) run that lies inside one span is finished by that
+// the length mix.  A (b, u) run that lies inside one span is finished by that
 // CTA; a run cut by span boundaries leaves one partial result per piece, in
 // slot 0 of a CTA (the piece that starts the CTA's span) or slot 1 (the piece
 // that ends it), and the merge kernel combines them with a log-sum-exp.
@@ -26,8 +30,8 @@ __device__ __forceinline__ bool seq_len_ok(int L, int max_blocks, int block_size
     return L >= 0 && (int64_t)L <= (int64_t)max_blocks * block_size;
 }
 
-__device__ __forceinline__ int tiles_of(int L, int max_blocks, int block_size) {
-    return seq_len_ok(L, max_blocks, block_size) ? (L + kTileTokens - 1) / kTileTokens : 0;
+__device__ __forceinline__ int tiles_of(int L, int max_blocks, int block_size, int T) {
+    return seq_len_ok(L, max_blocks, block_size) ? (L + T - 1) / T : 0;
 }
 
 __device__ __forceinline__ int64_t span_begin(int64_t c, int64_t N, int64_t P) {
@@ -55,8 +59,8 @@ struct SpanStart {
 // Every thread of the block must call this.  `scratch` is >= blockDim.x int64
 // of shared memory, `out` a shared SpanStart.  CTA 0 also writes
 // tile_base[0..B] to global memory for the merge kernel.
-__device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int B, int hkv,
-                                       int max_blocks, int block_size, int64_t parts,
+__device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int B, int units,
+                                       int T, int max_blocks, int block_size, int64_t parts,
                                        int64_t* scratch, SpanStart* out,
                                        int64_t* __restrict__ tile_base_out) {
     const int nt = blockDim.x;
@@ -65,7 +69,8 @@ __device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int
     const int b_lo = min(B, tid * per);
     const int b_hi = min(B, b_lo + per);
     int64_t local = 0;
-    for (int b = b_lo; b < b_hi; ++b) local += (int64_t)hkv * tiles_of(seq_lens[b], max_blocks, block_size);
+    for (int b = b_lo; b < b_hi; ++b)
+        local += (int64_t)units * tiles_of(seq_lens[b], max_blocks, block_size, T);
     scratch[tid] = local;
     __syncthreads();
     if (tid == 0) {  // exclusive scan of per-thread sums (nt is small)
@@ -85,7 +90,7 @@ __device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int
     const int64_t r0 = out->r0;
     int64_t run = scratch[tid];
     for (int b = b_lo; b < b_hi; ++b) {
-        int64_t n = (int64_t)hkv * tiles_of(seq_lens[b], max_blocks, block_size);
+        int64_t n = (int64_t)units * tiles_of(seq_lens[b], max_blocks, block_size, T);
         if (blockIdx.x == 0) tile_base_out[b] = run;
         if (r0 >= run && r0 < run + n) {
             out->b = b;
@@ -97,42 +102,43 @@ __device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int
     __syncthreads();
 }
 
-// Cursor over the (b, kvh, tile) sequence of one span.
+// Cursor over the (b, unit, tile) sequence of one span.
 struct TileCursor {
-    int b, kvh, i, n_b;      // current position: tile i of n_b of (b, kvh)
-    int64_t run_start;       // flat index of tile 0 of (b, kvh)
+    int b, unit, i, n_b;     // current position: tile i of n_b of (b, unit)
+    int64_t run_start;       // flat index of tile 0 of (b, unit)
 };
 
-__device__ inline TileCursor cursor_at(const SpanStart& s, const int32_t* seq_lens, int hkv,
-                                       int max_blocks, int block_size) {
+__device__ inline TileCursor cursor_at(const SpanStart& s, const int32_t* seq_lens, int units,
+                                       int T, int max_blocks, int block_size) {
     TileCursor c;
     c.b = s.b;
-    c.n_b = tiles_of(seq_lens[s.b], max_blocks, block_size);
+    c.n_b = tiles_of(seq_lens[s.b], max_blocks, block_size, T);
     int64_t off = s.r0 - s.b_base;
-    c.kvh = (int)(off / c.n_b);
+    c.unit = (int)(off / c.n_b);
     c.i = (int)(off % c.n_b);
-    c.run_start = s.b_base + (int64_t)c.kvh * c.n_b;
+    c.run_start = s.b_base + (int64_t)c.unit * c.n_b;
+    (void)units;
     return c;
 }
 
-__device__ inline void cursor_next(TileCursor& c, const int32_t* seq_lens, int B, int hkv,
-                                   int max_blocks, int block_size) {
+__device__ inline void cursor_next(TileCursor& c, const int32_t* seq_lens, int B, int units,
+                                   int T, int max_blocks, int block_size) {
     if (++c.i < c.n_b) return;
     c.run_start += c.n_b;
     c.i = 0;
-    if (++c.kvh < hkv) return;
-    c.kvh = 0;
+    if (++c.unit < units) return;
+    c.unit = 0;
     int nb = 0;
     while (++c.b < B) {
-        nb = tiles_of(seq_lens[c.b], max_blocks, block_size);
+        nb = tiles_of(seq_lens[c.b], max_blocks, block_size, T);
         if (nb > 0) break;
     }
     c.n_b = nb;
 }
 
-// Segment flags for the piece of (b, kvh) a CTA holds.
+// Segment flags for the piece of (b, unit) a CTA holds.
 enum : int {
-    kSegStart = 1,    // first tile of this CTA's piece of (b, kvh)
+    kSegStart = 1,    // first tile of this CTA's piece of (b, unit)
     kSegEnd = 2,      // last tile of the piece
     kSegPartial = 4,  // piece is not the whole run: write a partial result
     kSegSlot1 = 8,    // partial goes to slot 1 (else slot 0)

@@ -9,9 +9,8 @@
 
 namespace pgd {
 
-// Tokens per tile: the unit of work that is split across CTAs and the unit a
-// pipeline stage holds.
-constexpr int kTileTokens = 64;
+// Tokens per tile of the CUDA-core kernel (the TMA kernel uses 128 / HG).
+constexpr int kSimpleTileTokens = 64;
 
 // Largest query-head group the kernels handle (4 m16 row tiles).
 constexpr int kMaxGroup = 64;
@@ -27,9 +26,12 @@ struct Pool {
     int device;
     int num_sms;
     int* err;              // device error word (latched pgd_status)
-    bool has_tmap;         // bfloat16 TMA descriptors encoded
-    CUtensorMap tmap_k;    // 4-D view [d_lo 64, Hkv*D/64, block_size, num_blocks]
-    CUtensorMap tmap_v;
+    // bfloat16 TMA descriptors, one per head-group size HG = 1, 2, 4, 8 (index
+    // log2 HG), valid where HG divides Hkv: 4-D view (d_lo 64, slot, head-half,
+    // block) of the pool, box (64, min(bs, 128 / HG), HG * D / 64, 1).
+    bool tmap_ok[4];
+    CUtensorMap tmap_k[4];
+    CUtensorMap tmap_v[4];
 };
 
 // Everything a decode launch needs, resolved on the host.
@@ -50,19 +52,25 @@ struct DecodeArgs {
     int64_t num_blocks;
     float scale_log2;      // scale * log2(e): logits kept in base-2 units
     int num_parts;         // CTAs of the decode grid (spans of the tile sequence)
+    int hg;                // KV heads per unit of work
+    int units;             // units per sequence, Hkv / hg
+    int tile_tokens;       // tokens per tile
     int* err;
     // workspace carve-up
     int* counters;         // [B][Hkv][m-tiles] pieces finished per split run (kept zero between calls)
     int64_t* tile_base;    // [B + 1] first flat tile of each sequence
-    float* part_o;         // [num_parts][2][group][d] normalised partial outputs
-    float* part_lse;       // [num_parts][2][group]    partial log2-sum-exp
+    float* part_o;         // [num_parts][2][hg * group][d] normalised partial outputs
+    float* part_lse;       // [num_parts][2][hg * group]    partial log2-sum-exp
 };
 
 // Workspace layout for (B, G, D, parts); returns total bytes and fills offsets.
 struct WorkspaceLayout {
     size_t counters_off, tile_base_off, part_lse_off, part_o_off, total;
 };
-WorkspaceLayout workspace_layout(int B, int hkv, int group, int d, int parts);
+WorkspaceLayout workspace_layout(int B, int hkv, int group, int hg, int d, int parts);
+
+// KV heads per unit of work for this pool and group size.
+int choose_hg(const Pool& p, int group);
 
 // The description behind a pool handle.
 const Pool& pool_desc(pgd_pool_t h);
