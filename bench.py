@@ -348,8 +348,8 @@ def run_ours(args, world, rank, local):
         "tokens_per_s_per_layer": round(world * w.B / (t_ms * 1e-3), 1),
         "roofline": {"bound": "hbm", "achieved": round(per_gpu, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(per_gpu / peak, 4), "traffic": ncu_traffic(args.config),
-                     "note": "achieved = algorithmic bytes / event-timed step (decode + merge "
-                             "kernels), so it under-states the decode kernel alone"},
+                     "note": "bf16 steps are one kernel launch (split-KV merge fused), so "
+                             "achieved = algorithmic bytes / event-timed step"},
         "e2e": {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

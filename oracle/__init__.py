@@ -58,6 +58,10 @@ class Oracle:
         lib.oracle_decode_rows_f64.argtypes = argt + [ctypes.c_void_p, ctypes.c_int64,
                                                       ctypes.c_void_p]
         lib.oracle_decode_rows_f64.restype = ctypes.c_int
+        lib.oracle_decode_ex_f64.argtypes = ([ctypes.c_void_p] * 5 + [ctypes.c_int] * 7 +
+                                             [ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_double, ctypes.c_void_p])
+        lib.oracle_decode_ex_f64.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         self.lib = lib
@@ -93,6 +97,29 @@ class Oracle:
         return out, int(rc)
 
 
+    def decode_ex_f64(self, q, k_pool, v_pool, block_table, seq_lens, scale, window=0):
+        """q [B, q_len, Hq, D]: several query tokens per sequence (the last
+        q_len cached tokens), causal, optional window.  Returns (out, status)."""
+        q = np.ascontiguousarray(q)
+        if q.ndim != 4:
+            raise ValueError("q must be [B, q_len, Hq, D]")
+        B, q_len, Hq, D = q.shape
+        flat = q.reshape(B, q_len * Hq, D)
+        _, k_pool, v_pool, bt, sl, dtype, dims = _prep(flat, k_pool, v_pool, block_table,
+                                                       seq_lens)
+        _, _, Hkv, _, bs, nb, mb = dims
+        if Hq % Hkv:
+            raise ValueError("oracle rejected the arguments")
+        out = np.empty((B, q_len, Hq, D), dtype=np.float64)
+        rc = self.lib.oracle_decode_ex_f64(q.ctypes.data, k_pool.ctypes.data, v_pool.ctypes.data,
+                                           bt.ctypes.data, sl.ctypes.data, dtype, B, q_len, Hq,
+                                           Hkv, D, bs, nb, mb, int(window), float(scale),
+                                           out.ctypes.data)
+        if rc == 1:
+            raise ValueError("oracle rejected the arguments")
+        return out, int(rc)
+
+
 _default = None
 
 
@@ -110,6 +137,10 @@ def num_threads():
 
 def decode_f64(q, k_pool, v_pool, block_table, seq_lens, scale):
     return default().decode_f64(q, k_pool, v_pool, block_table, seq_lens, scale)
+
+
+def decode_ex_f64(q, k_pool, v_pool, block_table, seq_lens, scale, window=0):
+    return default().decode_ex_f64(q, k_pool, v_pool, block_table, seq_lens, scale, window)
 
 
 def decode_rows_f64(q, k_pool, v_pool, block_table, seq_lens, scale, rows):

@@ -48,3 +48,38 @@ def brute_decode(q, k_pool, v_pool, block_table, seq_lens, scale):
         P = P / P.sum(axis=1, keepdims=True)
         out[b] = np.einsum("hl,lhd->hd", P, V)
     return out
+
+
+def brute_decode_ex(q, k_pool, v_pool, block_table, seq_lens, scale, window=0):
+    """q [B, q_len, Hq, D]: dense scores over every cached token with a mask
+    that keeps, for query i at position p = L - q_len + i, the positions
+    max(0, p - window + 1) <= t <= p (no lower bound when window <= 0)."""
+    q = to_f64(q)
+    k_pool = to_f64(k_pool)
+    v_pool = to_f64(v_pool)
+    B, q_len, Hq, D = q.shape
+    _, bs, Hkv, _ = k_pool.shape
+    G = Hq // Hkv
+    out = np.zeros((B, q_len, Hq, D))
+    for b in range(B):
+        L = int(seq_lens[b])
+        if L == 0:
+            continue
+        t = np.arange(L)
+        phys = np.asarray(block_table[b])[t // bs]
+        K = np.repeat(k_pool[phys, t % bs], G, axis=1)      # [L, Hq, D]
+        V = np.repeat(v_pool[phys, t % bs], G, axis=1)
+        S = np.einsum("ihd,lhd->ihl", q[b], K) * scale       # [q_len, Hq, L]
+        pos = L - q_len + np.arange(q_len)                    # [q_len]
+        keep = t[None, :] <= pos[:, None]
+        if window > 0:
+            keep &= t[None, :] >= pos[:, None] - window + 1
+        for i in range(q_len):
+            if not keep[i].any():
+                continue
+            s = np.where(keep[i][None, :], S[i], -np.inf)
+            s = s - s.max(axis=1, keepdims=True)
+            P = np.exp(s)
+            P = P / P.sum(axis=1, keepdims=True)
+            out[b, i] = np.einsum("hl,lhd->hd", P, V)
+    return out

@@ -32,9 +32,20 @@
  *     "PagedAttention: The OS Analogy": the model sees a continuous logical
  *     sequence while the data is scattered over physical blocks.
  *
+ * Extension (oracle_decode_ex_f64): q_len query tokens per sequence, the last
+ * q_len cached tokens, each attending causally to the tokens up to its own
+ * position, optionally only to the most recent `window` of them.  Passages:
+ * speculative decoding checks several drafted tokens at once ("Modern LLM
+ * Inference ...", section 7.1); local attention restricts each token to the
+ * most recent K tokens (same notes, section 4.4 "Local Attention").
+ *
  * Readings where the pages are silent:
  *   - seq_lens[b] counts the cached tokens; the single decode query attends to
  *     all of them (no causal mask for one query token).
+ *   - With q_len query tokens, query i is the token at position
+ *     L - q_len + i and attends to positions [lo, L - q_len + i]; window W > 0
+ *     gives lo = max(0, L - q_len + i - W + 1) (the query's own token counts
+ *     as one of the W).  An empty range gives zeros.
  *   - L_b == 0 gives an all-zero output row.
  *   - A block id outside [0, num_blocks) or L_b outside [0, max_blocks*bs]
  *     gives NaN for the affected rows and a non-zero return code.
@@ -68,11 +79,18 @@ static double load_elem(const void *base, int64_t idx, int dtype)
     return (double)f;
 }
 
-/* One output row out[0..D) for sequence b, query head h.  Returns a status. */
+/*
+ * One output row out[0..D) for sequence b, query token i of q_len, query head
+ * h.  Query i sits at position p = L - q_len + i of the sequence (the q_len
+ * new tokens are the last ones in the cache) and attends to tokens
+ * [lo, p], lo = max(0, p - window + 1) when window > 0, else 0 (causal, and
+ * local attention keeps only the most recent `window` tokens).  An empty range
+ * gives zeros.  Returns a status.
+ */
 static int decode_row(const void *q, const void *k_pool, const void *v_pool,
                       const int32_t *block_table, const int32_t *seq_lens, int dtype,
-                      int Hq, int Hkv, int D, int block_size, int64_t num_blocks,
-                      int max_blocks, double scale, int b, int h, double *out)
+                      int q_len, int Hq, int Hkv, int D, int block_size, int64_t num_blocks,
+                      int max_blocks, int window, double scale, int b, int i, int h, double *out)
 {
     const int G = Hq / Hkv;
     const int kv = h / G;
@@ -84,20 +102,25 @@ static int decode_row(const void *q, const void *k_pool, const void *v_pool,
         return ORACLE_ERR_SEQ_LEN;
     }
     for (d = 0; d < D; ++d) out[d] = 0.0;
-    if (L == 0) return ORACLE_OK;
+    const int64_t p = L - q_len + i;
+    int64_t lo = 0;
+    if (window > 0 && p - window + 1 > 0) lo = p - window + 1;
+    const int64_t n = p - lo + 1;
+    if (n <= 0) return ORACLE_OK;
 
-    /* Gather: physical (block, slot) of every logical token, checked first. */
-    int64_t *row_base = (int64_t *)malloc((size_t)L * sizeof(int64_t));
-    double *s = (double *)malloc((size_t)L * sizeof(double));
+    /* Gather: physical (block, slot) of every attended token, checked first. */
+    int64_t *row_base = (int64_t *)malloc((size_t)n * sizeof(int64_t));
+    double *s = (double *)malloc((size_t)n * sizeof(double));
     if (!row_base || !s) {
         free(row_base);
         free(s);
         for (d = 0; d < D; ++d) out[d] = NAN;
         return ORACLE_ERR_ARG;
     }
-    for (int64_t t = 0; t < L; ++t) {
-        int64_t phys = block_table[(int64_t)b * max_blocks + t / block_size];
-        int64_t slot = t % block_size;
+    for (int64_t t = 0; t < n; ++t) {
+        const int64_t tok = lo + t;
+        int64_t phys = block_table[(int64_t)b * max_blocks + tok / block_size];
+        int64_t slot = tok % block_size;
         if (phys < 0 || phys >= num_blocks) {
             free(row_base);
             free(s);
@@ -108,9 +131,9 @@ static int decode_row(const void *q, const void *k_pool, const void *v_pool,
         row_base[t] = ((phys * block_size + slot) * Hkv + kv) * (int64_t)D;
     }
 
-    /* Scores s_t = scale * <q, k_t>. */
-    const int64_t q_base = ((int64_t)b * Hq + h) * (int64_t)D;
-    for (int64_t t = 0; t < L; ++t) {
+    /* Scores s_t = scale * <q, k_t>; q layout [B, q_len, Hq, D]. */
+    const int64_t q_base = (((int64_t)b * q_len + i) * Hq + h) * (int64_t)D;
+    for (int64_t t = 0; t < n; ++t) {
         double dot = 0.0;
         for (d = 0; d < D; ++d) {
             dot += load_elem(q, q_base + d, dtype) * load_elem(k_pool, row_base[t] + d, dtype);
@@ -120,15 +143,15 @@ static int decode_row(const void *q, const void *k_pool, const void *v_pool,
 
     /* Softmax weights, max-subtracted for range, then the weighted mean of V. */
     double m = s[0];
-    for (int64_t t = 1; t < L; ++t) {
+    for (int64_t t = 1; t < n; ++t) {
         if (s[t] > m) m = s[t];
     }
     double z = 0.0;
-    for (int64_t t = 0; t < L; ++t) {
+    for (int64_t t = 0; t < n; ++t) {
         s[t] = exp(s[t] - m);
         z += s[t];
     }
-    for (int64_t t = 0; t < L; ++t) {
+    for (int64_t t = 0; t < n; ++t) {
         for (d = 0; d < D; ++d) {
             out[d] += s[t] * load_elem(v_pool, row_base[t] + d, dtype);
         }
@@ -169,8 +192,8 @@ int oracle_decode_rows_f64(const void *q, const void *k_pool, const void *v_pool
     int status = ORACLE_OK;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t i = 0; i < n_rows; ++i) {
-        int r = decode_row(q, k_pool, v_pool, block_table, seq_lens, dtype, Hq, Hkv, D,
-                           block_size, num_blocks, max_blocks, scale, rows[2 * i],
+        int r = decode_row(q, k_pool, v_pool, block_table, seq_lens, dtype, 1, Hq, Hkv, D,
+                           block_size, num_blocks, max_blocks, 0, scale, rows[2 * i], 0,
                            rows[2 * i + 1], out + i * (int64_t)D);
         if (r) {
 #pragma omp critical
@@ -194,13 +217,47 @@ int oracle_decode_f64(const void *q, const void *k_pool, const void *v_pool,
     const int64_t n_rows = (int64_t)B * Hq;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t i = 0; i < n_rows; ++i) {
-        int r = decode_row(q, k_pool, v_pool, block_table, seq_lens, dtype, Hq, Hkv, D,
-                           block_size, num_blocks, max_blocks, scale, (int)(i / Hq),
+        int r = decode_row(q, k_pool, v_pool, block_table, seq_lens, dtype, 1, Hq, Hkv, D,
+                           block_size, num_blocks, max_blocks, 0, scale, (int)(i / Hq), 0,
                            (int)(i % Hq), out + i * (int64_t)D);
         if (r) {
 #pragma omp critical
             {
                 if (!status) status = r;
+            }
+        }
+    }
+    return status;
+}
+
+/*
+ * Several query tokens per sequence and an optional attention window:
+ * q and out are [B, q_len, Hq, D]; seq_lens count every cached token, the
+ * q_len query tokens included (they are the last q_len); window <= 0 means
+ * no window.  With q_len = 1 and window = 0 this is oracle_decode_f64.
+ */
+int oracle_decode_ex_f64(const void *q, const void *k_pool, const void *v_pool,
+                         const int32_t *block_table, const int32_t *seq_lens, int dtype, int B,
+                         int q_len, int Hq, int Hkv, int D, int block_size, int64_t num_blocks,
+                         int max_blocks, int window, double scale, double *out)
+{
+    int rc = check_args(dtype, B, Hq, Hkv, D, block_size, num_blocks, max_blocks);
+    if (rc) return rc;
+    if (q_len < 1) return ORACLE_ERR_ARG;
+    int status = ORACLE_OK;
+    const int64_t n_rows = (int64_t)B * q_len * Hq;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        const int h = (int)(r % Hq);
+        const int i = (int)((r / Hq) % q_len);
+        const int b = (int)(r / ((int64_t)Hq * q_len));
+        int st = decode_row(q, k_pool, v_pool, block_table, seq_lens, dtype, q_len, Hq, Hkv, D,
+                            block_size, num_blocks, max_blocks, window, scale, b, i, h,
+                            out + r * (int64_t)D);
+        if (st) {
+#pragma omp critical
+            {
+                if (!status) status = st;
             }
         }
     }

@@ -12,12 +12,13 @@ import torch
 
 from . import _lib
 from ._lib import PagedGQAError, STATUS_NAMES, strerror  # noqa: F401
+from .kv_cache import KVBlockManager, paged_kv_append, paged_kv_copy_blocks  # noqa: F401
 
 __all__ = [
     "PagedKVPool", "PagedGQAError", "paged_kv_pool_create", "paged_kv_pool_destroy",
     "paged_gqa_workspace_size", "paged_gqa_decode", "paged_gqa_get_error",
     "paged_gqa_auto_splits", "paged_gqa_decode_noalloc", "paged_gqa_noalloc_scratch_bytes",
-    "strerror", "decode",
+    "strerror", "decode", "KVBlockManager", "paged_kv_append", "paged_kv_copy_blocks",
 ]
 
 _DTYPES = {torch.float32: _lib.PGD_F32, torch.bfloat16: _lib.PGD_BF16}

@@ -11,6 +11,7 @@ import re
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libpaged_gqa.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "paged_gqa.h")
+HEADERS = [HEADER, os.path.join(os.path.dirname(HERE), "include", "paged_kv_manager.h")]
 
 PGD_F32 = 0
 PGD_BF16 = 1
@@ -19,6 +20,7 @@ STATUS_NAMES = {
     0: "PGD_OK", 1: "PGD_ERR_ARG", 2: "PGD_ERR_SHAPE", 3: "PGD_ERR_DTYPE", 4: "PGD_ERR_ALIGN",
     5: "PGD_ERR_WORKSPACE", 6: "PGD_ERR_CUDA", 7: "PGD_ERR_BLOCK_ID", 8: "PGD_ERR_SEQ_LEN",
     9: "PGD_ERR_UNSUPPORTED", 10: "PGD_ERR_TIMEOUT", 11: "PGD_ERR_TOO_LARGE",
+    20: "PGD_ERR_NO_BLOCKS", 21: "PGD_ERR_NO_SEQ", 22: "PGD_ERR_SEQ_EXISTS", 23: "PGD_ERR_SEQ_FULL",
 }
 globals().update({v: k for k, v in STATUS_NAMES.items()})
 
@@ -63,6 +65,25 @@ def load(path=LIB_PATH):
     lib.paged_gqa_decode_noalloc.restype = i32
     lib.paged_gqa_noalloc_scratch_bytes.argtypes = []
     lib.paged_gqa_noalloc_scratch_bytes.restype = sz
+    # KV write path (include/paged_kv_manager.h)
+    pi32 = ctypes.POINTER(ctypes.c_int32)
+    pint = ctypes.POINTER(ctypes.c_int)
+    lib.pgd_kvm_create.argtypes = [ctypes.POINTER(vp), i64, i32, i32, i32]
+    lib.pgd_kvm_destroy.argtypes = [vp]
+    lib.pgd_kvm_add_sequence.argtypes = [vp, i32]
+    lib.pgd_kvm_fork.argtypes = [vp, i32, i32]
+    lib.pgd_kvm_free_sequence.argtypes = [vp, i32]
+    lib.pgd_kvm_append_slots.argtypes = [vp, pint, i32, pi32, pi32, pi32, pint]
+    lib.pgd_kvm_block_tables.argtypes = [vp, pint, i32, pi32, i32, pi32]
+    lib.pgd_kvm_num_free.argtypes = [vp, ctypes.POINTER(i64)]
+    lib.pgd_kvm_ref_count.argtypes = [vp, i64, pint]
+    lib.paged_kv_copy_blocks.argtypes = [vp, vp, vp, i32, vp]
+    lib.paged_kv_append.argtypes = [vp, vp, vp, vp, i32, vp]
+    for name in ("pgd_kvm_create", "pgd_kvm_destroy", "pgd_kvm_add_sequence", "pgd_kvm_fork",
+                 "pgd_kvm_free_sequence", "pgd_kvm_append_slots", "pgd_kvm_block_tables",
+                 "pgd_kvm_num_free", "pgd_kvm_ref_count", "paged_kv_copy_blocks",
+                 "paged_kv_append"):
+        getattr(lib, name).restype = i32
     _lib = lib
     return lib
 
@@ -71,8 +92,10 @@ def strerror(status):
     return load().paged_gqa_strerror(int(status)).decode()
 
 
-def declared_functions(header=HEADER):
-    """Names of the functions include/paged_gqa.h declares."""
-    text = open(header).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(paged_\w+)\s*\(", text)))
+def declared_functions(headers=None):
+    """Names of the functions the headers under include/ declare."""
+    names = set()
+    for h in headers or HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b((?:paged|pgd)_\w+)\s*\(", text))
+    return sorted(names)

@@ -17,8 +17,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpaged_gqa.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cpp", "decode_simple.cu", "decode_tma_d64.cu", "decode_tma_d128.cu", "merge.cu",
-           "noalloc.cu"]
+SOURCES = ["api.cpp", "block_manager.cpp", "decode_simple.cu", "decode_tma_d64.cu",
+           "decode_tma_d128.cu", "kv_write.cu", "merge.cu", "noalloc.cu"]
 
 
 def nvcc():

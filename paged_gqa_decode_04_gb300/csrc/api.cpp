@@ -7,6 +7,7 @@
 
 #include <new>
 
+#include "paged_kv_manager.h"
 #include "pgd_internal.h"
 
 struct pgd_pool_s {
@@ -240,6 +241,7 @@ int paged_gqa_decode(pgd_pool_t pool, const void* q, int B, int Hq, const int32_
     a.num_blocks = p.num_blocks;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.num_parts = parts;
+    a.auto_parts = num_splits == 0;
     a.hg = hg;
     a.units = p.hkv / hg;
     a.tile_tokens = p.dtype == PGD_BF16 ? 128 / hg : kSimpleTileTokens;
@@ -289,6 +291,10 @@ const char* paged_gqa_strerror(int status) {
         case PGD_ERR_TIMEOUT: return "device pipeline wait timed out";
         case PGD_ERR_TOO_LARGE:
             return "request needs more scratch than the fixed no-alloc scratch array holds";
+        case PGD_ERR_NO_BLOCKS: return "no free block left in the pool";
+        case PGD_ERR_NO_SEQ: return "unknown sequence id";
+        case PGD_ERR_SEQ_EXISTS: return "sequence id already in use";
+        case PGD_ERR_SEQ_FULL: return "sequence holds its maximum number of blocks";
         default: return "unknown status";
     }
 }

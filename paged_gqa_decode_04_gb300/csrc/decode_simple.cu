@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(kSimpleThreads) decode_simple_kernel(DecodeArg
     __shared__ int64_t scratch[kSimpleThreads];
     __shared__ SpanStart ss;
     find_span_start(a.seq_lens, a.B, a.units, a.tile_tokens, a.max_blocks, a.block_size,
-                    a.num_parts, scratch, &ss, a.tile_base);
+                    a.num_parts, 1, scratch, &ss, a.tile_base);
     if (ss.r0 >= ss.r1) return;
 
     const int warp = threadIdx.x / 32;

@@ -51,6 +51,9 @@ namespace pgd {
 namespace tma {
 
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
+// With automatic splits, use fewer spans than CTAs when the call has fewer than
+// this many tiles per CTA: tiny calls then split runs into fewer pieces.
+constexpr int kMinTilesPerCta = 4;
 constexpr int kSmemBudget = 227 * 1024;
 
 // ----------------------------------------------------------------- PTX wrappers
@@ -190,6 +193,76 @@ struct StageDesc {
     int pad;
 };
 
+// Merge the pieces of a split run for the query rows one consumer warp owns
+// (m-tile `mt` of head `hgi` of the group) and write them to `ob` (the head's
+// G output rows).  Log-sum-exp combination in base 2: with lse_k = m_k +
+// log2 l_k and o_k the normalised partial of piece k,
+//     out = sum_k 2^(lse_k - M) o_k / sum_k 2^(lse_k - M),  M = max_k lse_k,
+// accumulated online.  Rows one after another; the lanes cover a row's
+// columns with float4 reads (two rows per pass when D = 64) and kPieceBatch
+// pieces are read before any is used, so a run of many pieces costs few L2
+// round trips.  Not inlined, so that its registers do not weigh on the tile
+// loop.
+constexpr int kPieceBatch = 4;
+
+template <class C>
+__device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int64_t t0, int64_t N, int64_t P,
+                                          int64_t c0, int npieces, bool first_is_tail, int hgi,
+                                          int mt, __nv_bfloat16* ob) {
+    constexpr int D = C::D;
+    constexpr int CPR = D / 4;             // float4 chunks per row
+    constexpr int RPP = 32 / CPR;          // rows per pass
+    const int lane = threadIdx.x % 32;
+    const int G = a.group;
+    const int piece_rows = C::HG * G;
+    const int r_lo = mt * 16;
+    const int r_hi = min(G, r_lo + C::ROWS);
+    const int col = (lane % CPR) * 4;
+    for (int rb = r_lo; rb < r_hi; rb += RPP) {
+        const int r = rb + lane / CPR;
+        const bool rok = r < r_hi;
+        const int64_t pr = (int64_t)(hgi * G + r);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float M = -INFINITY, W = 0.f;
+        for (int k0 = 0; k0 < npieces; k0 += kPieceBatch) {
+            float4 v[kPieceBatch];
+            float e[kPieceBatch];
+#pragma unroll
+            for (int u = 0; u < kPieceBatch; ++u) {
+                const int k = k0 + u;
+                const bool ok = rok && k < npieces;
+                // with P > N every non-empty span holds one tile: piece k is the
+                // owner of tile t0 + k; otherwise the pieces are CTAs c0, c0+1, ...
+                const int64_t c = P > N ? span_owner(t0 + k, N, P) : c0 + k;
+                const int64_t sl = c * 2 + ((first_is_tail && k == 0) ? 1 : 0);
+                v[u] = ok ? __ldcg(reinterpret_cast<const float4*>(a.part_o +
+                                                                   (sl * piece_rows + pr) * D + col))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                e[u] = ok ? __ldcg(a.part_lse + sl * piece_rows + pr) : -INFINITY;
+            }
+#pragma unroll
+            for (int u = 0; u < kPieceBatch; ++u) {
+                const float nm = fmaxf(M, e[u]);
+                const float base = nm == -INFINITY ? 0.f : nm;
+                const float sa = fast_exp2(M - base), sb = fast_exp2(e[u] - base);
+                M = nm;
+                W = W * sa + sb;
+                acc.x = acc.x * sa + v[u].x * sb;
+                acc.y = acc.y * sa + v[u].y * sb;
+                acc.z = acc.z * sa + v[u].z * sb;
+                acc.w = acc.w * sa + v[u].w * sb;
+            }
+        }
+        if (rok) {
+            const float w = 1.f / W;
+            uint2 pk;
+            pk.x = pack_bf16(acc.x * w, acc.y * w);
+            pk.y = pack_bf16(acc.z * w, acc.w * w);
+            *reinterpret_cast<uint2*>(ob + (int64_t)r * D + col) = pk;
+        }
+    }
+}
+
 // ----------------------------------------------------------------- the kernel
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
@@ -227,7 +300,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         aborted = 0;
         fence_barrier_init();
     }
-    find_span_start(a.seq_lens, a.B, a.units, T, a.max_blocks, bs, a.num_parts, scratch, &ss,
+    find_span_start(a.seq_lens, a.B, a.units, T, a.max_blocks, bs, a.num_parts,
+                    a.auto_parts ? kMinTilesPerCta : 1, scratch, &ss,
                     a.tile_base);  // ends with __syncthreads
 
     // Sequences that own no tiles: length 0 gives zeros, an out-of-range length
@@ -635,67 +709,23 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         __threadfence();
         __syncwarp();
         const int64_t t0 = dsc.run_start;
-        const int64_t N = ss.n_total, P = a.num_parts;
-        const int64_t c0 = span_owner(t0, N, P), c1 = span_owner(t0 + dsc.n_b - 1, N, P);
+        const int64_t N = ss.n_total, P = ss.parts;
+        // The pieces of run [t0, t0 + n_b): with P <= N every span holds at
+        // least one tile, so they are CTAs c0..c1; with P > N every span holds
+        // at most one tile, so piece k is the owner of tile t0 + k.
+        const int64_t c0 = span_owner(t0, N, P);
+        const int npieces = P > N ? dsc.n_b : (int)(span_owner(t0 + dsc.n_b - 1, N, P) - c0 + 1);
+        const bool first_is_tail = P <= N && span_begin(c0, N, P) < t0;
         int last = 0;
         if (lane == 0) {
-            int pieces = (int)(c1 - c0 + 1);
-            if (P > N) {
-                pieces = 0;
-                for (int64_t c = c0; c <= c1; ++c)
-                    pieces += span_begin(c, N, P) != span_begin(c + 1, N, P);
-            }
             int* ctr = a.counters + ((int64_t)dsc.b * a.hkv + kvh) * C::MT + mt;
-            last = atomicAdd(ctr, 1) == pieces - 1;
+            last = atomicAdd(ctr, 1) == npieces - 1;
             if (last) atomicExch(ctr, 0);
         }
         last = __shfl_sync(0xffffffffu, last, 0);
         if (!last) continue;
         __threadfence();
-        float M0 = -INFINITY, M1 = -INFINITY, W0 = 0.f, W1 = 0.f;
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-        for (int64_t c = c0; c <= c1; ++c) {
-            const int64_t sb = span_begin(c, N, P);
-            if (sb == span_begin(c + 1, N, P)) continue;
-            const int64_t sl = c * 2 + (sb < t0 ? 1 : 0);
-            const float* pc = a.part_o + sl * piece_rows * D;
-            const float* lc = a.part_lse + sl * piece_rows;
-            const float e0 = row0_ok ? __ldcg(lc + prow0) : 0.f;
-            const float e1 = row1_ok ? __ldcg(lc + prow1) : 0.f;
-            const float n0 = fmaxf(M0, e0), n1 = fmaxf(M1, e1);
-            const float a0 = fast_exp2(M0 - n0), b0 = fast_exp2(e0 - n0);
-            const float a1 = fast_exp2(M1 - n1), b1 = fast_exp2(e1 - n1);
-            M0 = n0;
-            M1 = n1;
-            W0 = W0 * a0 + b0;
-            W1 = W1 * a1 + b1;
-#pragma unroll
-            for (int n = 0; n < D / 8; ++n) {
-                if (row0_ok) {
-                    const float2 u = __ldcg(
-                        reinterpret_cast<const float2*>(pc + (int64_t)prow0 * D + n * 8 + tig * 2));
-                    o[n][0] = o[n][0] * a0 + u.x * b0;
-                    o[n][1] = o[n][1] * a0 + u.y * b0;
-                }
-                if (row1_ok) {
-                    const float2 u = __ldcg(
-                        reinterpret_cast<const float2*>(pc + (int64_t)prow1 * D + n * 8 + tig * 2));
-                    o[n][2] = o[n][2] * a1 + u.x * b1;
-                    o[n][3] = o[n][3] * a1 + u.y * b1;
-                }
-            }
-        }
-        const float w0 = 1.f / W0, w1 = 1.f / W1;
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-            if (row0_ok)
-                *reinterpret_cast<uint32_t*>(ob + (int64_t)row0 * D + n * 8 + tig * 2) =
-                    pack_bf16(o[n][0] * w0, o[n][1] * w0);
-            if (row1_ok)
-                *reinterpret_cast<uint32_t*>(ob + (int64_t)row1 * D + n * 8 + tig * 2) =
-                    pack_bf16(o[n][2] * w1, o[n][3] * w1);
-        }
+        merge_pieces<C>(a, t0, N, P, c0, npieces, first_is_tail, hgi, mt, ob);
     }
 }
 

@@ -51,17 +51,20 @@ __device__ __forceinline__ void latch_error(int* err, int code) {
 // Start of this CTA's span, found with a block-wide scan over the sequences.
 struct SpanStart {
     int64_t n_total;   // N
+    int64_t parts;     // spans in use (<= gridDim.x)
     int64_t r0, r1;    // this CTA's span
     int b;             // sequence holding r0 (valid when r0 < r1)
     int64_t b_base;    // tile_base[b]
 };
 
 // Every thread of the block must call this.  `scratch` is >= blockDim.x int64
-// of shared memory, `out` a shared SpanStart.  CTA 0 also writes
-// tile_base[0..B] to global memory for the merge kernel.
+// of shared memory, `out` a shared SpanStart.  With min_tiles > 1 the spans in
+// use are min(parts, ceil(N / min_tiles)) (at least 1) and CTAs beyond them get
+// an empty span; with min_tiles == 1 all `parts` spans are used.  CTA 0 also writes tile_base[0..B] to global memory for the merge
+// kernel.
 __device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int B, int units,
                                        int T, int max_blocks, int block_size, int64_t parts,
-                                       int64_t* scratch, SpanStart* out,
+                                       int min_tiles, int64_t* scratch, SpanStart* out,
                                        int64_t* __restrict__ tile_base_out) {
     const int nt = blockDim.x;
     const int tid = threadIdx.x;
@@ -80,9 +83,16 @@ __device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int
             scratch[i] = run;
             run += v;
         }
+        int64_t p = parts;
+        if (min_tiles > 1) {  // fewer spans only when asked for
+            p = (run + min_tiles - 1) / min_tiles;
+            p = p < parts ? p : parts;
+            p = p > 0 ? p : 1;
+        }
         out->n_total = run;
-        out->r0 = span_begin(blockIdx.x, run, parts);
-        out->r1 = span_begin(blockIdx.x + 1, run, parts);
+        out->parts = p;
+        out->r0 = blockIdx.x < p ? span_begin(blockIdx.x, run, p) : run;
+        out->r1 = blockIdx.x < p ? span_begin(blockIdx.x + 1, run, p) : run;
         out->b = -1;
         out->b_base = 0;
     }

@@ -52,6 +52,7 @@ struct DecodeArgs {
     int64_t num_blocks;
     float scale_log2;      // scale * log2(e): logits kept in base-2 units
     int num_parts;         // CTAs of the decode grid (spans of the tile sequence)
+    int auto_parts;        // num_parts came from num_splits == 0 (kernel may use fewer)
     int hg;                // KV heads per unit of work
     int units;             // units per sequence, Hkv / hg
     int tile_tokens;       // tokens per tile

@@ -30,7 +30,7 @@ import math
 import numpy as np
 import torch
 
-from oracle.brute import bf16_bits_to_f64, brute_decode
+from oracle.brute import bf16_bits_to_f64, brute_decode, brute_decode_ex
 
 
 # ----------------------------------------------------------------------------- inputs
@@ -314,6 +314,110 @@ def pin_rows_match_full(orc):
         assert np.array_equal(sub[i], out[b, h])
 
 
+# ----------------------------------------------------------------- extension pins
+# Several query tokens per sequence (speculative verification, "Modern LLM
+# Inference ...", section 7.1) and local attention over the most recent W
+# tokens (same notes, section 4.4 "Local Attention").
+def _ex_case(rng, B, q_len, Hq, Hkv, D, bs, lens, dtype="f32", max_blocks=None):
+    q, k, v, t, L = paged_case(rng, B, Hq * q_len, Hkv * q_len, D, bs, lens, dtype,
+                               max_blocks=max_blocks)
+    # reuse the generator's shapes, then reshape q to [B, q_len, Hq, D]
+    q = q.reshape(B, q_len, Hq, D)
+    k = k[:, :, :Hkv].copy()
+    v = v[:, :, :Hkv].copy()
+    return q, k, v, t, L
+
+
+def pin_ex_reduces_to_single_query(orc):
+    """q_len = 1 and no window is exactly the single-query decode."""
+    rng = np.random.default_rng(43)
+    q, k, v, t, L = paged_case(rng, 3, 8, 2, 16, 4, [9, 1, 14], "bf16")
+    a, _ = orc.decode_f64(q, k, v, t, L, 0.3)
+    b, _ = orc.decode_ex_f64(q[:, None], k, v, t, L, 0.3, 0)
+    assert np.array_equal(a, b[:, 0])
+
+
+def pin_ex_brute_force(orc):
+    """Dense masked formulation, several query counts and windows."""
+    rng = np.random.default_rng(47)
+    for q_len, window, dt in ((3, 0, "f32"), (4, 5, "bf16"), (2, 1, "f32"), (5, 100, "f32"),
+                              (1, 3, "bf16")):
+        q, k, v, t, L = _ex_case(rng, 3, q_len, 4, 2, 8, 4, [9, 17, 6], dt)
+        out, rc = orc.decode_ex_f64(q, k, v, t, L, 0.35, window)
+        ref = brute_decode_ex(q, k, v, t, L, 0.35, window)
+        assert rc == 0 and np.abs(out - ref).max() <= 1e-12, (q_len, window, dt)
+
+
+def pin_ex_causal_prefix(orc):
+    """Query i of a q_len call equals a single-query call on the sequence cut
+    right after query i's own token."""
+    rng = np.random.default_rng(53)
+    q_len = 4
+    q, k, v, t, L = _ex_case(rng, 2, q_len, 6, 3, 8, 4, [11, 7], "bf16")
+    out, _ = orc.decode_ex_f64(q, k, v, t, L, 0.25, 0)
+    for i in range(q_len):
+        cut = L - q_len + i + 1
+        one, _ = orc.decode_f64(q[:, i], k, v, t, cut, 0.25)
+        assert np.array_equal(out[:, i], one), i
+
+
+def pin_ex_window_is_recent_tokens(orc):
+    """A window of W equals attention over a sequence holding only the W most
+    recent tokens; W = 1 returns the query token's own V row."""
+    rng = np.random.default_rng(59)
+    q, k, v, t, L = _ex_case(rng, 2, 1, 4, 2, 8, 4, [13, 6], "bf16")
+    for W in (1, 3, 6, 20):
+        out, _ = orc.decode_ex_f64(q, k, v, t, L, 0.4, W)
+        for b in range(2):
+            n = min(W, int(L[b]))
+            lo = int(L[b]) - n
+            kk = np.zeros((1, n, 2, 8), dtype=k.dtype)
+            vv = np.zeros_like(kk)
+            for j in range(n):
+                tok = lo + j
+                kk[0, j] = k[t[b, tok // 4], tok % 4]
+                vv[0, j] = v[t[b, tok // 4], tok % 4]
+            one, _ = orc.decode_f64(q[b:b + 1, 0], kk, vv, np.zeros((1, 1), np.int32),
+                                    np.array([n], np.int32), 0.4)
+            assert np.array_equal(out[b, 0], one[0]), (W, b)
+        if W == 1:
+            vf = as_f64(v)
+            for b in range(2):
+                tok = int(L[b]) - 1
+                for h in range(4):
+                    assert np.array_equal(out[b, 0, h], vf[t[b, tok // 4], tok % 4, h // 2])
+
+
+def pin_ex_blocks_before_window_unread(orc):
+    """Blocks older than the window may be discarded (table entry -1): the
+    result does not change; discarding a block the window still needs is an
+    error.  Sequence 0: L 17, two queries at positions 15 and 16, window 5, so
+    tokens 11..16 are read (blocks 2, 3, 4 of 4-token blocks)."""
+    rng = np.random.default_rng(61)
+    q, k, v, t, L = _ex_case(rng, 2, 2, 4, 2, 8, 4, [17, 9], "f32")
+    a, rc = orc.decode_ex_f64(q, k, v, t, L, 0.3, 5)
+    t2 = t.copy()
+    t2[0, :2] = -1                     # tokens 0..7: outside every window of sequence 0
+    b, rc2 = orc.decode_ex_f64(q, k, v, t2, L, 0.3, 5)
+    assert rc == rc2 == 0 and np.array_equal(a, b)
+    t3 = t.copy()
+    t3[0, 2] = -1                      # tokens 8..11: token 11 is still in a window
+    _, rc3 = orc.decode_ex_f64(q, k, v, t3, L, 0.3, 5)
+    assert rc3 == 2
+
+
+def pin_ex_empty_rows_are_zero(orc):
+    """A query whose position is before the sequence start (L < q_len) has an
+    empty range and gives zeros; the others are unaffected."""
+    rng = np.random.default_rng(67)
+    q, k, v, t, L = _ex_case(rng, 1, 4, 4, 2, 8, 4, [2], "f32")
+    out, rc = orc.decode_ex_f64(q, k, v, t, L, 0.3, 0)
+    assert rc == 0
+    assert np.array_equal(out[0, :2], np.zeros_like(out[0, :2]))
+    ref = brute_decode_ex(q, k, v, t, L, 0.3, 0)
+    assert np.abs(out - ref).max() <= 1e-12
+
+
 PINS = [
     pin_brute_force,
     pin_paged_equals_contiguous,
@@ -328,4 +432,10 @@ PINS = [
     pin_edge_statuses,
     pin_bf16_widening,
     pin_rows_match_full,
+    pin_ex_reduces_to_single_query,
+    pin_ex_brute_force,
+    pin_ex_causal_prefix,
+    pin_ex_window_is_recent_tokens,
+    pin_ex_blocks_before_window_unread,
+    pin_ex_empty_rows_are_zero,
 ]

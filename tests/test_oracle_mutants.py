@@ -16,15 +16,20 @@ SRC = os.path.join(ROOT, "oracle", "oracle.c")
 
 MUTANTS = {
     "head_group_modulo": ("const int kv = h / G;", "const int kv = h % Hkv;"),
-    "slot_reversed": ("int64_t slot = t % block_size;",
-                      "int64_t slot = (block_size - 1) - t % block_size;"),
+    "slot_reversed": ("int64_t slot = tok % block_size;",
+                      "int64_t slot = (block_size - 1) - tok % block_size;"),
     "scale_dropped": ("s[t] = scale * dot;", "s[t] = dot;"),
     "max_is_min": ("if (s[t] > m) m = s[t];", "if (s[t] < m) m = s[t];"),
     "not_normalised": ("out[d] /= z;", "out[d] /= 1.0;"),
     "exp_sign": ("s[t] = exp(s[t] - m);", "s[t] = exp(m - s[t]);"),
     "exp_base_two": ("s[t] = exp(s[t] - m);", "s[t] = exp2(s[t] - m);"),
     "values_from_k": ("out[d] += s[t] * load_elem(v_pool,", "out[d] += s[t] * load_elem(k_pool,"),
-    "query_head_index": ("((int64_t)b * Hq + h) * (int64_t)D", "((int64_t)b * Hq + kv) * (int64_t)D"),
+    "query_head_index": ("* Hq + h) * (int64_t)D", "* Hq + kv) * (int64_t)D"),
+    "query_token_index": ("((int64_t)b * q_len + i) * Hq", "((int64_t)b * q_len) * Hq"),
+    "causal_shifted": ("const int64_t p = L - q_len + i;", "const int64_t p = L - q_len + i - 1;"),
+    "window_off_by_one": ("if (window > 0 && p - window + 1 > 0) lo = p - window + 1;",
+                          "if (window > 0 && p - window > 0) lo = p - window;"),
+    "window_ignored": ("if (window > 0 && p - window + 1 > 0) lo = p - window + 1;", ""),
     "bf16_shift": ("<< 16;", "<< 15;"),
     "pool_axes_swapped": ("((phys * block_size + slot) * Hkv + kv)",
                           "((phys * Hkv + kv) * block_size + slot)"),

@@ -101,3 +101,16 @@ def test_partition_covers_balances_and_merges(seed):
         for cs in written:
             assert cs not in slots_written
             slots_written.add(cs)
+
+
+def spans_in_use(N, P, min_tiles):
+    """The kernel's rule: fewer spans only when asked (min_tiles > 1)."""
+    if min_tiles <= 1:
+        return P
+    return max(1, min(P, -(-N // min_tiles)))
+
+
+@pytest.mark.parametrize("N,P,mt,want", [(6, 152, 4, 2), (12, 152, 1, 152), (1000, 152, 4, 152),
+                                         (0, 152, 4, 1), (7, 3, 4, 2)])
+def test_spans_in_use(N, P, mt, want):
+    assert spans_in_use(N, P, mt) == want
