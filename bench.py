@@ -251,6 +251,37 @@ def run_ours(args, world, rank, local):
         pgd.paged_gqa_decode(pool, w.q, w.block_table, w.seq_lens, w.scale, out=out,
                              workspace=ws, stream=stream)
 
+    op_note = "decode: one query token per sequence"
+    if args.op == "decode_ex":
+        # q_len query tokens per sequence (the last q_len cached ones), optional window
+        g = torch.Generator(device=dev)
+        g.manual_seed(w.seed + 7)
+        q_ex = torch.randn((w.B, args.q_len, w.Hq, w.D), generator=g, device=dev).to(w.q.dtype)
+        out = torch.empty_like(q_ex)
+        nbytes = accounting.algorithmic_bytes_ex(w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt,
+                                                 args.q_len, args.window)
+        ws = torch.zeros(max(256, pgd.paged_gqa_workspace_size_ex(pool, w.B, args.q_len, w.Hq)),
+                         dtype=torch.uint8, device=dev)
+
+        def step():
+            pgd.paged_gqa_decode_ex(pool, q_ex, w.block_table, w.seq_lens, w.scale,
+                                    window=args.window, out=out, workspace=ws, stream=stream)
+
+        op_note = "decode_ex: %d query tokens per sequence, window %d" % (args.q_len, args.window)
+    elif args.op == "append":
+        # store one new token per sequence (K and V rows) at distinct slots
+        g = torch.Generator(device=dev)
+        g.manual_seed(w.seed + 9)
+        k_new = torch.randn((w.B, w.Hkv, w.D), generator=g, device=dev).to(w.q.dtype)
+        v_new = torch.randn((w.B, w.Hkv, w.D), generator=g, device=dev).to(w.q.dtype)
+        slots = torch.arange(w.B, dtype=torch.int32, device=dev) * w.block_size
+        nbytes = 2 * 2 * k_new.numel() * k_new.element_size() + 4 * w.B
+
+        def step():
+            pgd.paged_kv_append(pool, k_new, v_new, slots, stream=stream)
+
+        op_note = "append: one new token per sequence (read + write of K and V rows)"
+
     step()
     status = pgd.paged_gqa_get_error(pool, stream)
     if status != 0:
@@ -295,6 +326,22 @@ def run_ours(args, world, rank, local):
     status = pgd.paged_gqa_get_error(pool, stream)
     if status != 0:
         raise RuntimeError("device error: %s" % pgd.strerror(status))
+
+    if args.op != "decode":
+        if rank == 0:
+            peak, peak_src = peak_hbm()
+            gbs = whole_job_gbs(nbytes, t_ms, world)
+            print(json.dumps({
+                "metric": METRIC, "op": args.op, "value": round(gbs, 2), "unit": "GB/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(t_ms, 5), "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+                "config": {"workload": describe(w), "op": op_note,
+                           "algorithmic_bytes_per_step": nbytes},
+                "pct_of_peak": round(100 * gbs / world / peak, 2),
+                "peak_source": "%s (%.0f GB/s)" % (peak_src, peak),
+                "clocks": clk.summary()}), flush=True)
+        return
 
     # end to end through the public API: per step, copy the step inputs (q, block
     # table, lengths) from pinned host memory, decode, read the output back.  The
@@ -372,6 +419,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="decode", choices=["decode", "decode_ex", "append"],
+                    help="decode (the headline), decode_ex (several query tokens and/or a "
+                         "window), append (KV write path)")
+    ap.add_argument("--q-len", type=int, default=4)
+    ap.add_argument("--window", type=int, default=0)
     ap.add_argument("--profile", action="store_true",
                     help="only W + K step launches (for ncu); prints no bench line")
     args = ap.parse_args()

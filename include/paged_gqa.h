@@ -133,6 +133,32 @@ int paged_gqa_decode(pgd_pool_t pool, const void *q, int B, int Hq, const int32_
                      void *workspace, size_t workspace_bytes, int num_splits, void *stream);
 
 /*
+ * Decode with several query tokens per sequence and an optional attention
+ * window: speculative verification of drafted tokens ("Modern LLM Inference
+ * ...", section 7.1) and local attention over the most recent tokens (same
+ * notes, section 4.4 "Local Attention").
+ *   q, out       [B, q_len, Hq, D], bfloat16 pools only (PGD_ERR_UNSUPPORTED
+ *                for float32 with q_len > 1 or window > 0)
+ *   seq_lens     cached tokens per sequence, the q_len query tokens included:
+ *                they are the last q_len, already appended.  Query i sits at
+ *                position p = Lb - q_len + i and attends causally to positions
+ *                [lo, p], lo = max(0, p - window + 1) when window > 0, else 0.
+ *                A query with p < 0 gets zeros.
+ *   window       0 = no window.  Blocks that lie wholly before every query's
+ *                window are never read, so their table entries may be -1.
+ * q_len * Hq / Hkv must be at most 64.  The workspace size comes from
+ * paged_gqa_workspace_size_ex.  q_len = 1 with window = 0 is paged_gqa_decode.
+ */
+int paged_gqa_decode_ex(pgd_pool_t pool, const void *q, int B, int q_len, int Hq,
+                        const int32_t *block_table, int max_blocks, const int32_t *seq_lens,
+                        int window, float scale, void *out, void *workspace,
+                        size_t workspace_bytes, int num_splits, void *stream);
+
+/* Workspace bytes for paged_gqa_decode_ex with q_len query tokens. */
+int paged_gqa_workspace_size_ex(pgd_pool_t pool, int B, int q_len, int Hq, int num_splits,
+                                size_t *bytes);
+
+/*
  * Synchronise `stream`, then read and clear the handle's latched device error.
  * Returns PGD_OK when no error was latched, the latched pgd_status otherwise,
  * or PGD_ERR_CUDA when the synchronisation itself failed.

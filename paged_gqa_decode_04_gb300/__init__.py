@@ -17,7 +17,8 @@ from .kv_cache import KVBlockManager, paged_kv_append, paged_kv_copy_blocks  # n
 __all__ = [
     "PagedKVPool", "PagedGQAError", "paged_kv_pool_create", "paged_kv_pool_destroy",
     "paged_gqa_workspace_size", "paged_gqa_decode", "paged_gqa_get_error",
-    "paged_gqa_auto_splits", "paged_gqa_decode_noalloc", "paged_gqa_noalloc_scratch_bytes",
+    "paged_gqa_auto_splits", "paged_gqa_decode_ex", "paged_gqa_workspace_size_ex",
+    "paged_gqa_decode_noalloc", "paged_gqa_noalloc_scratch_bytes",
     "strerror", "decode", "KVBlockManager", "paged_kv_append", "paged_kv_copy_blocks",
 ]
 
@@ -143,6 +144,48 @@ def paged_gqa_decode(pool, q, block_table, seq_lens, scale, out=None, workspace=
                                 block_table.shape[1], seq_lens.data_ptr(), float(scale),
                                 out.data_ptr(), workspace.data_ptr(), workspace.numel(),
                                 int(num_splits), _stream_handle(stream)), "paged_gqa_decode")
+    return out
+
+
+def paged_gqa_workspace_size_ex(pool, B, q_len, Hq, num_splits=0):
+    n = ctypes.c_size_t()
+    _check(_lib.load().paged_gqa_workspace_size_ex(pool.handle, int(B), int(q_len), int(Hq),
+                                                   int(num_splits), ctypes.byref(n)),
+           "paged_gqa_workspace_size_ex")
+    return n.value
+
+
+def paged_gqa_decode_ex(pool, q, block_table, seq_lens, scale, window=0, out=None,
+                        workspace=None, num_splits=0, stream=None):
+    """Several query tokens per sequence and an optional window.
+
+    q [B, q_len, Hq, D] (bf16): the last q_len cached tokens of each sequence,
+    each attending causally to the positions before it, or only to the
+    `window` most recent ones when window > 0.  Returns out [B, q_len, Hq, D].
+    """
+    lib = _lib.load()
+    if q.dim() != 4 or block_table.dim() != 2 or seq_lens.dim() != 1:
+        raise ValueError("q must be [B,q_len,Hq,D], block_table [B,max_blocks], seq_lens [B]")
+    if q.dtype != pool.dtype:
+        raise TypeError("q dtype must match the pool")
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    for t in (q, block_table, seq_lens):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    B, q_len, Hq, D = q.shape
+    if D != pool.head_dim or block_table.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("shape mismatch between q, tables and pool")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        nbytes = paged_gqa_workspace_size_ex(pool, B, q_len, Hq, num_splits)
+        workspace = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    _check(lib.paged_gqa_decode_ex(pool.handle, q.data_ptr(), B, q_len, Hq,
+                                   block_table.data_ptr(), block_table.shape[1],
+                                   seq_lens.data_ptr(), int(window), float(scale),
+                                   out.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                   int(num_splits), _stream_handle(stream)), "paged_gqa_decode_ex")
     return out
 
 

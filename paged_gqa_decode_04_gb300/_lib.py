@@ -60,6 +60,11 @@ def load(path=LIB_PATH):
     lib.paged_gqa_auto_splits.restype = i32
     lib.paged_gqa_strerror.argtypes = [i32]
     lib.paged_gqa_strerror.restype = ctypes.c_char_p
+    lib.paged_gqa_decode_ex.argtypes = [vp, vp, i32, i32, i32, vp, i32, vp, i32, ctypes.c_float,
+                                        vp, vp, sz, i32, vp]
+    lib.paged_gqa_decode_ex.restype = i32
+    lib.paged_gqa_workspace_size_ex.argtypes = [vp, i32, i32, i32, i32, ctypes.POINTER(sz)]
+    lib.paged_gqa_workspace_size_ex.restype = i32
     lib.paged_gqa_decode_noalloc.argtypes = [vp, vp, i32, i32, vp, i32, vp, ctypes.c_float, vp,
                                              i32, vp]
     lib.paged_gqa_decode_noalloc.restype = i32

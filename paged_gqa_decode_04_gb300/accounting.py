@@ -54,3 +54,29 @@ def paged_waste(length, block_size):
 def flattened_tokens(lengths):
     """Tokens of a batch packed with no padding."""
     return int(np.sum(lengths))
+
+
+def tokens_read(L, q_len=1, window=0):
+    """Cached tokens a call reads for one sequence: from the earliest token any
+    of its q_len queries attends to (window W: max(0, L - q_len - W + 1)) to the
+    end."""
+    L = int(L)
+    lo = max(0, L - q_len - window + 1) if window > 0 else 0
+    return max(0, L - lo)
+
+
+def algorithmic_bytes_ex(lens, hq, hkv, d, block_size, elt, q_len=1, window=0):
+    """Algorithmic bytes of a multi-token / windowed call: K/V of the tokens
+    read, q and out for q_len tokens per sequence, the table words of the
+    blocks read and seq_lens."""
+    lens = np.asarray(lens, dtype=np.int64)
+    kv = 0
+    words = 0
+    for L in lens.tolist():
+        n = tokens_read(L, q_len, window)
+        kv += n * kv_bytes_per_token(hkv, d, elt)
+        if n:
+            lo = L - n
+            words += (L - 1) // block_size - lo // block_size + 1
+    B = int(lens.size)
+    return kv + 2 * B * q_len * hq * d * elt + 4 * (B + words)

@@ -80,19 +80,19 @@ int resolve_parts(const Pool& p, int num_splits) {
 
 const Pool& pool_desc(pgd_pool_t h) { return h->p; }
 
-int choose_hg(const Pool& p, int group) {
+int choose_hg(const Pool& p, int rows) {
     if (p.dtype != PGD_BF16) return 1;
-    const int mt = (group + 15) / 16;
+    const int mt = (rows + 15) / 16;
     const int cap = mt == 1 ? 8 : mt == 2 ? 4 : 2;  // at most 8 consumer warps
     int hg = 8;
     while (hg > 1 && (p.hkv % hg != 0 || hg > cap)) hg /= 2;
     return hg;
 }
 
-WorkspaceLayout workspace_layout(int B, int hkv, int group, int hg, int d, int parts) {
+WorkspaceLayout workspace_layout(int B, int hkv, int rows_per_head, int hg, int d, int parts) {
     WorkspaceLayout w;
-    const int mtiles = (group + 15) / 16;
-    const size_t rows = (size_t)hg * group;  // rows of one partial result
+    const int mtiles = (rows_per_head + 15) / 16;
+    const size_t rows = (size_t)hg * rows_per_head;  // rows of one partial result
     w.counters_off = 0;
     w.tile_base_off = round_up((size_t)B * hkv * mtiles * sizeof(int), 256);
     w.part_lse_off = w.tile_base_off + round_up((size_t)(B + 1) * sizeof(int64_t), 256);
@@ -182,32 +182,44 @@ int paged_gqa_auto_splits(pgd_pool_t pool, int* num_splits) {
     return PGD_OK;
 }
 
-int paged_gqa_workspace_size(pgd_pool_t pool, int B, int Hq, int num_splits, size_t* bytes) {
-    if (!pool || !bytes || B < 0 || Hq < 1 || num_splits < 0 || num_splits > (1 << 20))
+int paged_gqa_workspace_size_ex(pgd_pool_t pool, int B, int q_len, int Hq, int num_splits,
+                                size_t* bytes) {
+    if (!pool || !bytes || B < 0 || q_len < 1 || Hq < 1 || num_splits < 0 ||
+        num_splits > (1 << 20))
         return PGD_ERR_ARG;
     const Pool& p = pool->p;
-    if (Hq % p.hkv != 0 || Hq / p.hkv > kMaxGroup) return PGD_ERR_SHAPE;
-    const int G = Hq / p.hkv;
-    *bytes = workspace_layout(B, p.hkv, G, choose_hg(p, G), p.d, resolve_parts(p, num_splits)).total;
+    if (Hq % p.hkv != 0) return PGD_ERR_SHAPE;
+    const int rows = q_len * (Hq / p.hkv);
+    if (rows > kMaxGroup) return PGD_ERR_SHAPE;
+    *bytes = workspace_layout(B, p.hkv, rows, choose_hg(p, rows), p.d,
+                              resolve_parts(p, num_splits)).total;
     return PGD_OK;
 }
 
-int paged_gqa_decode(pgd_pool_t pool, const void* q, int B, int Hq, const int32_t* block_table,
-                     int max_blocks, const int32_t* seq_lens, float scale, void* out,
-                     void* workspace, size_t workspace_bytes, int num_splits, void* stream) {
-    if (!pool || B < 0 || Hq < 1 || max_blocks < 0 || num_splits < 0 || num_splits > (1 << 20))
+int paged_gqa_workspace_size(pgd_pool_t pool, int B, int Hq, int num_splits, size_t* bytes) {
+    return paged_gqa_workspace_size_ex(pool, B, 1, Hq, num_splits, bytes);
+}
+
+int paged_gqa_decode_ex(pgd_pool_t pool, const void* q, int B, int q_len, int Hq,
+                        const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
+                        int window, float scale, void* out, void* workspace,
+                        size_t workspace_bytes, int num_splits, void* stream) {
+    if (!pool || B < 0 || q_len < 1 || Hq < 1 || max_blocks < 0 || num_splits < 0 ||
+        num_splits > (1 << 20) || window < 0)
         return PGD_ERR_ARG;
     if (!isfinite(scale)) return PGD_ERR_ARG;
     const Pool& p = pool->p;
     if (Hq % p.hkv != 0) return PGD_ERR_SHAPE;
     const int G = Hq / p.hkv;
-    if (G > kMaxGroup) return PGD_ERR_SHAPE;
+    const int rows = q_len * G;
+    if (rows > kMaxGroup) return PGD_ERR_SHAPE;
+    if (p.dtype != PGD_BF16 && (q_len > 1 || window > 0)) return PGD_ERR_UNSUPPORTED;
     if ((int64_t)max_blocks * p.block_size > INT32_MAX) return PGD_ERR_SHAPE;
     if (B == 0) return PGD_OK;
     if (!q || !out || !block_table || !seq_lens || !workspace) return PGD_ERR_ARG;
     if (max_blocks < 1) return PGD_ERR_SHAPE;
     const size_t elt = p.dtype == PGD_BF16 ? 2 : 4;
-    const size_t qbytes = (size_t)B * Hq * p.d * elt;
+    const size_t qbytes = (size_t)B * q_len * Hq * p.d * elt;
     {
         const uintptr_t q0 = reinterpret_cast<uintptr_t>(q), o0 = reinterpret_cast<uintptr_t>(out);
         if (q0 < o0 + qbytes && o0 < q0 + qbytes) return PGD_ERR_ARG;  // out aliases q
@@ -216,8 +228,8 @@ int paged_gqa_decode(pgd_pool_t pool, const void* q, int B, int Hq, const int32_
         !aligned(seq_lens, 4))
         return PGD_ERR_ALIGN;
     const int parts = resolve_parts(p, num_splits);
-    const int hg = choose_hg(p, G);
-    const WorkspaceLayout wl = workspace_layout(B, p.hkv, G, hg, p.d, parts);
+    const int hg = choose_hg(p, rows);
+    const WorkspaceLayout wl = workspace_layout(B, p.hkv, rows, hg, p.d, parts);
     if (!aligned(workspace, 256) || workspace_bytes < wl.total) return PGD_ERR_WORKSPACE;
 
     DeviceGuard g(p.device);
@@ -232,6 +244,8 @@ int paged_gqa_decode(pgd_pool_t pool, const void* q, int B, int Hq, const int32_
     a.block_table = block_table;
     a.seq_lens = seq_lens;
     a.B = B;
+    a.q_len = q_len;
+    a.window = window;
     a.hq = Hq;
     a.hkv = p.hkv;
     a.group = G;
@@ -261,6 +275,13 @@ int paged_gqa_decode(pgd_pool_t pool, const void* q, int B, int Hq, const int32_
         if (launch_merge(a, p.dtype, s) != cudaSuccess) return PGD_ERR_CUDA;
     }
     return PGD_OK;
+}
+
+int paged_gqa_decode(pgd_pool_t pool, const void* q, int B, int Hq, const int32_t* block_table,
+                     int max_blocks, const int32_t* seq_lens, float scale, void* out,
+                     void* workspace, size_t workspace_bytes, int num_splits, void* stream) {
+    return paged_gqa_decode_ex(pool, q, B, 1, Hq, block_table, max_blocks, seq_lens, 0, scale,
+                               out, workspace, workspace_bytes, num_splits, stream);
 }
 
 int paged_gqa_get_error(pgd_pool_t pool, void* stream) {

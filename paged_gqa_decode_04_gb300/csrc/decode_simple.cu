@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(kSimpleThreads) decode_simple_kernel(DecodeArg
     constexpr int DPL = D / 32;  // head-dim elements per lane
     __shared__ int64_t scratch[kSimpleThreads];
     __shared__ SpanStart ss;
-    find_span_start(a.seq_lens, a.B, a.units, a.tile_tokens, a.max_blocks, a.block_size,
+    find_span_start(a.seq_lens, a.B, a.units, a.tile_tokens, 1, 0, a.max_blocks, a.block_size,
                     a.num_parts, 1, scratch, &ss, a.tile_base);
     if (ss.r0 >= ss.r1) return;
 
@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(kSimpleThreads) decode_simple_kernel(DecodeArg
     T* __restrict__ out = static_cast<T*>(a.out);
     const int G = a.group;
 
-    TileCursor cur = cursor_at(ss, a.seq_lens, a.units, a.tile_tokens, a.max_blocks,
+    TileCursor cur = cursor_at(ss, a.seq_lens, a.units, a.tile_tokens, 1, 0, a.max_blocks,
                                a.block_size);
     int64_t x = ss.r0;
     while (x < ss.r1) {
@@ -122,7 +122,8 @@ __global__ void __launch_bounds__(kSimpleThreads) decode_simple_kernel(DecodeArg
         // advance past this piece
         x = piece_end;
         cur.i = i_end - 1;
-        cursor_next(cur, a.seq_lens, a.B, a.units, a.tile_tokens, a.max_blocks, a.block_size);
+        cursor_next(cur, a.seq_lens, a.B, a.units, a.tile_tokens, 1, 0, a.max_blocks,
+                    a.block_size);
     }
 }
 

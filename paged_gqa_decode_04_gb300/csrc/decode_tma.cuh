@@ -43,6 +43,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <limits.h>
 #include <math.h>
 
 #include "partition.cuh"
@@ -190,38 +191,46 @@ struct StageDesc {
     int64_t run_start;  // flat index of tile 0 of the (b, unit) run
     int b, unit, n_valid, flags;
     int n_b;            // tiles of the run
+    int tok0;           // sequence position of the tile's first token
+    int L;              // sequence length
     int pad;
 };
 
+// Offset (in elements) of query row r of KV head kvh of sequence b in q / out
+// [B, q_len, Hq, D]: row r is query token r / G, head kvh * G + r % G.
+__device__ __forceinline__ int64_t qrow_offset(const DecodeArgs& a, int b, int kvh, int r) {
+    const int G = a.group;
+    return (((int64_t)b * a.q_len + r / G) * a.hq + (int64_t)kvh * G + r % G) * a.d;
+}
+
 // Merge the pieces of a split run for the query rows one consumer warp owns
-// (m-tile `mt` of head `hgi` of the group) and write them to `ob` (the head's
-// G output rows).  Log-sum-exp combination in base 2: with lse_k = m_k +
+// (m-tile `mt` of head `hgi` of the group, KV head `kvh` of sequence `b`) and
+// write them to `out`.  Log-sum-exp combination in base 2: with lse_k = m_k +
 // log2 l_k and o_k the normalised partial of piece k,
 //     out = sum_k 2^(lse_k - M) o_k / sum_k 2^(lse_k - M),  M = max_k lse_k,
 // accumulated online.  Rows one after another; the lanes cover a row's
 // columns with float4 reads (two rows per pass when D = 64) and kPieceBatch
 // pieces are read before any is used, so a run of many pieces costs few L2
-// round trips.  Not inlined, so that its registers do not weigh on the tile
-// loop.
+// round trips.
 constexpr int kPieceBatch = 4;
 
 template <class C>
 __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int64_t t0, int64_t N, int64_t P,
                                           int64_t c0, int npieces, bool first_is_tail, int hgi,
-                                          int mt, __nv_bfloat16* ob) {
+                                          int mt, int b, int kvh) {
     constexpr int D = C::D;
     constexpr int CPR = D / 4;             // float4 chunks per row
     constexpr int RPP = 32 / CPR;          // rows per pass
     const int lane = threadIdx.x % 32;
-    const int G = a.group;
-    const int piece_rows = C::HG * G;
+    const int rows = a.q_len * a.group;    // query rows per KV head
+    const int piece_rows = C::HG * rows;
     const int r_lo = mt * 16;
-    const int r_hi = min(G, r_lo + C::ROWS);
+    const int r_hi = min(rows, r_lo + C::ROWS);
     const int col = (lane % CPR) * 4;
     for (int rb = r_lo; rb < r_hi; rb += RPP) {
         const int r = rb + lane / CPR;
         const bool rok = r < r_hi;
-        const int64_t pr = (int64_t)(hgi * G + r);
+        const int64_t pr = (int64_t)(hgi * rows + r);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         float M = -INFINITY, W = 0.f;
         for (int k0 = 0; k0 < npieces; k0 += kPieceBatch) {
@@ -254,11 +263,12 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int64_t t0, in
             }
         }
         if (rok) {
-            const float w = 1.f / W;
+            const float w = W > 0.f ? 1.f / W : 0.f;  // no token in any piece: zeros
             uint2 pk;
             pk.x = pack_bf16(acc.x * w, acc.y * w);
             pk.y = pack_bf16(acc.z * w, acc.w * w);
-            *reinterpret_cast<uint2*>(ob + (int64_t)r * D + col) = pk;
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) +
+                                      qrow_offset(a, b, kvh, r) + col) = pk;
         }
     }
 }
@@ -300,8 +310,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         aborted = 0;
         fence_barrier_init();
     }
-    find_span_start(a.seq_lens, a.B, a.units, T, a.max_blocks, bs, a.num_parts,
-                    a.auto_parts ? kMinTilesPerCta : 1, scratch, &ss,
+    find_span_start(a.seq_lens, a.B, a.units, T, a.q_len, a.window, a.max_blocks, bs,
+                    a.num_parts, a.auto_parts ? kMinTilesPerCta : 1, scratch, &ss,
                     a.tile_base);  // ends with __syncthreads
 
     // Sequences that own no tiles: length 0 gives zeros, an out-of-range length
@@ -311,8 +321,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (L != 0 && seq_len_ok(L, a.max_blocks, bs)) continue;
         if (L != 0 && threadIdx.x == 0) latch_error(a.err, PGD_ERR_SEQ_LEN);
         const __nv_bfloat16 fill = __float2bfloat16_rn(L == 0 ? 0.f : NAN);
-        __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) + (int64_t)b * a.hq * D;
-        for (int i = threadIdx.x; i < a.hq * D; i += blockDim.x) ob[i] = fill;
+        __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) + (int64_t)b * a.q_len * a.hq * D;
+        for (int i = threadIdx.x; i < a.q_len * a.hq * D; i += blockDim.x) ob[i] = fill;
     }
     if (ss.r0 >= ss.r1) return;
     const int64_t r0 = ss.r0, r1 = ss.r1;
@@ -320,7 +330,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
     if (warp == C::NC) {
         // ============================================================ producer
-        TileCursor cur = cursor_at(ss, a.seq_lens, a.units, T, a.max_blocks, bs);
+        TileCursor cur = cursor_at(ss, a.seq_lens, a.units, T, a.q_len, a.window, a.max_blocks,
+                                   bs);
         const uint64_t policy = policy_evict_first();
         const uint32_t box_bytes = (uint32_t)(C::HH * R * 128);
         // Block-id window: lane l holds block_table[win_b][win_lb + l]; the next
@@ -342,9 +353,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 L = a.seq_lens[cur.b];
                 L_b = cur.b;
             }
-            const int tok0 = cur.i * T;
+            const int tok0 = (cur.first + cur.i) * T;
             const int n_valid = min(T, L - tok0);
             const int npg = bs < T ? (n_valid + bs - 1) / bs : 1;
+            // pages wholly before the earliest token any query reads are not
+            // fetched (a windowed cache may have released them)
+            const int lo_min = a.window > 0 ? max(0, L - a.q_len - a.window + 1) : 0;
+            const int skip = (bs < T && lo_min > tok0) ? (lo_min - tok0) / bs : 0;
             const int lb0 = tok0 / bs;
             const int slot0 = bs < T ? 0 : tok0 % bs;
             if (cur.b != win_b || lb0 < win_lb || lb0 + npg > win_lb + 32) {
@@ -359,7 +374,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 nxt_id = table_row(win_b, win_lb + 32);
             }
             const int64_t phys = __shfl_sync(0xffffffffu, win_id, (lb0 - win_lb + lane) & 31);
-            const bool want = lane < npg;
+            const bool want = lane >= skip && lane < npg;
             const bool ok = want && phys >= 0 && phys < a.num_blocks;
             const bool bad = __any_sync(0xffffffffu, want && !ok);
             const int nok = __popc(__ballot_sync(0xffffffffu, ok));
@@ -376,7 +391,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (aborted) break;
             const uint32_t fb = smem_u32(&full_bar[s]);
             if (lane == 0) {
-                desc[s] = StageDesc{cur.run_start, cur.b, cur.unit, n_valid, flags, cur.n_b, 0};
+                desc[s] = StageDesc{cur.run_start, cur.b, cur.unit, n_valid, flags, cur.n_b,
+                                    tok0, L, 0};
                 mbar_arrive_expect_tx(fb, (uint32_t)nok * box_bytes * 2u);
                 if (bad) latch_error(a.err, PGD_ERR_BLOCK_ID);
             }
@@ -389,7 +405,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 tma_load_4d(dst, &tmap_k, fb, 0, slot0, hh0, (int)phys, policy);
                 tma_load_4d(dst + C::TENSOR_BYTES, &tmap_v, fb, 0, slot0, hh0, (int)phys, policy);
             }
-            cursor_next(cur, a.seq_lens, a.B, a.units, T, a.max_blocks, bs);
+            cursor_next(cur, a.seq_lens, a.B, a.units, T, a.q_len, a.window, a.max_blocks, bs);
         }
         // Do not leave while copies this CTA issued may still land.
         if (lane == 0) {
@@ -408,12 +424,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int gid = lane >> 2, tig = lane & 3;
     const int tw0 = tg * C::TW;
     const int G = a.group;
-    const int row0 = mt * 16 + gid;      // group row of accumulator rows c0,c1
-    const int row1 = row0 + 8;           // group row of c2,c3
-    const bool row0_ok = row0 < G;
-    const bool row1_ok = C::ROWS16 && row1 < G;
-    const int piece_rows = C::HG * G;    // rows of a partial result
+    const int rows = a.q_len * G;        // query rows per KV head: (token i, head g) = (r / G, r % G)
+    const int row0 = mt * 16 + gid;      // row of accumulator rows c0,c1
+    const int row1 = row0 + 8;           // row of c2,c3
+    const bool row0_ok = row0 < rows;
+    const bool row1_ok = C::ROWS16 && row1 < rows;
+    const int piece_rows = C::HG * rows; // rows of a partial result
     const int hh_mine = hgi * C::HALVES; // my head's first head-half in a page box
+    // Query token of each of my rows: attends to positions [lo, hi) with
+    // hi = L - q_len + i + 1 and lo = hi - window (clamped at 0) when windowed.
+    const int qi0 = row0 / G, qi1 = row1 / G;
 
     uint32_t qa[D / 16][4];
     float o[D / 8][4];
@@ -448,10 +468,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
         if (dsc.flags & kSegStart) {
             // New piece: load this warp's query rows as mma A fragments.
-            const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q) +
-                                      ((int64_t)dsc.b * a.hq + (int64_t)kvh * G) * D;
-            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(qg + (int64_t)row0 * D);
-            const uint32_t* q1 = reinterpret_cast<const uint32_t*>(qg + (int64_t)row1 * D);
+            const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q);
+            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(
+                qb + (row0_ok ? qrow_offset(a, dsc.b, kvh, row0) : 0));
+            const uint32_t* q1 = reinterpret_cast<const uint32_t*>(
+                qb + (row1_ok ? qrow_offset(a, dsc.b, kvh, row1) : 0));
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
                 const int c = ks * 8 + tig;  // 32-bit word index of columns 16ks + 2 tig
@@ -469,14 +490,21 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         seg_bad |= (dsc.flags & kTileBad) != 0;
 
         const int n_valid = dsc.n_valid;
-        const bool active = tw0 < n_valid;
-        const bool zeroed = active && n_valid < tw0 + C::TW;
+        // tile-local tokens before `v_lo` (pages not fetched: before every
+        // query's window) or from n_valid on (past the end) hold tail slots or
+        // stale data: zero their V rows so 0 * (NaN or Inf) never reaches O
+        const int lo_min = a.window > 0 ? max(0, dsc.L - a.q_len - a.window + 1) : 0;
+        const int v_lo = max(0, lo_min - dsc.tok0);
+        const bool active = tw0 < n_valid && tw0 + C::TW > v_lo;
+        const int z_hi = min(tw0 + C::TW, max(tw0, v_lo));  // zero [tw0, z_hi) ...
+        const int z_lo2 = max(tw0, n_valid);                // ... and [z_lo2, tw0 + TW)
+        const bool zeroed = active && (z_hi > tw0 || z_lo2 < tw0 + C::TW);
         if (zeroed) {
-            // Rows past the sequence end are tail slots or stale data: zero V
-            // there so that 0 * (NaN or Inf) never reaches the accumulators.
-            const int nz = tw0 + C::TW - n_valid;
+            const int n1 = z_hi - tw0;
+            const int nz = n1 + (tw0 + C::TW - z_lo2);
             for (int idx = lane; idx < nz * 8 * C::HALVES; idx += 32) {
-                const int t = n_valid + idx / (8 * C::HALVES);
+                const int j = idx / (8 * C::HALVES);
+                const int t = j < n1 ? tw0 + j : z_lo2 + (j - n1);
                 const int rem = idx % (8 * C::HALVES);
                 *reinterpret_cast<uint4*>(st + C::TENSOR_BYTES + row_off(t, rem / 8) +
                                           (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
@@ -502,16 +530,21 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     mma_bf16(sc[2 * np + 1], qa[ks], b2, b3);
                 }
             }
-            // ---- mask, scale to base-2 units, running max
+            // ---- mask (causal / window, per row), scale to base-2 units, running max
+            const int hi0 = dsc.L - a.q_len + qi0 + 1 - dsc.tok0;   // tile-local bounds
+            const int hi1 = dsc.L - a.q_len + qi1 + 1 - dsc.tok0;
+            const int lo0 = a.window > 0 ? hi0 - a.window : INT_MIN;
+            const int lo1 = a.window > 0 ? hi1 - a.window : INT_MIN;
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
             for (int j = 0; j < C::TW / 8; ++j) {
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int tok = tw0 + j * 8 + tig * 2 + e;
-                    const bool v = tok < n_valid;
-                    sc[j][e] = v ? sc[j][e] * a.scale_log2 : -INFINITY;
-                    sc[j][2 + e] = v ? sc[j][2 + e] * a.scale_log2 : -INFINITY;
+                    const bool v0 = tok < hi0 && tok >= lo0;
+                    const bool v1 = tok < hi1 && tok >= lo1;
+                    sc[j][e] = v0 ? sc[j][e] * a.scale_log2 : -INFINITY;
+                    sc[j][2 + e] = v1 ? sc[j][2 + e] * a.scale_log2 : -INFINITY;
                     mx0 = fmaxf(mx0, sc[j][e]);
                     mx1 = fmaxf(mx1, sc[j][2 + e]);
                 }
@@ -668,24 +701,28 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (tg != 0) continue;
 
         // ---- write: whole run -> out (bf16); split run -> partial (fp32) + lse
-        const float inv0 = seg_bad ? NAN : 1.f / lt0;
-        const float inv1 = seg_bad ? NAN : 1.f / lt1;
-        __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) +
-                            ((int64_t)dsc.b * a.hq + (int64_t)kvh * G) * D;
+        // a row that saw no token (window / causal range outside this piece, or
+        // a query before the sequence start) has l = 0: zeros, lse = -inf
+        const float inv0 = seg_bad ? NAN : (lt0 > 0.f ? 1.f / lt0 : 0.f);
+        const float inv1 = seg_bad ? NAN : (lt1 > 0.f ? 1.f / lt1 : 0.f);
         if (!(dsc.flags & kSegPartial)) {
+            __nv_bfloat16* o0 = static_cast<__nv_bfloat16*>(a.out) +
+                                (row0_ok ? qrow_offset(a, dsc.b, kvh, row0) : 0);
+            __nv_bfloat16* o1 = static_cast<__nv_bfloat16*>(a.out) +
+                                (row1_ok ? qrow_offset(a, dsc.b, kvh, row1) : 0);
 #pragma unroll
             for (int n = 0; n < D / 8; ++n) {
                 if (row0_ok)
-                    *reinterpret_cast<uint32_t*>(ob + (int64_t)row0 * D + n * 8 + tig * 2) =
+                    *reinterpret_cast<uint32_t*>(o0 + n * 8 + tig * 2) =
                         pack_bf16(o[n][0] * inv0, o[n][1] * inv0);
                 if (row1_ok)
-                    *reinterpret_cast<uint32_t*>(ob + (int64_t)row1 * D + n * 8 + tig * 2) =
+                    *reinterpret_cast<uint32_t*>(o1 + n * 8 + tig * 2) =
                         pack_bf16(o[n][2] * inv1, o[n][3] * inv1);
             }
             continue;
         }
         const int64_t slot = (int64_t)blockIdx.x * 2 + ((dsc.flags & kSegSlot1) ? 1 : 0);
-        const int prow0 = hgi * G + row0, prow1 = hgi * G + row1;  // rows of the piece
+        const int prow0 = hgi * rows + row0, prow1 = hgi * rows + row1;  // rows of the piece
         {
             float* po = a.part_o + slot * piece_rows * D;
 #pragma unroll
@@ -699,8 +736,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
             if (tig == 0) {
                 float* pl = a.part_lse + slot * piece_rows;
-                if (row0_ok) pl[prow0] = seg_bad ? 0.f : m0 + fast_log2(lt0);
-                if (row1_ok) pl[prow1] = seg_bad ? 0.f : m1 + fast_log2(lt1);
+                if (row0_ok)
+                    pl[prow0] = seg_bad ? 0.f : (lt0 > 0.f ? m0 + fast_log2(lt0) : -INFINITY);
+                if (row1_ok)
+                    pl[prow1] = seg_bad ? 0.f : (lt1 > 0.f ? m1 + fast_log2(lt1) : -INFINITY);
             }
         }
         // Publish the partial, count it; the warp that brings the run's count
@@ -725,7 +764,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         last = __shfl_sync(0xffffffffu, last, 0);
         if (!last) continue;
         __threadfence();
-        merge_pieces<C>(a, t0, N, P, c0, npieces, first_is_tail, hgi, mt, ob);
+        merge_pieces<C>(a, t0, N, P, c0, npieces, first_is_tail, hgi, mt, dsc.b, kvh);
     }
 }
 
@@ -775,11 +814,11 @@ cudaError_t launch_mt(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
 
 template <int D>
 cudaError_t launch_tma_d(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
-    const int G = a.group;
-    if (G <= 8) return launch_mt<D, 1, false>(a, p, s);
-    if (G <= 16) return launch_mt<D, 1, true>(a, p, s);
-    if (G <= 32) return launch_mt<D, 2, true>(a, p, s);
-    if (G <= 48) return launch_mt<D, 3, true>(a, p, s);
+    const int rows = a.q_len * a.group;  // query rows per KV head
+    if (rows <= 8) return launch_mt<D, 1, false>(a, p, s);
+    if (rows <= 16) return launch_mt<D, 1, true>(a, p, s);
+    if (rows <= 32) return launch_mt<D, 2, true>(a, p, s);
+    if (rows <= 48) return launch_mt<D, 3, true>(a, p, s);
     return launch_mt<D, 4, true>(a, p, s);
 }
 

@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeArgs a) {
 
     const int64_t N = a.tile_base[a.B];
     const int64_t P = a.num_parts;
-    const int n_b = tiles_of(L, a.max_blocks, a.block_size, a.tile_tokens);
+    const int n_b = tiles_of(L, a.max_blocks, a.block_size, a.tile_tokens, 1, 0);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int nwarps = blockDim.x / 32;
 

@@ -78,9 +78,9 @@ extern "C" int paged_gqa_decode_noalloc(pgd_pool_t pool, const void* q, int B, i
     int parts = 0;
     if (paged_gqa_auto_splits(pool, &parts) != PGD_OK) return PGD_ERR_ARG;
     if (num_splits > 0) parts = num_splits;
-    const int G = Hq / p.hkv;
+    const int rows = Hq / p.hkv;  // one query token per sequence
     const pgd::WorkspaceLayout wl =
-        pgd::workspace_layout(B, p.hkv, G, pgd::choose_hg(p, G), p.d, parts);
+        pgd::workspace_layout(B, p.hkv, rows, pgd::choose_hg(p, rows), p.d, parts);
     int prev = -1;
     if (cudaGetDevice(&prev) != cudaSuccess) return PGD_ERR_CUDA;
     if (prev != dev && cudaSetDevice(dev) != cudaSuccess) return PGD_ERR_CUDA;

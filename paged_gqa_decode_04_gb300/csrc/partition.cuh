@@ -30,8 +30,21 @@ __device__ __forceinline__ bool seq_len_ok(int L, int max_blocks, int block_size
     return L >= 0 && (int64_t)L <= (int64_t)max_blocks * block_size;
 }
 
-__device__ __forceinline__ int tiles_of(int L, int max_blocks, int block_size, int T) {
-    return seq_len_ok(L, max_blocks, block_size) ? (L + T - 1) / T : 0;
+// First tile a sequence of length L needs: with q_len query tokens (the last
+// q_len cached ones) and a window of the W most recent tokens per query, the
+// earliest token read is max(0, L - q_len - W + 1); without a window, 0.
+__device__ __forceinline__ int first_tile_of(int L, int T, int q_len, int window) {
+    if (window <= 0) return 0;
+    const int lo = L - q_len - window + 1;
+    return lo > 0 ? lo / T : 0;
+}
+
+// Tiles of T tokens a sequence of length L walks (0 for L == 0 or a length out
+// of range).
+__device__ __forceinline__ int tiles_of(int L, int max_blocks, int block_size, int T, int q_len,
+                                        int window) {
+    if (!seq_len_ok(L, max_blocks, block_size) || L == 0) return 0;
+    return (L + T - 1) / T - first_tile_of(L, T, q_len, window);
 }
 
 __device__ __forceinline__ int64_t span_begin(int64_t c, int64_t N, int64_t P) {
@@ -63,8 +76,9 @@ struct SpanStart {
 // an empty span; with min_tiles == 1 all `parts` spans are used.  CTA 0 also writes tile_base[0..B] to global memory for the merge
 // kernel.
 __device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int B, int units,
-                                       int T, int max_blocks, int block_size, int64_t parts,
-                                       int min_tiles, int64_t* scratch, SpanStart* out,
+                                       int T, int q_len, int window, int max_blocks,
+                                       int block_size, int64_t parts, int min_tiles,
+                                       int64_t* scratch, SpanStart* out,
                                        int64_t* __restrict__ tile_base_out) {
     const int nt = blockDim.x;
     const int tid = threadIdx.x;
@@ -73,7 +87,7 @@ __device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int
     const int b_hi = min(B, b_lo + per);
     int64_t local = 0;
     for (int b = b_lo; b < b_hi; ++b)
-        local += (int64_t)units * tiles_of(seq_lens[b], max_blocks, block_size, T);
+        local += (int64_t)units * tiles_of(seq_lens[b], max_blocks, block_size, T, q_len, window);
     scratch[tid] = local;
     __syncthreads();
     if (tid == 0) {  // exclusive scan of per-thread sums (nt is small)
@@ -100,7 +114,8 @@ __device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int
     const int64_t r0 = out->r0;
     int64_t run = scratch[tid];
     for (int b = b_lo; b < b_hi; ++b) {
-        int64_t n = (int64_t)units * tiles_of(seq_lens[b], max_blocks, block_size, T);
+        int64_t n =
+            (int64_t)units * tiles_of(seq_lens[b], max_blocks, block_size, T, q_len, window);
         if (blockIdx.x == 0) tile_base_out[b] = run;
         if (r0 >= run && r0 < run + n) {
             out->b = b;
@@ -112,17 +127,22 @@ __device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int
     __syncthreads();
 }
 
-// Cursor over the (b, unit, tile) sequence of one span.
+// Cursor over the (b, unit, tile) sequence of one span.  Tile i of a run
+// covers tokens [(first + i) T, (first + i + 1) T) of its sequence.
 struct TileCursor {
     int b, unit, i, n_b;     // current position: tile i of n_b of (b, unit)
+    int first;               // first tile of sequence b (windowed calls skip the start)
     int64_t run_start;       // flat index of tile 0 of (b, unit)
 };
 
 __device__ inline TileCursor cursor_at(const SpanStart& s, const int32_t* seq_lens, int units,
-                                       int T, int max_blocks, int block_size) {
+                                       int T, int q_len, int window, int max_blocks,
+                                       int block_size) {
     TileCursor c;
     c.b = s.b;
-    c.n_b = tiles_of(seq_lens[s.b], max_blocks, block_size, T);
+    const int L = seq_lens[s.b];
+    c.n_b = tiles_of(L, max_blocks, block_size, T, q_len, window);
+    c.first = first_tile_of(L, T, q_len, window);
     int64_t off = s.r0 - s.b_base;
     c.unit = (int)(off / c.n_b);
     c.i = (int)(off % c.n_b);
@@ -132,7 +152,7 @@ __device__ inline TileCursor cursor_at(const SpanStart& s, const int32_t* seq_le
 }
 
 __device__ inline void cursor_next(TileCursor& c, const int32_t* seq_lens, int B, int units,
-                                   int T, int max_blocks, int block_size) {
+                                   int T, int q_len, int window, int max_blocks, int block_size) {
     if (++c.i < c.n_b) return;
     c.run_start += c.n_b;
     c.i = 0;
@@ -140,10 +160,11 @@ __device__ inline void cursor_next(TileCursor& c, const int32_t* seq_lens, int B
     c.unit = 0;
     int nb = 0;
     while (++c.b < B) {
-        nb = tiles_of(seq_lens[c.b], max_blocks, block_size, T);
+        nb = tiles_of(seq_lens[c.b], max_blocks, block_size, T, q_len, window);
         if (nb > 0) break;
     }
     c.n_b = nb;
+    if (c.b < B) c.first = first_tile_of(seq_lens[c.b], T, q_len, window);
 }
 
 // Segment flags for the piece of (b, unit) a CTA holds.

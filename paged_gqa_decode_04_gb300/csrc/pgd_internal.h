@@ -43,6 +43,8 @@ struct DecodeArgs {
     const int32_t* block_table;
     const int32_t* seq_lens;
     int B;
+    int q_len;             // query tokens per sequence (the last q_len cached tokens)
+    int window;            // attend to the `window` most recent tokens per query; <= 0: all
     int hq;
     int hkv;
     int group;             // G = Hq / Hkv
@@ -68,10 +70,11 @@ struct DecodeArgs {
 struct WorkspaceLayout {
     size_t counters_off, tile_base_off, part_lse_off, part_o_off, total;
 };
-WorkspaceLayout workspace_layout(int B, int hkv, int group, int hg, int d, int parts);
+// `rows` = query rows per KV head: q_len * G.
+WorkspaceLayout workspace_layout(int B, int hkv, int rows, int hg, int d, int parts);
 
-// KV heads per unit of work for this pool and group size.
-int choose_hg(const Pool& p, int group);
+// KV heads per unit of work for this pool and rows per KV head.
+int choose_hg(const Pool& p, int rows);
 
 // The description behind a pool handle.
 const Pool& pool_desc(pgd_pool_t h);
