@@ -62,6 +62,11 @@ class Oracle:
                                              [ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                               ctypes.c_double, ctypes.c_void_p])
         lib.oracle_decode_ex_f64.restype = ctypes.c_int
+        lib.oracle_decode_kv8_f64.argtypes = ([ctypes.c_void_p, ctypes.c_int] +
+                                              [ctypes.c_void_p] * 6 + [ctypes.c_int] * 6 +
+                                              [ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_double, ctypes.c_void_p])
+        lib.oracle_decode_kv8_f64.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         self.lib = lib
@@ -120,6 +125,43 @@ class Oracle:
         return out, int(rc)
 
 
+    def decode_kv8_f64(self, q, k8, v8, k_scale, v_scale, block_table, seq_lens, scale,
+                       window=0):
+        """8-bit (e4m3) K/V pages with one scale per KV head.  q is
+        [B, q_len, Hq, D] (or [B, Hq, D]) float32 or bfloat16 bits; k8 / v8 are
+        uint8 [num_blocks, bs, Hkv, D]; k_scale / v_scale float32 [Hkv].
+        Returns (out with q's shape, float64; status)."""
+        q = np.ascontiguousarray(q)
+        squeeze = q.ndim == 3
+        if squeeze:
+            q = q[:, None]
+        if q.dtype == np.float32:
+            q_dtype = F32
+        elif q.dtype == np.uint16:
+            q_dtype = BF16
+        else:
+            raise TypeError("q must be float32 or bfloat16 bits")
+        k8 = np.ascontiguousarray(k8, dtype=np.uint8)
+        v8 = np.ascontiguousarray(v8, dtype=np.uint8)
+        ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+        vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        B, q_len, Hq, D = q.shape
+        nb, bs, Hkv, D2 = k8.shape
+        if D2 != D or v8.shape != k8.shape or ks.shape != (Hkv,) or vs.shape != (Hkv,):
+            raise ValueError("shape mismatch")
+        out = np.empty((B, q_len, Hq, D), dtype=np.float64)
+        rc = self.lib.oracle_decode_kv8_f64(q.ctypes.data, q_dtype, k8.ctypes.data,
+                                            v8.ctypes.data, ks.ctypes.data, vs.ctypes.data,
+                                            bt.ctypes.data, sl.ctypes.data, B, q_len, Hq, Hkv,
+                                            D, bs, nb, bt.shape[1], int(window), float(scale),
+                                            out.ctypes.data)
+        if rc == 1:
+            raise ValueError("oracle rejected the arguments")
+        return (out[:, 0] if squeeze else out), int(rc)
+
+
 _default = None
 
 
@@ -141,6 +183,11 @@ def decode_f64(q, k_pool, v_pool, block_table, seq_lens, scale):
 
 def decode_ex_f64(q, k_pool, v_pool, block_table, seq_lens, scale, window=0):
     return default().decode_ex_f64(q, k_pool, v_pool, block_table, seq_lens, scale, window)
+
+
+def decode_kv8_f64(q, k8, v8, k_scale, v_scale, block_table, seq_lens, scale, window=0):
+    return default().decode_kv8_f64(q, k8, v8, k_scale, v_scale, block_table, seq_lens, scale,
+                                    window)
 
 
 def decode_rows_f64(q, k_pool, v_pool, block_table, seq_lens, scale, rows):

@@ -83,3 +83,23 @@ def brute_decode_ex(q, k_pool, v_pool, block_table, seq_lens, scale, window=0):
             P = P / P.sum(axis=1, keepdims=True)
             out[b, i] = np.einsum("hl,lhd->hd", P, V)
     return out
+
+
+def e4m3_to_f64(bits):
+    """uint8 e4m3 bit patterns -> float64, through torch's float8_e4m3fn type
+    (an implementation independent of the C oracle's decoder)."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+def brute_decode_kv8(q, k8, v8, k_scale, v_scale, block_table, seq_lens, scale, window=0):
+    """Dequantise the 8-bit pages (value = per-head scale x e4m3) and run the
+    dense masked formulation."""
+    k = e4m3_to_f64(k8) * np.asarray(k_scale, dtype=np.float64)[None, None, :, None]
+    v = e4m3_to_f64(v8) * np.asarray(v_scale, dtype=np.float64)[None, None, :, None]
+    q = np.asarray(q)
+    if q.ndim == 3:
+        return brute_decode_ex(q[:, None], k, v, block_table, seq_lens, scale, window)[:, 0]
+    return brute_decode_ex(q, k, v, block_table, seq_lens, scale, window)

@@ -64,14 +64,35 @@
 #include <omp.h>
 #endif
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_FP8_E4M3 = 2 };
 enum { ORACLE_OK = 0, ORACLE_ERR_ARG = 1, ORACLE_ERR_BLOCK_ID = 2, ORACLE_ERR_SEQ_LEN = 3 };
 
-/* Exact widening of element `idx` of a float32 or bfloat16 array. */
+/*
+ * An 8-bit float with 1 sign bit, 4 exponent bits (bias 7) and 3 mantissa
+ * bits, no infinities, all-ones exponent and mantissa = NaN: normal values
+ * (-1)^s 2^(e-7) (1 + m/8), subnormal (e = 0) values (-1)^s 2^-6 (m/8).
+ */
+static double e4m3_value(uint8_t v)
+{
+    const int sign = v >> 7, e = (v >> 3) & 15, m = v & 7;
+    double x;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) {
+        x = ldexp((double)m / 8.0, -6);
+    } else {
+        x = ldexp(1.0 + (double)m / 8.0, e - 7);
+    }
+    return sign ? -x : x;
+}
+
+/* Exact widening of element `idx` of a float32, bfloat16 or e4m3 array. */
 static double load_elem(const void *base, int64_t idx, int dtype)
 {
     if (dtype == ORACLE_F32) {
         return (double)((const float *)base)[idx];
+    }
+    if (dtype == ORACLE_FP8_E4M3) {
+        return e4m3_value(((const uint8_t *)base)[idx]);
     }
     uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
     float f;
@@ -88,13 +109,18 @@ static double load_elem(const void *base, int64_t idx, int dtype)
  * gives zeros.  Returns a status.
  */
 static int decode_row(const void *q, const void *k_pool, const void *v_pool,
+                      const float *k_scale, const float *v_scale,
                       const int32_t *block_table, const int32_t *seq_lens, int dtype,
+                      int kv_dtype,
                       int q_len, int Hq, int Hkv, int D, int block_size, int64_t num_blocks,
                       int max_blocks, int window, double scale, int b, int i, int h, double *out)
 {
     const int G = Hq / Hkv;
     const int kv = h / G;
     const int64_t L = seq_lens[b];
+    /* a stored K/V element stands for scale[kv] times its value (1 without scales) */
+    const double ks = k_scale ? (double)k_scale[kv] : 1.0;
+    const double vs = v_scale ? (double)v_scale[kv] : 1.0;
     int d;
 
     if (L < 0 || L > (int64_t)max_blocks * block_size) {
@@ -136,7 +162,8 @@ static int decode_row(const void *q, const void *k_pool, const void *v_pool,
     for (int64_t t = 0; t < n; ++t) {
         double dot = 0.0;
         for (d = 0; d < D; ++d) {
-            dot += load_elem(q, q_base + d, dtype) * load_elem(k_pool, row_base[t] + d, dtype);
+            dot += load_elem(q, q_base + d, dtype) *
+                   (ks * load_elem(k_pool, row_base[t] + d, kv_dtype));
         }
         s[t] = scale * dot;
     }
@@ -153,7 +180,7 @@ static int decode_row(const void *q, const void *k_pool, const void *v_pool,
     }
     for (int64_t t = 0; t < n; ++t) {
         for (d = 0; d < D; ++d) {
-            out[d] += s[t] * load_elem(v_pool, row_base[t] + d, dtype);
+            out[d] += s[t] * (vs * load_elem(v_pool, row_base[t] + d, kv_dtype));
         }
     }
     for (d = 0; d < D; ++d) out[d] /= z;
@@ -166,7 +193,7 @@ static int decode_row(const void *q, const void *k_pool, const void *v_pool,
 static int check_args(int dtype, int B, int Hq, int Hkv, int D, int block_size,
                       int64_t num_blocks, int max_blocks)
 {
-    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return ORACLE_ERR_ARG;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_FP8_E4M3) return ORACLE_ERR_ARG;
     if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || block_size <= 0) return ORACLE_ERR_ARG;
     if (num_blocks < 0 || max_blocks < 0) return ORACLE_ERR_ARG;
     if (Hq % Hkv != 0) return ORACLE_ERR_ARG;
@@ -192,7 +219,8 @@ int oracle_decode_rows_f64(const void *q, const void *k_pool, const void *v_pool
     int status = ORACLE_OK;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t i = 0; i < n_rows; ++i) {
-        int r = decode_row(q, k_pool, v_pool, block_table, seq_lens, dtype, 1, Hq, Hkv, D,
+        int r = decode_row(q, k_pool, v_pool, NULL, NULL, block_table, seq_lens, dtype, dtype,
+                           1, Hq, Hkv, D,
                            block_size, num_blocks, max_blocks, 0, scale, rows[2 * i], 0,
                            rows[2 * i + 1], out + i * (int64_t)D);
         if (r) {
@@ -217,7 +245,8 @@ int oracle_decode_f64(const void *q, const void *k_pool, const void *v_pool,
     const int64_t n_rows = (int64_t)B * Hq;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t i = 0; i < n_rows; ++i) {
-        int r = decode_row(q, k_pool, v_pool, block_table, seq_lens, dtype, 1, Hq, Hkv, D,
+        int r = decode_row(q, k_pool, v_pool, NULL, NULL, block_table, seq_lens, dtype, dtype,
+                           1, Hq, Hkv, D,
                            block_size, num_blocks, max_blocks, 0, scale, (int)(i / Hq), 0,
                            (int)(i % Hq), out + i * (int64_t)D);
         if (r) {
@@ -236,10 +265,11 @@ int oracle_decode_f64(const void *q, const void *k_pool, const void *v_pool,
  * q_len query tokens included (they are the last q_len); window <= 0 means
  * no window.  With q_len = 1 and window = 0 this is oracle_decode_f64.
  */
-int oracle_decode_ex_f64(const void *q, const void *k_pool, const void *v_pool,
-                         const int32_t *block_table, const int32_t *seq_lens, int dtype, int B,
-                         int q_len, int Hq, int Hkv, int D, int block_size, int64_t num_blocks,
-                         int max_blocks, int window, double scale, double *out)
+static int decode_ex(const void *q, const void *k_pool, const void *v_pool, const float *k_scale,
+                     const float *v_scale, const int32_t *block_table, const int32_t *seq_lens,
+                     int dtype, int kv_dtype, int B, int q_len, int Hq, int Hkv, int D,
+                     int block_size, int64_t num_blocks, int max_blocks, int window,
+                     double scale, double *out)
 {
     int rc = check_args(dtype, B, Hq, Hkv, D, block_size, num_blocks, max_blocks);
     if (rc) return rc;
@@ -251,7 +281,8 @@ int oracle_decode_ex_f64(const void *q, const void *k_pool, const void *v_pool,
         const int h = (int)(r % Hq);
         const int i = (int)((r / Hq) % q_len);
         const int b = (int)(r / ((int64_t)Hq * q_len));
-        int st = decode_row(q, k_pool, v_pool, block_table, seq_lens, dtype, q_len, Hq, Hkv, D,
+        int st = decode_row(q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, dtype,
+                            kv_dtype, q_len, Hq, Hkv, D,
                             block_size, num_blocks, max_blocks, window, scale, b, i, h,
                             out + r * (int64_t)D);
         if (st) {
@@ -262,6 +293,33 @@ int oracle_decode_ex_f64(const void *q, const void *k_pool, const void *v_pool,
         }
     }
     return status;
+}
+
+int oracle_decode_ex_f64(const void *q, const void *k_pool, const void *v_pool,
+                         const int32_t *block_table, const int32_t *seq_lens, int dtype, int B,
+                         int q_len, int Hq, int Hkv, int D, int block_size, int64_t num_blocks,
+                         int max_blocks, int window, double scale, double *out)
+{
+    return decode_ex(q, k_pool, v_pool, NULL, NULL, block_table, seq_lens, dtype, dtype, B, q_len,
+                     Hq, Hkv, D, block_size, num_blocks, max_blocks, window, scale, out);
+}
+
+/*
+ * 8-bit K/V pages: k_pool / v_pool hold e4m3 bytes; element (block, slot,
+ * head kv, d) stands for k_scale[kv] * e4m3(byte) (v_scale for V), one scale
+ * per KV head.  q and out as in oracle_decode_ex_f64, q in `q_dtype`
+ * (float32 or bfloat16).
+ */
+int oracle_decode_kv8_f64(const void *q, int q_dtype, const void *k_pool, const void *v_pool,
+                          const float *k_scale, const float *v_scale,
+                          const int32_t *block_table, const int32_t *seq_lens, int B, int q_len,
+                          int Hq, int Hkv, int D, int block_size, int64_t num_blocks,
+                          int max_blocks, int window, double scale, double *out)
+{
+    if (q_dtype == ORACLE_FP8_E4M3 || !k_scale || !v_scale) return ORACLE_ERR_ARG;
+    return decode_ex(q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, q_dtype,
+                     ORACLE_FP8_E4M3, B, q_len, Hq, Hkv, D, block_size, num_blocks, max_blocks,
+                     window, scale, out);
 }
 
 /* Threads OpenMP will use (1 without OpenMP). */

@@ -418,6 +418,84 @@ def pin_ex_empty_rows_are_zero(orc):
     assert np.abs(out - ref).max() <= 1e-12
 
 
+# ----------------------------------------------------------------- 8-bit K/V pins
+# K/V stored as 8-bit floats (1 sign, 4 exponent bits with bias 7, 3 mantissa
+# bits) with one scale per KV head: quantized KV pages ("Modern LLM Inference
+# ...", section 6, quantization; "The Ultimate Guide ... Part 2", "KV Cache
+# Compression").
+E4M3_CASES = [(0x38, 1.0), (0x40, 2.0), (0x30, 0.5), (0x39, 1.125), (0x7E, 448.0),
+              (0xFE, -448.0), (0x08, 2.0 ** -6), (0x01, 2.0 ** -9), (0x07, 7 * 2.0 ** -9),
+              (0xB8, -1.0), (0x00, 0.0), (0x5A, 20.0), (0x5C, 24.0)]
+
+
+def _kv8_case(rng, B, Hq, Hkv, D, bs, lens):
+    q, k, v, t, L = paged_case(rng, B, Hq, Hkv, D, bs, lens, "f32")
+    k8 = rng.integers(0, 256, size=k.shape).astype(np.uint8)
+    v8 = rng.integers(0, 256, size=v.shape).astype(np.uint8)
+    k8[(k8 & 0x7F) == 0x7F] = 0x38          # no NaN codes
+    v8[(v8 & 0x7F) == 0x7F] = 0x30
+    ks = rng.uniform(0.01, 0.1, size=Hkv).astype(np.float32)   # keep logits moderate
+    vs = rng.uniform(0.5, 2.0, size=Hkv).astype(np.float32)
+    return q, k8, v8, ks, vs, t, L
+
+
+def pin_kv8_e4m3_values(orc):
+    """One cached token: the output is v_scale times the e4m3 value, for codes
+    with known values (normal, subnormal, largest, signed zero)."""
+    D = len(E4M3_CASES)
+    q = np.zeros((1, 1, D), dtype=np.float32)
+    k8 = np.zeros((1, 1, 1, D), dtype=np.uint8)
+    v8 = np.array([c for c, _ in E4M3_CASES], dtype=np.uint8).reshape(1, 1, 1, D)
+    for vs in (1.0, 0.75):
+        out, rc = orc.decode_kv8_f64(q, k8, v8, np.ones(1, np.float32),
+                                     np.full(1, vs, np.float32), np.zeros((1, 1), np.int32),
+                                     np.ones(1, np.int32), 1.0)
+        assert rc == 0
+        assert np.array_equal(out[0, 0], vs * np.array([x for _, x in E4M3_CASES]))
+
+
+def pin_kv8_brute_force(orc):
+    """Against the dense formulation fed by torch's own e4m3 decoding."""
+    from oracle.brute import brute_decode_kv8
+    rng = np.random.default_rng(71)
+    for lens, q_len, window in (([9, 17, 3], 1, 0), ([12, 5, 30], 3, 0), ([20, 8, 14], 2, 6)):
+        q, k8, v8, ks, vs, t, L = _kv8_case(rng, 3, 4 * q_len, 2, 8, 4, lens)
+        q = q.reshape(3, q_len, 4, 8)
+        out, rc = orc.decode_kv8_f64(q, k8, v8, ks, vs, t, L, 0.3, window)
+        ref = brute_decode_kv8(q, k8, v8, ks, vs, t, L, 0.3, window)
+        assert rc == 0 and np.abs(out - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+def pin_kv8_equals_wide_pages(orc):
+    """With unit scales, 8-bit pages give exactly the result of bfloat16 pages
+    holding the same values (every finite e4m3 value is a bfloat16 value)."""
+    from oracle.brute import e4m3_to_f64
+    rng = np.random.default_rng(73)
+    q, k8, v8, _, _, t, L = _kv8_case(rng, 2, 4, 2, 8, 4, [11, 6])
+    qb = bf16_bits(q)
+    one = np.ones(2, np.float32)
+    a, _ = orc.decode_kv8_f64(qb, k8, v8, one, one, t, L, 0.05)
+    kb = bf16_bits(e4m3_to_f64(k8).astype(np.float32))
+    vb = bf16_bits(e4m3_to_f64(v8).astype(np.float32))
+    b, _ = orc.decode_f64(qb, kb, vb, t, L, 0.05)
+    assert np.array_equal(a, b)
+
+
+def pin_kv8_scales(orc):
+    """A V scale s multiplies the output by s; a K scale s acts like a logit
+    scale times s."""
+    rng = np.random.default_rng(79)
+    q, k8, v8, ks, vs, t, L = _kv8_case(rng, 2, 4, 2, 8, 4, [9, 13])
+    one = np.ones(2, np.float32)
+    base, _ = orc.decode_kv8_f64(q, k8, v8, one, one, t, L, 0.02)
+    v2, _ = orc.decode_kv8_f64(q, k8, v8, one, np.array([3.0, 0.5], np.float32), t, L, 0.02)
+    assert np.abs(v2[:, :2] - 3.0 * base[:, :2]).max() <= 1e-12 * np.abs(base).max()
+    assert np.abs(v2[:, 2:] - 0.5 * base[:, 2:]).max() <= 1e-12 * np.abs(base).max()
+    k2, _ = orc.decode_kv8_f64(q, k8, v8, np.full(2, 2.0, np.float32), one, t, L, 0.02)
+    s2, _ = orc.decode_kv8_f64(q, k8, v8, one, one, t, L, 0.04)
+    assert np.abs(k2 - s2).max() <= 1e-12 * np.abs(s2).max()
+
+
 PINS = [
     pin_brute_force,
     pin_paged_equals_contiguous,
@@ -438,4 +516,8 @@ PINS = [
     pin_ex_window_is_recent_tokens,
     pin_ex_blocks_before_window_unread,
     pin_ex_empty_rows_are_zero,
+    pin_kv8_e4m3_values,
+    pin_kv8_brute_force,
+    pin_kv8_equals_wide_pages,
+    pin_kv8_scales,
 ]
