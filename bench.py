@@ -182,12 +182,17 @@ def cpu_oracle_rate(w, budget_s, rows_cap=None):
     import oracle
 
     q, k, v = gen.to_numpy_bits(w.q), gen.to_numpy_bits(w.k_pool), gen.to_numpy_bits(w.v_pool)
-    elt = accounting.ELT[w.dtype]
-    nbytes = accounting.algorithmic_bytes(w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt)
+    elt, q_elt = accounting.ELT[w.dtype], accounting.Q_ELT[w.dtype]
+    nbytes = accounting.algorithmic_bytes(w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt, q_elt)
+    if w.dtype == "fp8":
+        ks, vs = w.k_scale.cpu().numpy(), w.v_scale.cpu().numpy()
+        run = lambda: oracle.decode_kv8_f64(q, k, v, ks, vs, w.table_np, w.lens_np, w.scale)
+    else:
+        run = lambda: oracle.decode_f64(q, k, v, w.table_np, w.lens_np, w.scale)
     reps = 0
     t0 = time.perf_counter()
     while True:
-        oracle.decode_f64(q, k, v, w.table_np, w.lens_np, w.scale)
+        run()
         reps += 1
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -201,25 +206,37 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     w = gen.make(args.config, device="cpu")
-    elt = accounting.ELT[w.dtype]
-    nbytes = accounting.algorithmic_bytes(w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt)
+    elt, q_elt = accounting.ELT[w.dtype], accounting.Q_ELT[w.dtype]
+    nbytes = accounting.algorithmic_bytes(w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt, q_elt)
     import oracle
 
     q, k, v = gen.to_numpy_bits(w.q), gen.to_numpy_bits(w.k_pool), gen.to_numpy_bits(w.v_pool)
     # One step = the oracle over a bounded sample: every sequence, a subset of
     # query heads (whole KV groups) so that K+W steps fit in a few minutes.
-    heads = max(w.G, min(w.Hq, (w.Hq // 8) // w.G * w.G or w.G))
-    rows = np.array([[b, h] for b in range(w.B) for h in range(heads)], dtype=np.int32)
-    frac = heads / w.Hq
+    if w.dtype == "fp8":
+        # 8-bit pages: every query head of the first B/8 sequences per step
+        nb = max(1, w.B // 8)
+        ks, vs = w.k_scale.numpy(), w.v_scale.numpy()
+        step = lambda: oracle.decode_kv8_f64(q[:nb], k, v, ks, vs, w.table_np[:nb],
+                                             w.lens_np[:nb], w.scale)
+        frac = accounting.algorithmic_bytes(w.lens_np[:nb], w.Hq, w.Hkv, w.D, w.block_size, elt,
+                                            q_elt) / nbytes
+        sample = ("each step: sequences 0..%d of %d, every query head, float64, host cores"
+                  % (nb - 1, w.B))
+    else:
+        heads = max(w.G, min(w.Hq, (w.Hq // 8) // w.G * w.G or w.G))
+        rows = np.array([[b, h] for b in range(w.B) for h in range(heads)], dtype=np.int32)
+        frac = heads / w.Hq
+        step = lambda: oracle.decode_rows_f64(q, k, v, w.table_np, w.lens_np, w.scale, rows)
+        sample = ("each step: every sequence, query heads 0..%d of %d (%.1f%% of the rows), "
+                  "float64, host cores" % (heads - 1, w.Hq, 100 * frac))
     for _ in range(args.warmup):
-        oracle.decode_rows_f64(q, k, v, w.table_np, w.lens_np, w.scale, rows)
+        step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.decode_rows_f64(q, k, v, w.table_np, w.lens_np, w.scale, rows)
+        step()
     dt = (time.perf_counter() - t0) / args.steps
     value = nbytes * frac / dt / 1e9
-    sample = ("each step: every sequence, query heads 0..%d of %d (%.1f%% of the rows), "
-              "float64, host cores" % (heads - 1, w.Hq, 100 * frac))
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -240,9 +257,9 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = gen.make(args.config, device=dev, seed=replica_seed(args.config, rank))
-    elt = accounting.ELT[w.dtype]
-    nbytes = accounting.algorithmic_bytes(w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt)
-    pool = pgd.PagedKVPool(w.k_pool, w.v_pool)
+    elt, q_elt = accounting.ELT[w.dtype], accounting.Q_ELT[w.dtype]
+    nbytes = accounting.algorithmic_bytes(w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt, q_elt)
+    pool = pgd.PagedKVPool(w.k_pool, w.v_pool, w.k_scale, w.v_scale)
     out = torch.empty_like(w.q)
     ws = pgd.alloc_workspace(pool, w.B, w.Hq, 0)
     stream = torch.cuda.current_stream(dev)
@@ -259,7 +276,7 @@ def run_ours(args, world, rank, local):
         q_ex = torch.randn((w.B, args.q_len, w.Hq, w.D), generator=g, device=dev).to(w.q.dtype)
         out = torch.empty_like(q_ex)
         nbytes = accounting.algorithmic_bytes_ex(w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt,
-                                                 args.q_len, args.window)
+                                                 args.q_len, args.window, q_elt)
         ws = torch.zeros(max(256, pgd.paged_gqa_workspace_size_ex(pool, w.B, args.q_len, w.Hq)),
                          dtype=torch.uint8, device=dev)
 
@@ -272,8 +289,8 @@ def run_ours(args, world, rank, local):
         # store one new token per sequence (K and V rows) at distinct slots
         g = torch.Generator(device=dev)
         g.manual_seed(w.seed + 9)
-        k_new = torch.randn((w.B, w.Hkv, w.D), generator=g, device=dev).to(w.q.dtype)
-        v_new = torch.randn((w.B, w.Hkv, w.D), generator=g, device=dev).to(w.q.dtype)
+        k_new = torch.randn((w.B, w.Hkv, w.D), generator=g, device=dev).to(w.k_pool.dtype)
+        v_new = torch.randn((w.B, w.Hkv, w.D), generator=g, device=dev).to(w.k_pool.dtype)
         slots = torch.arange(w.B, dtype=torch.int32, device=dev) * w.block_size
         nbytes = 2 * 2 * k_new.numel() * k_new.element_size() + 4 * w.B
 

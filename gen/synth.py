@@ -58,7 +58,13 @@ for _bs in (8, 16, 32, 64, 128):
                                        Hkv=8, D=128, block_size=_bs, dtype="bf16", max_len=8192,
                                        seed=1005)
 
-TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
+TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.float8_e4m3fn}
+
+# 8-bit (e4m3) pages: the Llama-3-8B and 70B layer shapes with K/V stored as
+# e4m3 codes of N(0, 1) draws and one scale per KV head drawn from U[0.5, 1.5];
+# q stays bfloat16.
+CONFIGS["llama3_8b_fp8"] = dict(CONFIGS["llama3_8b"], dtype="fp8")
+CONFIGS["long_70b_fp8"] = dict(CONFIGS["long_70b"], dtype="fp8")
 
 
 def config_names():
@@ -85,6 +91,8 @@ class Workload:
     seed: int
     lens_np: np.ndarray = field(repr=False)
     table_np: np.ndarray = field(repr=False)
+    k_scale: torch.Tensor = None   # 8-bit pages: per-KV-head scales [Hkv] float32
+    v_scale: torch.Tensor = None
 
     @property
     def G(self):
@@ -151,11 +159,16 @@ def make(name="tiny", device="cpu", poison=False, seed=None, **over):
         pos += nb[b]
 
     tdt = TORCH_DTYPES[spec["dtype"]]
+    fp8 = spec["dtype"] == "fp8"
     gen = torch.Generator(device=device)
     gen.manual_seed(int(spec["seed"]))
-    q = _randn((B, Hq, D), gen, device, tdt)
+    q = _randn((B, Hq, D), gen, device, torch.bfloat16 if fp8 else tdt)
     k_pool = _randn((num_blocks, bs, Hkv, D), gen, device, tdt)
     v_pool = _randn((num_blocks, bs, Hkv, D), gen, device, tdt)
+    k_scale = v_scale = None
+    if fp8:
+        k_scale = (0.5 + torch.rand((Hkv,), generator=gen, device=device)).to(torch.float32)
+        v_scale = (0.5 + torch.rand((Hkv,), generator=gen, device=device)).to(torch.float32)
     if poison:
         used_mask = np.zeros(num_blocks, dtype=bool)
         used_mask[perm[:used]] = True
@@ -174,15 +187,19 @@ def make(name="tiny", device="cpu", poison=False, seed=None, **over):
                     seq_lens=torch.from_numpy(lens.astype(np.int32)).to(device),
                     scale=1.0 / math.sqrt(D), B=B, Hq=Hq, Hkv=Hkv, D=D, block_size=bs,
                     num_blocks=num_blocks, max_blocks=max_blocks, dtype=spec["dtype"],
-                    seed=int(spec["seed"]), lens_np=lens, table_np=table)
+                    seed=int(spec["seed"]), lens_np=lens, table_np=table, k_scale=k_scale,
+                    v_scale=v_scale)
 
 
 def to_numpy_bits(t):
     """A float32 or bfloat16 tensor as a host numpy array the oracle accepts
-    (float32 as is, bfloat16 as its uint16 bit patterns)."""
+    (float32 as is, bfloat16 as its uint16 bit patterns, 8-bit e4m3 as uint8
+    codes)."""
     t = t.detach().to("cpu").contiguous()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype in (torch.float8_e4m3fn, torch.uint8):
+        return t.view(torch.uint8).numpy()
     if t.dtype == torch.float32:
         return t.numpy()
     raise TypeError("unsupported dtype %s" % t.dtype)

@@ -31,7 +31,9 @@
  *     block_table  [B, max_blocks]                     int32
  *     seq_lens     [B]                                 int32
  *     out          [B, Hq, D]                          dtype
- * dtype is float32 or bfloat16 (PGD_F32 / PGD_BF16); accumulation is float32.
+ * dtype is float32 or bfloat16 (PGD_F32 / PGD_BF16), or 8-bit e4m3 pages with
+ * bfloat16 q and out (PGD_FP8_E4M3, paged_kv_pool_create_fp8); accumulation
+ * is float32.
  * D (head_dim) is 64 or 128; G = Hq / Hkv is 1..64; block_size is 1..256
  * (bfloat16 pools need a power of two in 8..256).
  *
@@ -63,7 +65,7 @@ extern "C" {
 
 typedef struct pgd_pool_s *pgd_pool_t;
 
-enum pgd_dtype { PGD_F32 = 0, PGD_BF16 = 1 };
+enum pgd_dtype { PGD_F32 = 0, PGD_BF16 = 1, PGD_FP8_E4M3 = 2 };
 
 enum pgd_status {
     PGD_OK = 0,
@@ -96,6 +98,21 @@ enum pgd_status {
 int paged_kv_pool_create(pgd_pool_t *out, const void *k_pool, const void *v_pool,
                          int64_t num_blocks, int block_size, int num_kv_heads, int head_dim,
                          int dtype);
+
+/*
+ * Describe a pool pair of 8-bit K/V pages: k_pool / v_pool hold e4m3 bytes
+ * (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits, no infinities),
+ * [num_blocks, block_size, num_kv_heads, 128]; element (block, slot, h, d)
+ * stands for k_scale[h] * e4m3(byte) (v_scale[h] for V).  k_scale and
+ * v_scale are device float32 arrays of num_kv_heads entries that must outlive
+ * the handle.  Queries and outputs stay bfloat16 (q must be below 65504 in
+ * magnitude: q . K is formed in f16).  block_size: a power of two in 8..256.
+ * Quantized KV pages halve the bytes decode reads ("Modern LLM Inference ...",
+ * section 6; "The Ultimate Guide ... Part 2", "KV Cache Compression").
+ */
+int paged_kv_pool_create_fp8(pgd_pool_t *out, const void *k_pool, const void *v_pool,
+                             const float *k_scale, const float *v_scale, int64_t num_blocks,
+                             int block_size, int num_kv_heads, int head_dim);
 
 /* Release a handle (not the pools).  NULL is accepted. */
 int paged_kv_pool_destroy(pgd_pool_t pool);

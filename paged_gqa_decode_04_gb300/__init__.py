@@ -23,6 +23,7 @@ __all__ = [
 ]
 
 _DTYPES = {torch.float32: _lib.PGD_F32, torch.bfloat16: _lib.PGD_BF16}
+_FP8 = (torch.float8_e4m3fn, torch.uint8)  # 8-bit e4m3 pages (uint8 = raw codes)
 
 
 def _check(rc, what=""):
@@ -44,14 +45,17 @@ class PagedKVPool:
     Keeps references to the two tensors so they outlive the handle.
     """
 
-    def __init__(self, k_pool, v_pool):
+    def __init__(self, k_pool, v_pool, k_scale=None, v_scale=None):
+        """float32 / bfloat16 pools, or 8-bit e4m3 pages (torch.float8_e4m3fn or
+        uint8 codes) with per-KV-head float32 scales k_scale / v_scale [Hkv]."""
         lib = _lib.load()
         if not (isinstance(k_pool, torch.Tensor) and isinstance(v_pool, torch.Tensor)):
             raise TypeError("k_pool and v_pool must be torch tensors")
         if k_pool.shape != v_pool.shape or k_pool.dim() != 4:
             raise ValueError("pools must both be [num_blocks, block_size, Hkv, D]")
-        if k_pool.dtype != v_pool.dtype or k_pool.dtype not in _DTYPES:
-            raise TypeError("pools must be float32 or bfloat16, the same for K and V")
+        fp8 = k_pool.dtype in _FP8
+        if k_pool.dtype != v_pool.dtype or not (fp8 or k_pool.dtype in _DTYPES):
+            raise TypeError("pools must be float32, bfloat16 or 8-bit, the same for K and V")
         if not (k_pool.is_cuda and v_pool.is_cuda):
             raise ValueError("pools must be CUDA tensors")
         if not (k_pool.is_contiguous() and v_pool.is_contiguous()):
@@ -59,12 +63,25 @@ class PagedKVPool:
         self.k_pool, self.v_pool = k_pool, v_pool
         self.num_blocks, self.block_size, self.num_kv_heads, self.head_dim = k_pool.shape
         self.dtype = k_pool.dtype
+        self.q_dtype = torch.bfloat16 if fp8 else k_pool.dtype
+        self.k_scale, self.v_scale = k_scale, v_scale
         h = ctypes.c_void_p()
         with torch.cuda.device(k_pool.device):
-            _check(lib.paged_kv_pool_create(ctypes.byref(h), k_pool.data_ptr(), v_pool.data_ptr(),
-                                            self.num_blocks, self.block_size, self.num_kv_heads,
-                                            self.head_dim, _DTYPES[self.dtype]),
-                   "paged_kv_pool_create")
+            if fp8:
+                for sc in (k_scale, v_scale):
+                    if (not isinstance(sc, torch.Tensor) or sc.dtype != torch.float32 or
+                            not sc.is_cuda or sc.shape != (self.num_kv_heads,)):
+                        raise ValueError("8-bit pools need float32 CUDA scales [Hkv]")
+                _check(lib.paged_kv_pool_create_fp8(
+                    ctypes.byref(h), k_pool.data_ptr(), v_pool.data_ptr(), k_scale.data_ptr(),
+                    v_scale.data_ptr(), self.num_blocks, self.block_size, self.num_kv_heads,
+                    self.head_dim), "paged_kv_pool_create_fp8")
+            else:
+                _check(lib.paged_kv_pool_create(ctypes.byref(h), k_pool.data_ptr(),
+                                                v_pool.data_ptr(), self.num_blocks,
+                                                self.block_size, self.num_kv_heads,
+                                                self.head_dim, _DTYPES[self.dtype]),
+                       "paged_kv_pool_create")
         self._h = h
 
     @property
@@ -126,8 +143,8 @@ def paged_gqa_decode(pool, q, block_table, seq_lens, scale, out=None, workspace=
     lib = _lib.load()
     if q.dim() != 3 or block_table.dim() != 2 or seq_lens.dim() != 1:
         raise ValueError("q must be [B,Hq,D], block_table [B,max_blocks], seq_lens [B]")
-    if q.dtype != pool.dtype:
-        raise TypeError("q dtype must match the pool")
+    if q.dtype != pool.q_dtype:
+        raise TypeError("q must be %s for this pool" % pool.q_dtype)
     if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise TypeError("block_table and seq_lens must be int32")
     for t in (q, block_table, seq_lens):
@@ -166,8 +183,8 @@ def paged_gqa_decode_ex(pool, q, block_table, seq_lens, scale, window=0, out=Non
     lib = _lib.load()
     if q.dim() != 4 or block_table.dim() != 2 or seq_lens.dim() != 1:
         raise ValueError("q must be [B,q_len,Hq,D], block_table [B,max_blocks], seq_lens [B]")
-    if q.dtype != pool.dtype:
-        raise TypeError("q dtype must match the pool")
+    if q.dtype != pool.q_dtype:
+        raise TypeError("q must be %s for this pool" % pool.q_dtype)
     if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise TypeError("block_table and seq_lens must be int32")
     for t in (q, block_table, seq_lens):
@@ -217,9 +234,10 @@ def paged_gqa_get_error(pool, stream=None):
     return int(_lib.load().paged_gqa_get_error(pool.handle, _stream_handle(stream)))
 
 
-def decode(q, k_pool, v_pool, block_table, seq_lens, scale, num_splits=0):
+def decode(q, k_pool, v_pool, block_table, seq_lens, scale, num_splits=0, k_scale=None,
+           v_scale=None):
     """One-shot convenience: build a pool handle, decode, check device errors."""
-    pool = PagedKVPool(k_pool, v_pool)
+    pool = PagedKVPool(k_pool, v_pool, k_scale, v_scale)
     try:
         out = paged_gqa_decode(pool, q, block_table, seq_lens, scale, num_splits=num_splits)
         _check(paged_gqa_get_error(pool), "device")

@@ -56,18 +56,26 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // (d_lo = 64, slot = bs, head-half = Hkv*D/64, block = num_blocks), so that a
 // box (64, rows, hg*D/64, 1) -- `rows` slots of one block for hg consecutive
 // KV heads -- lands in shared memory head-half-major: [head-half][slot][64].
+// 8-bit pages: the same view with one 128-byte row per head (D = 128 bytes):
+// (d 128, slot, head, block), uint8 elements.
 bool encode_pool_map(CUtensorMap* map, const void* base, int64_t num_blocks, int bs, int hkv,
-                     int d, int hg) {
+                     int d, int hg, bool fp8) {
     auto fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t row_bytes = (cuuint64_t)hkv * d * 2;  // one slot, all heads
+    const int elt = fp8 ? 1 : 2;
+    const int row_elems = 128 / elt;                        // elements in a 128-byte row
+    const int rows_per_head = d * elt / 128;                // 128-byte rows of one head
+    const cuuint64_t row_bytes = (cuuint64_t)hkv * d * elt;  // one slot, all heads
     const int tile = 128 / hg;
-    cuuint64_t dims[4] = {64, (cuuint64_t)bs, (cuuint64_t)hkv * (d / 64), (cuuint64_t)num_blocks};
+    cuuint64_t dims[4] = {(cuuint64_t)row_elems, (cuuint64_t)bs,
+                          (cuuint64_t)hkv * rows_per_head, (cuuint64_t)num_blocks};
     cuuint64_t strides[3] = {row_bytes, 128, row_bytes * bs};
-    cuuint32_t box[4] = {64, (cuuint32_t)(bs < tile ? bs : tile), (cuuint32_t)(hg * (d / 64)), 1};
+    cuuint32_t box[4] = {(cuuint32_t)row_elems, (cuuint32_t)(bs < tile ? bs : tile),
+                         (cuuint32_t)(hg * rows_per_head), 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
-                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                    4, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -81,7 +89,7 @@ int resolve_parts(const Pool& p, int num_splits) {
 const Pool& pool_desc(pgd_pool_t h) { return h->p; }
 
 int choose_hg(const Pool& p, int rows) {
-    if (p.dtype != PGD_BF16) return 1;
+    if (p.dtype == PGD_F32) return 1;
     const int mt = (rows + 15) / 16;
     const int cap = mt == 1 ? 8 : mt == 2 ? 4 : 2;  // at most 8 consumer warps
     int hg = 8;
@@ -107,20 +115,25 @@ using namespace pgd;
 
 extern "C" {
 
-int paged_kv_pool_create(pgd_pool_t* out, const void* k_pool, const void* v_pool,
-                         int64_t num_blocks, int block_size, int num_kv_heads, int head_dim,
-                         int dtype) {
+static int pool_create(pgd_pool_t* out, const void* k_pool, const void* v_pool,
+                       const float* k_scale, const float* v_scale, int64_t num_blocks,
+                       int block_size, int num_kv_heads, int head_dim, int dtype) {
     if (!out) return PGD_ERR_ARG;
     *out = nullptr;
     if (!k_pool || !v_pool) return PGD_ERR_ARG;
     if (num_blocks < 1 || num_blocks > INT32_MAX || block_size < 1 || num_kv_heads < 1)
         return PGD_ERR_ARG;
-    if (dtype != PGD_F32 && dtype != PGD_BF16) return PGD_ERR_DTYPE;
+    if (dtype != PGD_F32 && dtype != PGD_BF16 && dtype != PGD_FP8_E4M3) return PGD_ERR_DTYPE;
     if (head_dim != 64 && head_dim != 128) return PGD_ERR_SHAPE;
     if (block_size > 1024) return PGD_ERR_SHAPE;
-    if (dtype == PGD_BF16 &&
+    if (dtype != PGD_F32 &&
         (block_size < 8 || block_size > 256 || (block_size & (block_size - 1)) != 0))
         return PGD_ERR_SHAPE;
+    if (dtype == PGD_FP8_E4M3) {
+        if (head_dim != 128) return PGD_ERR_SHAPE;
+        if (!k_scale || !v_scale) return PGD_ERR_ARG;
+        if (!aligned(k_scale, 4) || !aligned(v_scale, 4)) return PGD_ERR_ALIGN;
+    }
     if (!aligned(k_pool, 16) || !aligned(v_pool, 16)) return PGD_ERR_ALIGN;
 
     pgd_pool_s* h = new (std::nothrow) pgd_pool_s;
@@ -134,6 +147,8 @@ int paged_kv_pool_create(pgd_pool_t* out, const void* k_pool, const void* v_pool
     p.hkv = num_kv_heads;
     p.d = head_dim;
     p.dtype = dtype;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
     if (cudaGetDevice(&p.device) != cudaSuccess ||
         cudaDeviceGetAttribute(&p.num_sms, cudaDevAttrMultiProcessorCount, p.device) !=
             cudaSuccess ||
@@ -146,14 +161,15 @@ int paged_kv_pool_create(pgd_pool_t* out, const void* k_pool, const void* v_pool
         delete h;
         return PGD_ERR_CUDA;
     }
-    if (dtype == PGD_BF16) {
+    if (dtype != PGD_F32) {
+        const bool fp8 = dtype == PGD_FP8_E4M3;
         for (int i = 0; i < 4; ++i) {
             const int hg = 1 << i;
             if (num_kv_heads % hg != 0) continue;
             if (!encode_pool_map(&p.tmap_k[i], k_pool, num_blocks, block_size, num_kv_heads,
-                                 head_dim, hg) ||
+                                 head_dim, hg, fp8) ||
                 !encode_pool_map(&p.tmap_v[i], v_pool, num_blocks, block_size, num_kv_heads,
-                                 head_dim, hg)) {
+                                 head_dim, hg, fp8)) {
                 cudaFree(p.err);
                 delete h;
                 return PGD_ERR_CUDA;
@@ -163,6 +179,21 @@ int paged_kv_pool_create(pgd_pool_t* out, const void* k_pool, const void* v_pool
     }
     *out = h;
     return PGD_OK;
+}
+
+int paged_kv_pool_create(pgd_pool_t* out, const void* k_pool, const void* v_pool,
+                         int64_t num_blocks, int block_size, int num_kv_heads, int head_dim,
+                         int dtype) {
+    if (dtype == PGD_FP8_E4M3) return PGD_ERR_ARG;  // needs scales: paged_kv_pool_create_fp8
+    return pool_create(out, k_pool, v_pool, nullptr, nullptr, num_blocks, block_size,
+                       num_kv_heads, head_dim, dtype);
+}
+
+int paged_kv_pool_create_fp8(pgd_pool_t* out, const void* k_pool, const void* v_pool,
+                             const float* k_scale, const float* v_scale, int64_t num_blocks,
+                             int block_size, int num_kv_heads, int head_dim) {
+    return pool_create(out, k_pool, v_pool, k_scale, v_scale, num_blocks, block_size,
+                       num_kv_heads, head_dim, PGD_FP8_E4M3);
 }
 
 int paged_kv_pool_destroy(pgd_pool_t pool) {
@@ -213,12 +244,12 @@ int paged_gqa_decode_ex(pgd_pool_t pool, const void* q, int B, int q_len, int Hq
     const int G = Hq / p.hkv;
     const int rows = q_len * G;
     if (rows > kMaxGroup) return PGD_ERR_SHAPE;
-    if (p.dtype != PGD_BF16 && (q_len > 1 || window > 0)) return PGD_ERR_UNSUPPORTED;
+    if (p.dtype == PGD_F32 && (q_len > 1 || window > 0)) return PGD_ERR_UNSUPPORTED;
     if ((int64_t)max_blocks * p.block_size > INT32_MAX) return PGD_ERR_SHAPE;
     if (B == 0) return PGD_OK;
     if (!q || !out || !block_table || !seq_lens || !workspace) return PGD_ERR_ARG;
     if (max_blocks < 1) return PGD_ERR_SHAPE;
-    const size_t elt = p.dtype == PGD_BF16 ? 2 : 4;
+    const size_t elt = p.dtype == PGD_F32 ? 4 : 2;  // q / out element (bf16 for 8-bit pages)
     const size_t qbytes = (size_t)B * q_len * Hq * p.d * elt;
     {
         const uintptr_t q0 = reinterpret_cast<uintptr_t>(q), o0 = reinterpret_cast<uintptr_t>(out);
@@ -254,11 +285,13 @@ int paged_gqa_decode_ex(pgd_pool_t pool, const void* q, int B, int q_len, int Hq
     a.max_blocks = max_blocks;
     a.num_blocks = p.num_blocks;
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.k_scale = p.k_scale;
+    a.v_scale = p.v_scale;
     a.num_parts = parts;
     a.auto_parts = num_splits == 0;
     a.hg = hg;
     a.units = p.hkv / hg;
-    a.tile_tokens = p.dtype == PGD_BF16 ? 128 / hg : kSimpleTileTokens;
+    a.tile_tokens = p.dtype != PGD_F32 ? 128 / hg : kSimpleTileTokens;
     a.err = p.err;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     a.counters = reinterpret_cast<int*>(ws + wl.counters_off);
@@ -267,7 +300,7 @@ int paged_gqa_decode_ex(pgd_pool_t pool, const void* q, int B, int q_len, int Hq
     a.part_o = reinterpret_cast<float*>(ws + wl.part_o_off);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (p.dtype == PGD_BF16) {
+    if (p.dtype != PGD_F32) {
         // one launch: the TMA kernel merges split runs itself
         if (launch_decode_tma(a, p, s) != cudaSuccess) return PGD_ERR_CUDA;
     } else {

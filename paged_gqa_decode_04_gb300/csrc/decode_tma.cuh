@@ -43,6 +43,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <limits.h>
 #include <math.h>
 
@@ -157,16 +158,48 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// D = A(16x16, row) * B(16x8, col) + D; f16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two e4m3 values (low byte -> low half) to two f16: exact, every e4m3 value
+// is an f16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
+}
+
+// Two bf16 (one 32-bit word) to two f16.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&w);
+    const float2 f = __bfloat1622float2(b);
+    return pack_f16(f.x, f.y);
+}
+
 // ----------------------------------------------------------------- configuration
-template <int D_, int HG_, int MT_, int TG_, bool ROWS16_>
+template <int D_, int HG_, int MT_, int TG_, bool ROWS16_, bool FP8_ = false>
 struct Cfg {
     static constexpr int D = D_;
     static constexpr int HG = HG_;            // KV heads per unit of work
     static constexpr int MT = MT_;            // m16 row tiles of one head's query group
     static constexpr int TG = TG_;            // token groups per tile
     static constexpr bool ROWS16 = ROWS16_;   // rows 8..15 of an m-tile in use
-    static constexpr int HALVES = D / 64;     // 128-byte halves of a head row
-    static constexpr int HH = HG * HALVES;    // head-halves per tile
+    static constexpr bool FP8 = FP8_;         // 8-bit (e4m3) K/V pages, f16 products
+    // 128-byte rows of a head in a page box: D/64 for bf16, 1 for 8-bit D = 128
+    static constexpr int HALVES = FP8 ? D / 128 : D / 64;
+    static constexpr int HH = HG * HALVES;    // 128-byte head rows per token in a tile
     static constexpr int T = 128 / HG;        // tokens per tile
     static constexpr int NC = HG * MT * TG;   // consumer warps
     static constexpr int THREADS = (NC + 1) * 32;
@@ -176,11 +209,16 @@ struct Cfg {
     static constexpr int ROWS = ROWS16 ? 16 : 8;
     static constexpr int COMB_FLOATS = (TG - 1) * HG * MT * ROWS * (D + 2);
     static constexpr int COMB_BYTES = COMB_FLOATS * 4;
+    // 8-bit V is widened to f16 per 16-token step in a per-warp buffer for the
+    // transposed ldmatrix: [2 halves][16 tokens][128 B]
+    static constexpr int VBUF_BYTES = FP8 ? NC * 2 * 16 * 128 : 0;
     static constexpr int STATIC_RESERVE = 4096;  // static smem + alignment slack
-    static constexpr int STAGES_FIT = (kSmemBudget - STATIC_RESERVE - COMB_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES_FIT =
+        (kSmemBudget - STATIC_RESERVE - COMB_BYTES - VBUF_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-    // dynamic smem: [1024 align slack][stages][comb]
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + COMB_BYTES;
+    // dynamic smem: [1024 align slack][stages][comb][v buffers]
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + COMB_BYTES + VBUF_BYTES;
+    static_assert(!FP8 || D == 128, "8-bit pages: head_dim 128");
     static_assert(STAGES >= 2, "pipeline needs at least two stages");
     static_assert(TW % 16 == 0, "a warp's token slice must be whole k16 steps");
     static_assert(THREADS <= 288, "at most 8 consumer warps");
@@ -293,6 +331,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint8_t* stage_base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
     float* comb = reinterpret_cast<float*>(stage_base + S * C::STAGE_BYTES);
+    uint8_t* vbufs = stage_base + S * C::STAGE_BYTES + C::COMB_BYTES;  // 8-bit path only
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -437,6 +476,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
     uint32_t qa[D / 16][4];
     float o[D / 8][4];
+    // logit multiplier (base-2 units; times the K scale of 8-bit pages) and the
+    // V scale of 8-bit pages, set per piece
+    float s_mul = a.scale_log2, v_mul = 1.f;
+    uint8_t* vbuf = vbufs + warp * (2 * 16 * 128);
+    const uint32_t vbuf_u = smem_u32(vbuf);
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     bool seg_bad = false;
     uint32_t comb_phase = 0;
@@ -473,13 +517,31 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 qb + (row0_ok ? qrow_offset(a, dsc.b, kvh, row0) : 0));
             const uint32_t* q1 = reinterpret_cast<const uint32_t*>(
                 qb + (row1_ok ? qrow_offset(a, dsc.b, kvh, row1) : 0));
+            if constexpr (C::FP8) {
+                // f16 fragments with the head dimension permuted inside each
+                // 16-wide step: mma k-slots (2 tig, 2 tig + 1) and (2 tig + 8,
+                // 2 tig + 9) hold d = 16 ks + 4 tig + (0, 1) and + (2, 3), so
+                // that one 32-bit read of an 8-bit K row feeds both B registers.
+                // The dot product does not depend on the order of d.
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                const int c = ks * 8 + tig;  // 32-bit word index of columns 16ks + 2 tig
-                qa[ks][0] = row0_ok ? __ldg(q0 + c) : 0u;
-                qa[ks][1] = row1_ok ? __ldg(q1 + c) : 0u;
-                qa[ks][2] = row0_ok ? __ldg(q0 + c + 4) : 0u;
-                qa[ks][3] = row1_ok ? __ldg(q1 + c + 4) : 0u;
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const int c = ks * 8 + 2 * tig;  // word of columns 16ks + 4 tig
+                    qa[ks][0] = row0_ok ? bf16x2_to_f16x2(__ldg(q0 + c)) : 0u;
+                    qa[ks][1] = row1_ok ? bf16x2_to_f16x2(__ldg(q1 + c)) : 0u;
+                    qa[ks][2] = row0_ok ? bf16x2_to_f16x2(__ldg(q0 + c + 1)) : 0u;
+                    qa[ks][3] = row1_ok ? bf16x2_to_f16x2(__ldg(q1 + c + 1)) : 0u;
+                }
+                s_mul = a.scale_log2 * __ldg(a.k_scale + kvh);
+                v_mul = __ldg(a.v_scale + kvh);
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const int c = ks * 8 + tig;  // 32-bit word index of columns 16ks + 2 tig
+                    qa[ks][0] = row0_ok ? __ldg(q0 + c) : 0u;
+                    qa[ks][1] = row1_ok ? __ldg(q1 + c) : 0u;
+                    qa[ks][2] = row0_ok ? __ldg(q0 + c + 4) : 0u;
+                    qa[ks][3] = row1_ok ? __ldg(q1 + c + 4) : 0u;
+                }
             }
 #pragma unroll
             for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -498,7 +560,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const bool active = tw0 < n_valid && tw0 + C::TW > v_lo;
         const int z_hi = min(tw0 + C::TW, max(tw0, v_lo));  // zero [tw0, z_hi) ...
         const int z_lo2 = max(tw0, n_valid);                // ... and [z_lo2, tw0 + TW)
-        const bool zeroed = active && (z_hi > tw0 || z_lo2 < tw0 + C::TW);
+        // (8-bit pages: V is widened into vbuf, where those rows are zeroed)
+        const bool zeroed = !C::FP8 && active && (z_hi > tw0 || z_lo2 < tw0 + C::TW);
         if (zeroed) {
             const int n1 = z_hi - tw0;
             const int nz = n1 + (tw0 + C::TW - z_lo2);
@@ -517,17 +580,33 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             float sc[C::TW / 8][4];
 #pragma unroll
             for (int j = 0; j < C::TW / 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+            if constexpr (C::FP8) {
+                // lane (gid, tig) reads bytes 16 ks + 4 tig .. +3 of token row
+                // tw0 + 8 j + gid and widens them to the two f16 B registers
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                const int h = ks / 4;
-                const int kc = (ks % 4) * 2 + (lm_mi & 1);
+                for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll
-                for (int np = 0; np < C::TW / 16; ++np) {
-                    const int tok = tw0 + np * 16 + (lm_mi >> 1) * 8 + lm_i;
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(k_u + row_off(tok, h) + ((kc ^ lm_i) << 4), b0, b1, b2, b3);
-                    mma_bf16(sc[2 * np], qa[ks], b0, b1);
-                    mma_bf16(sc[2 * np + 1], qa[ks], b2, b3);
+                    for (int j = 0; j < C::TW / 8; ++j) {
+                        const int tok = tw0 + j * 8 + gid;
+                        const uint32_t w = *reinterpret_cast<const uint32_t*>(
+                            st + row_off(tok, 0) + ((ks ^ gid) << 4) + 4 * tig);
+                        mma_f16(sc[j], qa[ks], e4m3x2_to_f16x2((uint16_t)(w & 0xffffu)),
+                                e4m3x2_to_f16x2((uint16_t)(w >> 16)));
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const int h = ks / 4;
+                    const int kc = (ks % 4) * 2 + (lm_mi & 1);
+#pragma unroll
+                    for (int np = 0; np < C::TW / 16; ++np) {
+                        const int tok = tw0 + np * 16 + (lm_mi >> 1) * 8 + lm_i;
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(k_u + row_off(tok, h) + ((kc ^ lm_i) << 4), b0, b1, b2, b3);
+                        mma_bf16(sc[2 * np], qa[ks], b0, b1);
+                        mma_bf16(sc[2 * np + 1], qa[ks], b2, b3);
+                    }
                 }
             }
             // ---- mask (causal / window, per row), scale to base-2 units, running max
@@ -543,8 +622,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     const int tok = tw0 + j * 8 + tig * 2 + e;
                     const bool v0 = tok < hi0 && tok >= lo0;
                     const bool v1 = tok < hi1 && tok >= lo1;
-                    sc[j][e] = v0 ? sc[j][e] * a.scale_log2 : -INFINITY;
-                    sc[j][2 + e] = v1 ? sc[j][2 + e] * a.scale_log2 : -INFINITY;
+                    sc[j][e] = v0 ? sc[j][e] * s_mul : -INFINITY;
+                    sc[j][2 + e] = v1 ? sc[j][2 + e] * s_mul : -INFINITY;
                     mx0 = fmaxf(mx0, sc[j][e]);
                     mx1 = fmaxf(mx1, sc[j][2 + e]);
                 }
@@ -592,6 +671,55 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             // ---- O += P V
 #pragma unroll
             for (int kk = 0; kk < C::TW / 16; ++kk) {
+                if constexpr (C::FP8) {
+                    // widen V rows tw0 + 16 kk .. +15 to f16 in vbuf (rows
+                    // outside [v_lo, n_valid) become 0); lane: token lane / 2,
+                    // head half lane % 2 (64 values = four 16-byte chunks)
+                    const int t_loc = lane >> 1, half = lane & 1;
+                    const int tok = tw0 + kk * 16 + t_loc;
+                    const bool keep = tok >= v_lo && tok < n_valid;
+                    const uint8_t* src = st + C::TENSOR_BYTES + row_off(tok, 0);
+                    uint8_t* dst = vbuf + (half * 16 + t_loc) * 128;
+#pragma unroll 1
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const int cc = half * 4 + c4;  // 8-bit chunk: d = 16 cc .. 16 cc + 15
+                        uint4 x = make_uint4(0, 0, 0, 0);
+                        if (keep)
+                            x = *reinterpret_cast<const uint4*>(src + ((cc ^ (tok & 7)) << 4));
+                        const uint4 y0 = make_uint4(
+                            e4m3x2_to_f16x2((uint16_t)(x.x & 0xffffu)),
+                            e4m3x2_to_f16x2((uint16_t)(x.x >> 16)),
+                            e4m3x2_to_f16x2((uint16_t)(x.y & 0xffffu)),
+                            e4m3x2_to_f16x2((uint16_t)(x.y >> 16)));
+                        const uint4 y1 = make_uint4(
+                            e4m3x2_to_f16x2((uint16_t)(x.z & 0xffffu)),
+                            e4m3x2_to_f16x2((uint16_t)(x.z >> 16)),
+                            e4m3x2_to_f16x2((uint16_t)(x.w & 0xffffu)),
+                            e4m3x2_to_f16x2((uint16_t)(x.w >> 16)));
+                        const int c0 = 2 * c4;  // f16 chunk inside the half row
+                        *reinterpret_cast<uint4*>(dst + ((c0 ^ (t_loc & 7)) << 4)) = y0;
+                        *reinterpret_cast<uint4*>(dst + (((c0 + 1) ^ (t_loc & 7)) << 4)) = y1;
+                    }
+                    __syncwarp();
+                    uint32_t pa[4];
+                    pa[0] = pack_f16(sc[2 * kk][0], sc[2 * kk][1]);
+                    pa[1] = pack_f16(sc[2 * kk][2], sc[2 * kk][3]);
+                    pa[2] = pack_f16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+                    pa[3] = pack_f16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+                    const int tl = (lm_mi & 1) * 8 + lm_i;
+#pragma unroll
+                    for (int dp = 0; dp < D / 16; ++dp) {
+                        const int h = dp / 4;
+                        const int vc = (dp % 4) * 2 + (lm_mi >> 1);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(vbuf_u + (h * 16 + tl) * 128 + ((vc ^ lm_i) << 4), b0, b1, b2,
+                                  b3);
+                        mma_f16(o[2 * dp], pa, b0, b1);
+                        mma_f16(o[2 * dp + 1], pa, b2, b3);
+                    }
+                    __syncwarp();  // vbuf is rewritten for the next 16 tokens
+                    continue;
+                }
                 uint32_t pa[4];
                 pa[0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
                 pa[1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
@@ -703,8 +831,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // ---- write: whole run -> out (bf16); split run -> partial (fp32) + lse
         // a row that saw no token (window / causal range outside this piece, or
         // a query before the sequence start) has l = 0: zeros, lse = -inf
-        const float inv0 = seg_bad ? NAN : (lt0 > 0.f ? 1.f / lt0 : 0.f);
-        const float inv1 = seg_bad ? NAN : (lt1 > 0.f ? 1.f / lt1 : 0.f);
+        const float inv0 = seg_bad ? NAN : (lt0 > 0.f ? v_mul / lt0 : 0.f);
+        const float inv1 = seg_bad ? NAN : (lt1 > 0.f ? v_mul / lt1 : 0.f);
         if (!(dsc.flags & kSegPartial)) {
             __nv_bfloat16* o0 = static_cast<__nv_bfloat16*>(a.out) +
                                 (row0_ok ? qrow_offset(a, dsc.b, kvh, row0) : 0);
@@ -790,36 +918,37 @@ constexpr int token_groups(int hg, int mt) {
     return by_tokens < by_warps ? by_tokens : by_warps;
 }
 
-template <int D, int HG, int MT, bool R16>
+template <int D, int HG, int MT, bool R16, bool FP8>
 cudaError_t launch_hg(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
     constexpr int TG = token_groups(HG, MT);
     const int idx = HG == 1 ? 0 : HG == 2 ? 1 : HG == 4 ? 2 : 3;
-    return launch_cfg<Cfg<D, HG, MT, TG, R16>>(a, p.tmap_k[idx], p.tmap_v[idx], s);
+    return launch_cfg<Cfg<D, HG, MT, TG, R16, FP8>>(a, p.tmap_k[idx], p.tmap_v[idx], s);
 }
 
-template <int D, int MT, bool R16>
+template <int D, int MT, bool R16, bool FP8>
 cudaError_t launch_mt(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
     switch (a.hg) {
-        case 1: return launch_hg<D, 1, MT, R16>(a, p, s);
-        case 2: return launch_hg<D, 2, MT, R16>(a, p, s);
+        case 1: return launch_hg<D, 1, MT, R16, FP8>(a, p, s);
+        case 2: return launch_hg<D, 2, MT, R16, FP8>(a, p, s);
         case 4:
-            if constexpr (MT <= 2) return launch_hg<D, 4, MT, R16>(a, p, s);
+            if constexpr (MT <= 2) return launch_hg<D, 4, MT, R16, FP8>(a, p, s);
             break;
         case 8:
-            if constexpr (MT == 1) return launch_hg<D, 8, MT, R16>(a, p, s);
+            if constexpr (MT == 1) return launch_hg<D, 8, MT, R16, FP8>(a, p, s);
             break;
     }
     return cudaErrorInvalidValue;
 }
 
-template <int D>
+// FP8: 8-bit (e4m3) K/V pages (head_dim 128 only).
+template <int D, bool FP8 = false>
 cudaError_t launch_tma_d(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
     const int rows = a.q_len * a.group;  // query rows per KV head
-    if (rows <= 8) return launch_mt<D, 1, false>(a, p, s);
-    if (rows <= 16) return launch_mt<D, 1, true>(a, p, s);
-    if (rows <= 32) return launch_mt<D, 2, true>(a, p, s);
-    if (rows <= 48) return launch_mt<D, 3, true>(a, p, s);
-    return launch_mt<D, 4, true>(a, p, s);
+    if (rows <= 8) return launch_mt<D, 1, false, FP8>(a, p, s);
+    if (rows <= 16) return launch_mt<D, 1, true, FP8>(a, p, s);
+    if (rows <= 32) return launch_mt<D, 2, true, FP8>(a, p, s);
+    if (rows <= 48) return launch_mt<D, 3, true, FP8>(a, p, s);
+    return launch_mt<D, 4, true, FP8>(a, p, s);
 }
 
 }  // namespace tma

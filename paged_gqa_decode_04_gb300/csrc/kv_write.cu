@@ -72,7 +72,7 @@ extern "C" int paged_kv_append(pgd_pool_t pool, const void* k_new, const void* v
     if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(slot_mapping) & 3))
         return PGD_ERR_ALIGN;
     const Pool& p = pool_desc(pool);
-    const int elt = p.dtype == PGD_BF16 ? 2 : 4;
+    const int elt = p.dtype == PGD_F32 ? 4 : p.dtype == PGD_BF16 ? 2 : 1;
     const int row_vec = p.hkv * p.d * elt / 16;  // D is 64 or 128: whole vectors
     int prev = -1;
     if (cudaGetDevice(&prev) != cudaSuccess) return PGD_ERR_CUDA;
@@ -95,7 +95,7 @@ extern "C" int paged_kv_copy_blocks(pgd_pool_t pool, const int32_t* src, const i
     if (!src || !dst) return PGD_ERR_ARG;
     if (n > 65535) return PGD_ERR_SHAPE;  // grid y limit
     const Pool& p = pool_desc(pool);
-    const int elt = p.dtype == PGD_BF16 ? 2 : 4;
+    const int elt = p.dtype == PGD_F32 ? 4 : p.dtype == PGD_BF16 ? 2 : 1;
     const int64_t block_vec = (int64_t)p.block_size * p.hkv * p.d * elt / 16;
     const int chunks = (int)((block_vec + 4095) / 4096);  // <= 64 KB of each tensor per CTA
     int prev = -1;

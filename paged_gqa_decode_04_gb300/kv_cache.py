@@ -104,7 +104,8 @@ def paged_kv_append(pool, k_new, v_new, slot_mapping, stream=None):
     """Store n new tokens: k_new / v_new [n, Hkv, D] (pool dtype, CUDA),
     slot_mapping [n] int32 CUDA tensor of physical slots."""
     if k_new.shape != v_new.shape or k_new.dim() != 3 or k_new.dtype != pool.dtype:
-        raise ValueError("k_new / v_new must be [n, Hkv, D] in the pool's dtype")
+        raise ValueError("k_new / v_new must be [n, Hkv, D] in the pool's dtype (8-bit codes "
+                         "for 8-bit pools, already scaled)")
     if slot_mapping.dtype != torch.int32 or slot_mapping.numel() != k_new.shape[0]:
         raise ValueError("slot_mapping must be int32 with one slot per new token")
     for t in (k_new, v_new, slot_mapping):

@@ -12,11 +12,12 @@ F32_MAX, F32_MEAN = 1e-5, 1e-5
 
 
 def tol(dtype):
+    """float32 pools: 1e-5; bfloat16 and 8-bit pages (bf16 out, fp32 accumulation)."""
     return (F32_MAX, F32_MEAN) if dtype in ("f32", torch.float32) else (BF16_MAX, BF16_MEAN)
 
 
 def run_cuda(w, num_splits=0, stream=None, check_error=True):
-    pool = pgd.PagedKVPool(w.k_pool, w.v_pool)
+    pool = pgd.PagedKVPool(w.k_pool, w.v_pool, w.k_scale, w.v_scale)
     try:
         out = pgd.paged_gqa_decode(pool, w.q, w.block_table, w.seq_lens, w.scale,
                                    num_splits=num_splits, stream=stream)
@@ -32,9 +33,19 @@ def host(t):
     return gen.to_numpy_bits(t)
 
 
-def run_oracle(w, table=None, lens=None):
+def run_oracle(w, table=None, lens=None, q=None, window=None):
+    """Oracle answer for workload w (8-bit pages included); q [B, q_len, Hq, D]
+    and window select the multi-token / windowed form."""
     table = w.table_np if table is None else table
     lens = w.lens_np if lens is None else lens
+    qq = w.q if q is None else q
+    if w.dtype == "fp8":
+        return oracle.decode_kv8_f64(host(qq), host(w.k_pool), host(w.v_pool),
+                                     w.k_scale.cpu().numpy(), w.v_scale.cpu().numpy(), table,
+                                     lens, w.scale, window or 0)
+    if q is not None or window:
+        return oracle.decode_ex_f64(host(qq), host(w.k_pool), host(w.v_pool), table, lens,
+                                    w.scale, window or 0)
     return oracle.decode_f64(host(w.q), host(w.k_pool), host(w.v_pool), table, lens, w.scale)
 
 

@@ -70,3 +70,17 @@ def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         _lib.load(str(tmp_path / "missing.so"))
+
+
+def test_fp8_pool_create_rejects(lib):
+    h = ctypes.c_void_p()
+    # 8-bit pages need their scales: the plain create refuses the dtype
+    assert lib.paged_kv_pool_create(ctypes.byref(h), 256, 256, 10, 16, 8, 128,
+                                    _lib.PGD_FP8_E4M3) == _lib.PGD_ERR_ARG
+    assert lib.paged_kv_pool_create_fp8(ctypes.byref(h), 256, 256, None, None, 10, 16, 8,
+                                        128) == _lib.PGD_ERR_ARG
+    assert lib.paged_kv_pool_create_fp8(ctypes.byref(h), 256, 256, 256, 256, 10, 16, 8,
+                                        64) == _lib.PGD_ERR_SHAPE
+    assert lib.paged_kv_pool_create_fp8(ctypes.byref(h), 256, 256, 258, 256, 10, 16, 8,
+                                        128) == _lib.PGD_ERR_ALIGN
+    assert h.value is None

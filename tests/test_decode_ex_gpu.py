@@ -20,7 +20,7 @@ def make_q(w, q_len, seed=5):
 
 
 def run_ex(w, q, window, num_splits=0, table=None):
-    pool = pgd.PagedKVPool(w.k_pool, w.v_pool)
+    pool = pgd.PagedKVPool(w.k_pool, w.v_pool, w.k_scale, w.v_scale)
     try:
         bt = w.block_table if table is None else table
         out = pgd.paged_gqa_decode_ex(pool, q, bt, w.seq_lens, w.scale, window=window,
@@ -33,9 +33,8 @@ def run_ex(w, q, window, num_splits=0, table=None):
 
 
 def oracle_ex(w, q, window, table=None):
-    t = w.table_np if table is None else table
-    return oracle.decode_ex_f64(host(q), host(w.k_pool), host(w.v_pool), t, w.lens_np, w.scale,
-                                window)
+    from gpu_cases import run_oracle
+    return run_oracle(w, table=table, q=q, window=window)
 
 
 CASES = [
@@ -49,6 +48,8 @@ CASES = [
     ("mqa_13b_b8", dict(B=2, lens=[300, 77], max_len=512), 1, 20),
     ("sweep_bs8", dict(B=8, lens=("lognormal", 100.0, 1.0, 1, 400), max_len=512), 2, 16),
     ("sweep_bs128", dict(B=8, lens=("lognormal", 300.0, 1.0, 1, 900), max_len=1024), 2, 200),
+    ("llama3_8b_fp8", dict(B=6, lens=("uniform", 50, 900), max_len=1024), 4, 0),
+    ("llama3_8b_fp8", dict(B=6, lens=("uniform", 50, 900), max_len=1024), 2, 100),
 ]
 
 

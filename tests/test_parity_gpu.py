@@ -37,6 +37,15 @@ SMALL = {
     "group24": ("llama3_8b", dict(B=3, Hq=48, Hkv=2, lens=[90, 200, 17], max_len=256)),
     "group64": ("llama3_8b", dict(B=2, Hq=64, Hkv=1, lens=[150, 9], max_len=256)),
     "bs256": ("llama3_8b", dict(B=3, block_size=256, lens=[700, 256, 3], max_len=768)),
+    # 8-bit (e4m3) pages with per-head scales, bfloat16 q and out
+    "fp8_llama3_small": ("llama3_8b_fp8", dict(B=8, lens=("uniform", 1, 700), max_len=1024)),
+    "fp8_long_small": ("long_70b_fp8", dict(B=2, lens=("uniform", 2000, 4100), max_len=4224)),
+    "fp8_mha": ("llama3_8b_fp8", dict(B=2, Hq=40, Hkv=40, lens=[333, 64], max_len=512)),
+    "fp8_mqa": ("llama3_8b_fp8", dict(B=2, Hq=40, Hkv=1, lens=[517, 1], max_len=1024)),
+    "fp8_bs8": ("llama3_8b_fp8", dict(B=12, block_size=8, lens=("lognormal", 200.0, 1.0, 1, 900),
+                                      max_len=1024)),
+    "fp8_bs128": ("llama3_8b_fp8", dict(B=12, block_size=128,
+                                        lens=("lognormal", 200.0, 1.0, 1, 900), max_len=1024)),
 }
 
 
@@ -204,3 +213,12 @@ def test_golden_fixture_on_gpu():
     dev = lambda a: torch.from_numpy(a).to(DEV)
     out = pgd.decode(dev(q), dev(k), dev(v), dev(t), dev(L), scale)
     assert_close(out, want, "f32", "golden")
+
+
+@pytest.mark.parametrize("splits", [1, 7, 1000])
+def test_fp8_split_invariance_and_poison(splits):
+    w = gen.make("llama3_8b_fp8", device=DEV, B=6, lens=("uniform", 1, 2000), max_len=2048,
+                 poison=True)
+    want, _ = run_oracle(w)
+    out, _ = run_cuda(w, num_splits=splits)
+    assert_close(out, want, "fp8", "fp8 splits=%d" % splits)
