@@ -215,6 +215,16 @@ int paged_gqa_decode_noalloc(pgd_pool_t pool, const void *q, int B, int Hq,
 /* Size in bytes of the fixed scratch array paged_gqa_decode_noalloc uses. */
 size_t paged_gqa_noalloc_scratch_bytes(void);
 
+/*
+ * Diagnostic of the failure path: launch one thread that waits, with the
+ * bounded wait the pipeline kernels use and a limit of limit_us microseconds
+ * (1 .. 1e6), on a barrier nothing arrives on.  The wait gives up, latches
+ * PGD_ERR_TIMEOUT in the handle's error word (read it with
+ * paged_gqa_get_error) and the kernel returns; nothing faults and the context
+ * stays usable.  The pages have no counterpart; it tests this library.
+ */
+int paged_gqa_selftest_wait_timeout(pgd_pool_t pool, int64_t limit_us, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -72,6 +72,8 @@ def load(path=LIB_PATH):
     lib.paged_gqa_decode_noalloc.argtypes = [vp, vp, i32, i32, vp, i32, vp, ctypes.c_float, vp,
                                              i32, vp]
     lib.paged_gqa_decode_noalloc.restype = i32
+    lib.paged_gqa_selftest_wait_timeout.argtypes = [vp, i64, vp]
+    lib.paged_gqa_selftest_wait_timeout.restype = i32
     lib.paged_gqa_noalloc_scratch_bytes.argtypes = []
     lib.paged_gqa_noalloc_scratch_bytes.restype = sz
     # KV write path (include/paged_kv_manager.h)

@@ -94,12 +94,13 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
-// Wait for the phase of `bar` with the given parity; false after kWaitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for the phase of `bar` with the given parity; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
     return true;
 }
@@ -493,6 +494,51 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         return (uint32_t)(((p * C::HH + hh_mine + h) * R + r) * 128);
     };
 
+    // Load the query rows this warp owns for (sequence q_seq, KV head q_kvh) as
+    // mma A fragments (and, for 8-bit pages, that head's scales).
+    auto load_q = [&](int q_seq, int q_kvh) {
+        const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q);
+        const uint32_t* q0 = reinterpret_cast<const uint32_t*>(
+            qb + (row0_ok ? qrow_offset(a, q_seq, q_kvh, row0) : 0));
+        const uint32_t* q1 = reinterpret_cast<const uint32_t*>(
+            qb + (row1_ok ? qrow_offset(a, q_seq, q_kvh, row1) : 0));
+        if constexpr (C::FP8) {
+            // f16 fragments with the head dimension permuted inside each
+            // 16-wide step: mma k-slots (2 tig, 2 tig + 1) and (2 tig + 8,
+            // 2 tig + 9) hold d = 16 ks + 4 tig + (0, 1) and + (2, 3), so
+            // that one 32-bit read of an 8-bit K row feeds both B registers.
+            // The dot product does not depend on the order of d.
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const int c = ks * 8 + 2 * tig;  // word of columns 16ks + 4 tig
+                qa[ks][0] = row0_ok ? bf16x2_to_f16x2(__ldg(q0 + c)) : 0u;
+                qa[ks][1] = row1_ok ? bf16x2_to_f16x2(__ldg(q1 + c)) : 0u;
+                qa[ks][2] = row0_ok ? bf16x2_to_f16x2(__ldg(q0 + c + 1)) : 0u;
+                qa[ks][3] = row1_ok ? bf16x2_to_f16x2(__ldg(q1 + c + 1)) : 0u;
+            }
+            s_mul = a.scale_log2 * __ldg(a.k_scale + q_kvh);
+            v_mul = __ldg(a.v_scale + q_kvh);
+        } else {
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const int c = ks * 8 + tig;  // 32-bit word index of columns 16ks + 2 tig
+                qa[ks][0] = row0_ok ? __ldg(q0 + c) : 0u;
+                qa[ks][1] = row1_ok ? __ldg(q1 + c) : 0u;
+                qa[ks][2] = row0_ok ? __ldg(q0 + c + 4) : 0u;
+                qa[ks][3] = row1_ok ? __ldg(q1 + c + 4) : 0u;
+            }
+        }
+    };
+    // Prefetch the first piece's query rows while its pages are in flight.
+    int pre_seq = -1, pre_kvh = -1;
+    {
+        const TileCursor c0 = cursor_at(ss, a.seq_lens, a.units, T, a.q_len, a.window,
+                                        a.max_blocks, bs);
+        pre_seq = c0.b;
+        pre_kvh = c0.unit * C::HG + hgi;
+        load_q(pre_seq, pre_kvh);
+    }
+
     for (int it = 0; it < n_tiles; ++it) {
         const int s = it % S;
         const uint32_t ph = (uint32_t)(it / S) & 1u;
@@ -511,38 +557,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int kvh = dsc.unit * C::HG + hgi;
 
         if (dsc.flags & kSegStart) {
-            // New piece: load this warp's query rows as mma A fragments.
-            const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q);
-            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(
-                qb + (row0_ok ? qrow_offset(a, dsc.b, kvh, row0) : 0));
-            const uint32_t* q1 = reinterpret_cast<const uint32_t*>(
-                qb + (row1_ok ? qrow_offset(a, dsc.b, kvh, row1) : 0));
-            if constexpr (C::FP8) {
-                // f16 fragments with the head dimension permuted inside each
-                // 16-wide step: mma k-slots (2 tig, 2 tig + 1) and (2 tig + 8,
-                // 2 tig + 9) hold d = 16 ks + 4 tig + (0, 1) and + (2, 3), so
-                // that one 32-bit read of an 8-bit K row feeds both B registers.
-                // The dot product does not depend on the order of d.
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const int c = ks * 8 + 2 * tig;  // word of columns 16ks + 4 tig
-                    qa[ks][0] = row0_ok ? bf16x2_to_f16x2(__ldg(q0 + c)) : 0u;
-                    qa[ks][1] = row1_ok ? bf16x2_to_f16x2(__ldg(q1 + c)) : 0u;
-                    qa[ks][2] = row0_ok ? bf16x2_to_f16x2(__ldg(q0 + c + 1)) : 0u;
-                    qa[ks][3] = row1_ok ? bf16x2_to_f16x2(__ldg(q1 + c + 1)) : 0u;
-                }
-                s_mul = a.scale_log2 * __ldg(a.k_scale + kvh);
-                v_mul = __ldg(a.v_scale + kvh);
-            } else {
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const int c = ks * 8 + tig;  // 32-bit word index of columns 16ks + 2 tig
-                    qa[ks][0] = row0_ok ? __ldg(q0 + c) : 0u;
-                    qa[ks][1] = row1_ok ? __ldg(q1 + c) : 0u;
-                    qa[ks][2] = row0_ok ? __ldg(q0 + c + 4) : 0u;
-                    qa[ks][3] = row1_ok ? __ldg(q1 + c + 4) : 0u;
-                }
-            }
+            // New piece: its query rows (unless prefetched at the start).
+            if (dsc.b != pre_seq || kvh != pre_kvh) load_q(dsc.b, kvh);
+            pre_seq = -1;
 #pragma unroll
             for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
             m0 = m1 = -INFINITY;

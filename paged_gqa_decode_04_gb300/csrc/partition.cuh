@@ -70,8 +70,8 @@ struct SpanStart {
     int64_t b_base;    // tile_base[b]
 };
 
-// Every thread of the block must call this.  `scratch` is >= blockDim.x int64
-// of shared memory, `out` a shared SpanStart.  With min_tiles > 1 the spans in
+// Every thread of the block must call this; blockDim.x is a multiple of 32 and at
+// most 1024.  `scratch` is >= 64 int64 of shared memory, `out` a shared SpanStart.  With min_tiles > 1 the spans in
 // use are min(parts, ceil(N / min_tiles)) (at least 1) and CTAs beyond them get
 // an empty span; with min_tiles == 1 all `parts` spans are used.  CTA 0 also writes tile_base[0..B] to global memory for the merge
 // kernel.
@@ -80,39 +80,52 @@ __device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int
                                        int block_size, int64_t parts, int min_tiles,
                                        int64_t* scratch, SpanStart* out,
                                        int64_t* __restrict__ tile_base_out) {
-    const int nt = blockDim.x;
+    const int nt = blockDim.x;  // a multiple of 32
     const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
     const int per = (B + nt - 1) / nt;
     const int b_lo = min(B, tid * per);
     const int b_hi = min(B, b_lo + per);
     int64_t local = 0;
     for (int b = b_lo; b < b_hi; ++b)
         local += (int64_t)units * tiles_of(seq_lens[b], max_blocks, block_size, T, q_len, window);
-    scratch[tid] = local;
+    // block-wide exclusive scan of the per-thread sums: warp shuffles, then the
+    // warp totals scanned by warp 0 (scratch[32 + w] = inclusive prefix of warps)
+    int64_t incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int64_t v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) scratch[warp] = incl;
     __syncthreads();
-    if (tid == 0) {  // exclusive scan of per-thread sums (nt is small)
-        int64_t run = 0;
-        for (int i = 0; i < nt; ++i) {
-            int64_t v = scratch[i];
-            scratch[i] = run;
-            run += v;
+    if (warp == 0) {
+        int64_t w = lane < nwarps ? scratch[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int64_t v = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += v;
         }
-        int64_t p = parts;
-        if (min_tiles > 1) {  // fewer spans only when asked for
-            p = (run + min_tiles - 1) / min_tiles;
-            p = p < parts ? p : parts;
-            p = p > 0 ? p : 1;
+        if (lane < nwarps) scratch[32 + lane] = w;
+        if (lane == nwarps - 1) {
+            const int64_t run = w;  // N
+            int64_t p = parts;
+            if (min_tiles > 1) {  // fewer spans only when asked for
+                p = (run + min_tiles - 1) / min_tiles;
+                p = p < parts ? p : parts;
+                p = p > 0 ? p : 1;
+            }
+            out->n_total = run;
+            out->parts = p;
+            out->r0 = blockIdx.x < p ? span_begin(blockIdx.x, run, p) : run;
+            out->r1 = blockIdx.x < p ? span_begin(blockIdx.x + 1, run, p) : run;
+            out->b = -1;
+            out->b_base = 0;
         }
-        out->n_total = run;
-        out->parts = p;
-        out->r0 = blockIdx.x < p ? span_begin(blockIdx.x, run, p) : run;
-        out->r1 = blockIdx.x < p ? span_begin(blockIdx.x + 1, run, p) : run;
-        out->b = -1;
-        out->b_base = 0;
     }
     __syncthreads();
     const int64_t r0 = out->r0;
-    int64_t run = scratch[tid];
+    int64_t run = (warp ? scratch[32 + warp - 1] : 0) + incl - local;  // exclusive prefix
     for (int b = b_lo; b < b_hi; ++b) {
         int64_t n =
             (int64_t)units * tiles_of(seq_lens[b], max_blocks, block_size, T, q_len, window);
