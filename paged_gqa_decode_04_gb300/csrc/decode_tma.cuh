@@ -226,6 +226,15 @@ struct Cfg {
 };
 
 // What the producer tells the consumers about the tile in a stage.
+// A run whose pieces this warp brought to completion: merged after the tile loop.
+struct MergeJob {
+    int64_t t0;     // first tile of the run
+    int64_t c0;     // CTA of its first piece
+    int npieces;
+    int first_is_tail;
+    int b, kvh;     // b < 0: no job
+};
+
 struct StageDesc {
     int64_t run_start;  // flat index of tile 0 of the (b, unit) run
     int b, unit, n_valid, flags;
@@ -247,67 +256,104 @@ __device__ __forceinline__ int64_t qrow_offset(const DecodeArgs& a, int b, int k
 // write them to `out`.  Log-sum-exp combination in base 2: with lse_k = m_k +
 // log2 l_k and o_k the normalised partial of piece k,
 //     out = sum_k 2^(lse_k - M) o_k / sum_k 2^(lse_k - M),  M = max_k lse_k,
-// accumulated online.  Rows one after another; the lanes cover a row's
-// columns with float4 reads (two rows per pass when D = 64) and kPieceBatch
-// pieces are read before any is used, so a run of many pieces costs few L2
-// round trips.
+// accumulated online.  The lanes cover a row's columns with float4 reads, and
+// each lane keeps kMergeRows slots: a slot is a row pass, or (PHASED, when the
+// warp's rows fit one pass) every slot takes the same rows and piece phase x
+// (pieces x, x + RU, ...), the slots folded together at the end.  kPieceBatch
+// pieces per slot are read before any is used, so a lane has 16 loads in
+// flight.  Runs after the tile loop, when the loop's accumulators are dead.
 constexpr int kPieceBatch = 4;
+constexpr int kMergeRows = 4;
 
-template <class C>
+__device__ __forceinline__ void lse_fold(float& M, float& W, float4& acc, float e, float w,
+                                         float4 v) {
+    // (M, W, acc) holds acc = sum_k 2^(lse_k - M) o_k and W = sum_k 2^(lse_k - M);
+    // add a term that is (e, w, v) in the same form: a piece is (lse, 1, o),
+    // another slot is (M', W', acc')
+    const float nm = fmaxf(M, e);
+    const float base = nm == -INFINITY ? 0.f : nm;
+    const float sa = fast_exp2(M - base), sb = fast_exp2(e - base);
+    M = nm;
+    W = W * sa + w * sb;
+    acc.x = acc.x * sa + v.x * sb;
+    acc.y = acc.y * sa + v.y * sb;
+    acc.z = acc.z * sa + v.z * sb;
+    acc.w = acc.w * sa + v.w * sb;
+}
+
+template <class C, bool PHASED>
 __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int64_t t0, int64_t N, int64_t P,
                                           int64_t c0, int npieces, bool first_is_tail, int hgi,
                                           int mt, int b, int kvh) {
     constexpr int D = C::D;
     constexpr int CPR = D / 4;             // float4 chunks per row
     constexpr int RPP = 32 / CPR;          // rows per pass
+    constexpr int RU = kMergeRows;
+    constexpr int PB = kPieceBatch;
     const int lane = threadIdx.x % 32;
     const int rows = a.q_len * a.group;    // query rows per KV head
     const int piece_rows = C::HG * rows;
     const int r_lo = mt * 16;
     const int r_hi = min(rows, r_lo + C::ROWS);
     const int col = (lane % CPR) * 4;
-    for (int rb = r_lo; rb < r_hi; rb += RPP) {
-        const int r = rb + lane / CPR;
-        const bool rok = r < r_hi;
-        const int64_t pr = (int64_t)(hgi * rows + r);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float M = -INFINITY, W = 0.f;
-        for (int k0 = 0; k0 < npieces; k0 += kPieceBatch) {
-            float4 v[kPieceBatch];
-            float e[kPieceBatch];
+    constexpr int npe = PHASED ? 1 : RU;  // row passes per round
+    constexpr int rep = RU / npe;          // piece phases per row pass
+    for (int rb = r_lo; rb < r_hi; rb += RPP * npe) {
+        int r[RU], ph[RU];
+        bool rok[RU];
+        int64_t pr[RU];
+        float4 acc[RU];
+        float M[RU], W[RU];
 #pragma unroll
-            for (int u = 0; u < kPieceBatch; ++u) {
-                const int k = k0 + u;
-                const bool ok = rok && k < npieces;
-                // with P > N every non-empty span holds one tile: piece k is the
-                // owner of tile t0 + k; otherwise the pieces are CTAs c0, c0+1, ...
-                const int64_t c = P > N ? span_owner(t0 + k, N, P) : c0 + k;
-                const int64_t sl = c * 2 + ((first_is_tail && k == 0) ? 1 : 0);
-                v[u] = ok ? __ldcg(reinterpret_cast<const float4*>(a.part_o +
-                                                                   (sl * piece_rows + pr) * D + col))
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-                e[u] = ok ? __ldcg(a.part_lse + sl * piece_rows + pr) : -INFINITY;
+        for (int x = 0; x < RU; ++x) {
+            ph[x] = x / npe;
+            r[x] = rb + (x % npe) * RPP + lane / CPR;
+            rok[x] = ph[x] < rep && r[x] < r_hi;
+            pr[x] = (int64_t)(hgi * rows + r[x]);
+            acc[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+            M[x] = -INFINITY;
+            W[x] = 0.f;
+        }
+        for (int k0 = 0; k0 < npieces; k0 += PB * rep) {
+            float4 v[RU][PB];
+            float e[RU][PB];
+#pragma unroll
+            for (int u = 0; u < PB; ++u) {
+#pragma unroll
+                for (int x = 0; x < RU; ++x) {
+                    const int k = k0 + ph[x] + rep * u;
+                    const bool ok = rok[x] && k < npieces;
+                    // with P > N every non-empty span holds one tile: piece k is
+                    // the owner of tile t0 + k; otherwise the pieces are CTAs
+                    // c0, c0 + 1, ...
+                    const int64_t c = P > N ? (ok ? span_owner(t0 + k, N, P) : 0) : c0 + k;
+                    const int64_t sl = c * 2 + ((first_is_tail && k == 0) ? 1 : 0);
+                    v[x][u] = ok ? __ldcg(reinterpret_cast<const float4*>(
+                                       a.part_o + (sl * piece_rows + pr[x]) * D + col))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                    e[x][u] = ok ? __ldcg(a.part_lse + sl * piece_rows + pr[x]) : -INFINITY;
+                }
             }
 #pragma unroll
-            for (int u = 0; u < kPieceBatch; ++u) {
-                const float nm = fmaxf(M, e[u]);
-                const float base = nm == -INFINITY ? 0.f : nm;
-                const float sa = fast_exp2(M - base), sb = fast_exp2(e[u] - base);
-                M = nm;
-                W = W * sa + sb;
-                acc.x = acc.x * sa + v[u].x * sb;
-                acc.y = acc.y * sa + v[u].y * sb;
-                acc.z = acc.z * sa + v[u].z * sb;
-                acc.w = acc.w * sa + v[u].w * sb;
+            for (int x = 0; x < RU; ++x) {
+#pragma unroll
+                for (int u = 0; u < PB; ++u) lse_fold(M[x], W[x], acc[x], e[x][u], 1.f, v[x][u]);
             }
         }
-        if (rok) {
-            const float w = W > 0.f ? 1.f / W : 0.f;  // no token in any piece: zeros
+        // fold the other piece phases of a row pass into its first slot
+#pragma unroll
+        for (int x = npe; x < RU; ++x) {
+            if (rok[x]) lse_fold(M[x % npe], W[x % npe], acc[x % npe], M[x], W[x], acc[x]);
+        }
+#pragma unroll
+        for (int x = 0; x < RU; ++x) {
+            if (x >= npe || !rok[x]) continue;
+            const float w = W[x] > 0.f ? 1.f / W[x] : 0.f;  // no token in any piece: zeros
             uint2 pk;
-            pk.x = pack_bf16(acc.x * w, acc.y * w);
-            pk.y = pack_bf16(acc.z * w, acc.w * w);
+            pk.x = pack_bf16(acc[x].x * w, acc[x].y * w);
+            pk.y = pack_bf16(acc[x].z * w, acc[x].w * w);
             *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) +
-                                      qrow_offset(a, b, kvh, r) + col) = pk;
+                                      qrow_offset(a, b, kvh, r[x]) + col) = pk;
         }
     }
 }
@@ -327,6 +373,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     __shared__ __align__(8) uint64_t empty_bar[S];
     __shared__ __align__(8) uint64_t comb_bar;
     __shared__ StageDesc desc[S];
+    __shared__ MergeJob jobs[C::NC][2];  // per consumer warp and partial slot
     __shared__ volatile int aborted;
 
     uint8_t* stage_base = reinterpret_cast<uint8_t*>(
@@ -347,6 +394,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_init(smem_u32(&empty_bar[s]), C::NC * 32);
         }
         mbar_init(smem_u32(&comb_bar), C::NC * 32);
+        for (int w = 0; w < C::NC; ++w) jobs[w][0].b = jobs[w][1].b = -1;
         aborted = 0;
         fence_barrier_init();
     }
@@ -900,16 +948,31 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int64_t c0 = span_owner(t0, N, P);
         const int npieces = P > N ? dsc.n_b : (int)(span_owner(t0 + dsc.n_b - 1, N, P) - c0 + 1);
         const bool first_is_tail = P <= N && span_begin(c0, N, P) < t0;
-        int last = 0;
         if (lane == 0) {
             int* ctr = a.counters + ((int64_t)dsc.b * a.hkv + kvh) * C::MT + mt;
-            last = atomicAdd(ctr, 1) == npieces - 1;
-            if (last) atomicExch(ctr, 0);
+            if (atomicAdd(ctr, 1) == npieces - 1) {
+                atomicExch(ctr, 0);
+                // one piece per partial slot and CTA, so one job per slot
+                jobs[warp][(dsc.flags & kSegSlot1) ? 1 : 0] =
+                    MergeJob{t0, c0, npieces, first_is_tail ? 1 : 0, dsc.b, kvh};
+            }
         }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (!last) continue;
+    }
+    // ---- merge the runs this warp completed
+    __syncwarp();
+    if (aborted) return;
+#pragma unroll 1
+    for (int j = 0; j < 2; ++j) {
+        const MergeJob jb = jobs[warp][j];
+        if (jb.b < 0) continue;
         __threadfence();
-        merge_pieces<C>(a, t0, N, P, c0, npieces, first_is_tail, hgi, mt, dsc.b, kvh);
+        constexpr int RPP = 32 / (D / 4);  // rows per merge pass
+        if (min(rows - mt * 16, C::ROWS) <= RPP)
+            merge_pieces<C, true>(a, jb.t0, ss.n_total, ss.parts, jb.c0, jb.npieces,
+                                  jb.first_is_tail != 0, hgi, mt, jb.b, jb.kvh);
+        else
+            merge_pieces<C, false>(a, jb.t0, ss.n_total, ss.parts, jb.c0, jb.npieces,
+                                   jb.first_is_tail != 0, hgi, mt, jb.b, jb.kvh);
     }
 }
 
