@@ -210,22 +210,17 @@ struct Cfg {
     static constexpr int ROWS = ROWS16 ? 16 : 8;
     static constexpr int COMB_FLOATS = (TG - 1) * HG * MT * ROWS * (D + 2);
     static constexpr int COMB_BYTES = COMB_FLOATS * 4;
-    // 8-bit V is widened to f16 per 16-token step in a per-warp buffer for the
-    // transposed ldmatrix: [2 halves][16 tokens][128 B]
-    static constexpr int VBUF_BYTES = FP8 ? NC * 2 * 16 * 128 : 0;
     static constexpr int STATIC_RESERVE = 4096;  // static smem + alignment slack
-    static constexpr int STAGES_FIT =
-        (kSmemBudget - STATIC_RESERVE - COMB_BYTES - VBUF_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES_FIT = (kSmemBudget - STATIC_RESERVE - COMB_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-    // dynamic smem: [1024 align slack][stages][comb][v buffers]
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + COMB_BYTES + VBUF_BYTES;
+    // dynamic smem: [1024 align slack][stages][comb]
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + COMB_BYTES;
     static_assert(!FP8 || D == 128, "8-bit pages: head_dim 128");
     static_assert(STAGES >= 2, "pipeline needs at least two stages");
     static_assert(TW % 16 == 0, "a warp's token slice must be whole k16 steps");
     static_assert(THREADS <= 288, "at most 8 consumer warps");
 };
 
-// What the producer tells the consumers about the tile in a stage.
 // A run whose pieces this warp brought to completion: merged after the tile loop.
 struct MergeJob {
     int64_t t0;     // first tile of the run
@@ -235,6 +230,7 @@ struct MergeJob {
     int b, kvh;     // b < 0: no job
 };
 
+// What the producer tells the consumers about the tile in a stage.
 struct StageDesc {
     int64_t run_start;  // flat index of tile 0 of the (b, unit) run
     int b, unit, n_valid, flags;
@@ -379,7 +375,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint8_t* stage_base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
     float* comb = reinterpret_cast<float*>(stage_base + S * C::STAGE_BYTES);
-    uint8_t* vbufs = stage_base + S * C::STAGE_BYTES + C::COMB_BYTES;  // 8-bit path only
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -528,8 +523,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // logit multiplier (base-2 units; times the K scale of 8-bit pages) and the
     // V scale of 8-bit pages, set per piece
     float s_mul = a.scale_log2, v_mul = 1.f;
-    uint8_t* vbuf = vbufs + warp * (2 * 16 * 128);
-    const uint32_t vbuf_u = smem_u32(vbuf);
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     bool seg_bad = false;
     uint32_t comb_phase = 0;
@@ -625,8 +618,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const bool active = tw0 < n_valid && tw0 + C::TW > v_lo;
         const int z_hi = min(tw0 + C::TW, max(tw0, v_lo));  // zero [tw0, z_hi) ...
         const int z_lo2 = max(tw0, n_valid);                // ... and [z_lo2, tw0 + TW)
-        // (8-bit pages: V is widened into vbuf, where those rows are zeroed)
-        const bool zeroed = !C::FP8 && active && (z_hi > tw0 || z_lo2 < tw0 + C::TW);
+        const bool zeroed = active && (z_hi > tw0 || z_lo2 < tw0 + C::TW);
         if (zeroed) {
             const int n1 = z_hi - tw0;
             const int nz = n1 + (tw0 + C::TW - z_lo2);
@@ -737,52 +729,36 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
             for (int kk = 0; kk < C::TW / 16; ++kk) {
                 if constexpr (C::FP8) {
-                    // widen V rows tw0 + 16 kk .. +15 to f16 in vbuf (rows
-                    // outside [v_lo, n_valid) become 0); lane: token lane / 2,
-                    // head half lane % 2 (64 values = four 16-byte chunks)
-                    const int t_loc = lane >> 1, half = lane & 1;
-                    const int tok = tw0 + kk * 16 + t_loc;
-                    const bool keep = tok >= v_lo && tok < n_valid;
-                    const uint8_t* src = st + C::TENSOR_BYTES + row_off(tok, 0);
-                    uint8_t* dst = vbuf + (half * 16 + t_loc) * 128;
-#pragma unroll 1
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        const int cc = half * 4 + c4;  // 8-bit chunk: d = 16 cc .. 16 cc + 15
-                        uint4 x = make_uint4(0, 0, 0, 0);
-                        if (keep)
-                            x = *reinterpret_cast<const uint4*>(src + ((cc ^ (tok & 7)) << 4));
-                        const uint4 y0 = make_uint4(
-                            e4m3x2_to_f16x2((uint16_t)(x.x & 0xffffu)),
-                            e4m3x2_to_f16x2((uint16_t)(x.x >> 16)),
-                            e4m3x2_to_f16x2((uint16_t)(x.y & 0xffffu)),
-                            e4m3x2_to_f16x2((uint16_t)(x.y >> 16)));
-                        const uint4 y1 = make_uint4(
-                            e4m3x2_to_f16x2((uint16_t)(x.z & 0xffffu)),
-                            e4m3x2_to_f16x2((uint16_t)(x.z >> 16)),
-                            e4m3x2_to_f16x2((uint16_t)(x.w & 0xffffu)),
-                            e4m3x2_to_f16x2((uint16_t)(x.w >> 16)));
-                        const int c0 = 2 * c4;  // f16 chunk inside the half row
-                        *reinterpret_cast<uint4*>(dst + ((c0 ^ (t_loc & 7)) << 4)) = y0;
-                        *reinterpret_cast<uint4*>(dst + (((c0 + 1) ^ (t_loc & 7)) << 4)) = y1;
-                    }
-                    __syncwarp();
+                    // 8-bit V straight from the stage: a transposed 16-bit ldmatrix
+                    // gives lane (gid, tig) tokens (2 tig, 2 tig + 1) x bytes
+                    // d = (2 gid, 2 gid + 1) of a 16-byte chunk; one byte permute
+                    // puts the two tokens of d = 2 gid in the low half and those of
+                    // 2 gid + 1 in the high half, each an e4m3x2 B operand.  n-tile
+                    // 2 c + par then holds d = 16 c + 2 j + par for B column j, so
+                    // the output columns come out permuted (undone where O is stored).
                     uint32_t pa[4];
                     pa[0] = pack_f16(sc[2 * kk][0], sc[2 * kk][1]);
                     pa[1] = pack_f16(sc[2 * kk][2], sc[2 * kk][3]);
                     pa[2] = pack_f16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
                     pa[3] = pack_f16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
-                    const int tl = (lm_mi & 1) * 8 + lm_i;
+                    const int tok = tw0 + kk * 16 + (lm_mi & 1) * 8 + lm_i;
 #pragma unroll
-                    for (int dp = 0; dp < D / 16; ++dp) {
-                        const int h = dp / 4;
-                        const int vc = (dp % 4) * 2 + (lm_mi >> 1);
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4_t(vbuf_u + (h * 16 + tl) * 128 + ((vc ^ lm_i) << 4), b0, b1, b2,
-                                  b3);
-                        mma_f16(o[2 * dp], pa, b0, b1);
-                        mma_f16(o[2 * dp + 1], pa, b2, b3);
+                    for (int c2 = 0; c2 < D / 32; ++c2) {
+                        const int vc = c2 * 2 + (lm_mi >> 1);
+                        uint32_t r[4];
+                        ldsm_x4_t(v_u + row_off(tok, 0) + ((vc ^ lm_i) << 4), r[0], r[1], r[2],
+                                  r[3]);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) r[q] = __byte_perm(r[q], 0u, 0x3120);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {  // chunk 2 c2 + h: r[2h] tokens 0-7, r[2h+1] 8-15
+                            const int n = 4 * c2 + 2 * h;
+                            mma_f16(o[n], pa, e4m3x2_to_f16x2((uint16_t)(r[2 * h] & 0xffffu)),
+                                    e4m3x2_to_f16x2((uint16_t)(r[2 * h + 1] & 0xffffu)));
+                            mma_f16(o[n + 1], pa, e4m3x2_to_f16x2((uint16_t)(r[2 * h] >> 16)),
+                                    e4m3x2_to_f16x2((uint16_t)(r[2 * h + 1] >> 16)));
+                        }
                     }
-                    __syncwarp();  // vbuf is rewritten for the next 16 tokens
                     continue;
                 }
                 uint32_t pa[4];
@@ -903,14 +879,29 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                 (row0_ok ? qrow_offset(a, dsc.b, kvh, row0) : 0);
             __nv_bfloat16* o1 = static_cast<__nv_bfloat16*>(a.out) +
                                 (row1_ok ? qrow_offset(a, dsc.b, kvh, row1) : 0);
+            if constexpr (C::FP8) {
+                // n-tiles 2c, 2c+1 hold d = 16 c + 4 tig + (0, 2) and (1, 3)
 #pragma unroll
-            for (int n = 0; n < D / 8; ++n) {
-                if (row0_ok)
-                    *reinterpret_cast<uint32_t*>(o0 + n * 8 + tig * 2) =
-                        pack_bf16(o[n][0] * inv0, o[n][1] * inv0);
-                if (row1_ok)
-                    *reinterpret_cast<uint32_t*>(o1 + n * 8 + tig * 2) =
-                        pack_bf16(o[n][2] * inv1, o[n][3] * inv1);
+                for (int c = 0; c < D / 16; ++c) {
+                    if (row0_ok)
+                        *reinterpret_cast<uint2*>(o0 + 16 * c + 4 * tig) =
+                            make_uint2(pack_bf16(o[2 * c][0] * inv0, o[2 * c + 1][0] * inv0),
+                                       pack_bf16(o[2 * c][1] * inv0, o[2 * c + 1][1] * inv0));
+                    if (row1_ok)
+                        *reinterpret_cast<uint2*>(o1 + 16 * c + 4 * tig) =
+                            make_uint2(pack_bf16(o[2 * c][2] * inv1, o[2 * c + 1][2] * inv1),
+                                       pack_bf16(o[2 * c][3] * inv1, o[2 * c + 1][3] * inv1));
+                }
+            } else {
+#pragma unroll
+                for (int n = 0; n < D / 8; ++n) {
+                    if (row0_ok)
+                        *reinterpret_cast<uint32_t*>(o0 + n * 8 + tig * 2) =
+                            pack_bf16(o[n][0] * inv0, o[n][1] * inv0);
+                    if (row1_ok)
+                        *reinterpret_cast<uint32_t*>(o1 + n * 8 + tig * 2) =
+                            pack_bf16(o[n][2] * inv1, o[n][3] * inv1);
+                }
             }
             continue;
         }
@@ -918,14 +909,28 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int prow0 = hgi * rows + row0, prow1 = hgi * rows + row1;  // rows of the piece
         {
             float* po = a.part_o + slot * piece_rows * D;
+            if constexpr (C::FP8) {
 #pragma unroll
-            for (int n = 0; n < D / 8; ++n) {
-                if (row0_ok)
-                    *reinterpret_cast<float2*>(po + (int64_t)prow0 * D + n * 8 + tig * 2) =
-                        make_float2(o[n][0] * inv0, o[n][1] * inv0);
-                if (row1_ok)
-                    *reinterpret_cast<float2*>(po + (int64_t)prow1 * D + n * 8 + tig * 2) =
-                        make_float2(o[n][2] * inv1, o[n][3] * inv1);
+                for (int c = 0; c < D / 16; ++c) {
+                    if (row0_ok)
+                        *reinterpret_cast<float4*>(po + (int64_t)prow0 * D + 16 * c + 4 * tig) =
+                            make_float4(o[2 * c][0] * inv0, o[2 * c + 1][0] * inv0,
+                                        o[2 * c][1] * inv0, o[2 * c + 1][1] * inv0);
+                    if (row1_ok)
+                        *reinterpret_cast<float4*>(po + (int64_t)prow1 * D + 16 * c + 4 * tig) =
+                            make_float4(o[2 * c][2] * inv1, o[2 * c + 1][2] * inv1,
+                                        o[2 * c][3] * inv1, o[2 * c + 1][3] * inv1);
+                }
+            } else {
+#pragma unroll
+                for (int n = 0; n < D / 8; ++n) {
+                    if (row0_ok)
+                        *reinterpret_cast<float2*>(po + (int64_t)prow0 * D + n * 8 + tig * 2) =
+                            make_float2(o[n][0] * inv0, o[n][1] * inv0);
+                    if (row1_ok)
+                        *reinterpret_cast<float2*>(po + (int64_t)prow1 * D + n * 8 + tig * 2) =
+                            make_float2(o[n][2] * inv1, o[n][3] * inv1);
+                }
             }
             if (tig == 0) {
                 float* pl = a.part_lse + slot * piece_rows;
