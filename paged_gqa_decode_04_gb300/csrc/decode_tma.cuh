@@ -638,17 +638,25 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
             for (int j = 0; j < C::TW / 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
             if constexpr (C::FP8) {
-                // lane (gid, tig) reads bytes 16 ks + 4 tig .. +3 of token row
-                // tw0 + 8 j + gid and widens them to the two f16 B registers
+                // lane (gid, tig) needs bytes 16 ks + 4 tig .. +3 of token row
+                // tw0 + 8 j + gid, widened to the two f16 B registers: one
+                // ldmatrix.x4 brings them for n-tiles (jp, jp + 1) x k-steps
+                // (ks, ks + 1)
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
+                for (int ks = 0; ks < D / 16; ks += 2) {
 #pragma unroll
-                    for (int j = 0; j < C::TW / 8; ++j) {
-                        const int tok = tw0 + j * 8 + gid;
-                        const uint32_t w = *reinterpret_cast<const uint32_t*>(
-                            st + row_off(tok, 0) + ((ks ^ gid) << 4) + 4 * tig);
-                        mma_f16(sc[j], qa[ks], e4m3x2_to_f16x2((uint16_t)(w & 0xffffu)),
-                                e4m3x2_to_f16x2((uint16_t)(w >> 16)));
+                    for (int jp = 0; jp < C::TW / 8; jp += 2) {
+                        const int tok = tw0 + (jp + (lm_mi & 1)) * 8 + lm_i;
+                        const int kc = ks + (lm_mi >> 1);
+                        uint32_t w[4];
+                        ldsm_x4(k_u + row_off(tok, 0) + ((kc ^ lm_i) << 4), w[0], w[1], w[2],
+                                w[3]);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            mma_f16(sc[jp + (q & 1)], qa[ks + (q >> 1)],
+                                    e4m3x2_to_f16x2((uint16_t)(w[q] & 0xffffu)),
+                                    e4m3x2_to_f16x2((uint16_t)(w[q] >> 16)));
+                        }
                     }
                 }
             } else {
@@ -672,17 +680,33 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const int lo0 = a.window > 0 ? hi0 - a.window : INT_MIN;
             const int lo1 = a.window > 0 ? hi1 - a.window : INT_MIN;
             float mx0 = -INFINITY, mx1 = -INFINITY;
+            // every row sees all of this warp's tokens (the usual case): no mask
+            const bool full = tw0 + C::TW <= dsc.L - a.q_len + 1 - dsc.tok0 &&
+                              (a.window == 0 || tw0 >= dsc.L - a.window - dsc.tok0);
+            if (full) {
 #pragma unroll
-            for (int j = 0; j < C::TW / 8; ++j) {
+                for (int j = 0; j < C::TW / 8; ++j) {
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int tok = tw0 + j * 8 + tig * 2 + e;
-                    const bool v0 = tok < hi0 && tok >= lo0;
-                    const bool v1 = tok < hi1 && tok >= lo1;
-                    sc[j][e] = v0 ? sc[j][e] * s_mul : -INFINITY;
-                    sc[j][2 + e] = v1 ? sc[j][2 + e] * s_mul : -INFINITY;
-                    mx0 = fmaxf(mx0, sc[j][e]);
-                    mx1 = fmaxf(mx1, sc[j][2 + e]);
+                    for (int e = 0; e < 2; ++e) {
+                        sc[j][e] *= s_mul;
+                        sc[j][2 + e] *= s_mul;
+                        mx0 = fmaxf(mx0, sc[j][e]);
+                        mx1 = fmaxf(mx1, sc[j][2 + e]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < C::TW / 8; ++j) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int tok = tw0 + j * 8 + tig * 2 + e;
+                        const bool v0 = tok < hi0 && tok >= lo0;
+                        const bool v1 = tok < hi1 && tok >= lo1;
+                        sc[j][e] = v0 ? sc[j][e] * s_mul : -INFINITY;
+                        sc[j][2 + e] = v1 ? sc[j][2 + e] * s_mul : -INFINITY;
+                        mx0 = fmaxf(mx0, sc[j][e]);
+                        mx1 = fmaxf(mx1, sc[j][2 + e]);
+                    }
                 }
             }
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
