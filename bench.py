@@ -8,7 +8,9 @@ resident in HBM.  The default workload is the Llama-3-8B layer shape: B=64
 sequences, lengths uniform in [128, 4096], Hq=32, Hkv=8, D=128, 16-token
 blocks, bf16, a pool of ceil(1.1 * used) blocks with a seeded shuffled block
 table.  Its K/V (about 0.6 GB) is larger than L2, so no flush is needed between
-steps.  Rank 0 prints one JSON line.
+steps.  The K timed steps are captured as one CUDA graph and replayed, as a
+serving loop replays its decode step (--launch stream launches them one by one
+from Python instead).  Rank 0 prints one JSON line.
 
 --impl reference times the float64 CPU oracle on the host cores instead (the
 comparison arm), over the same workload.
@@ -169,6 +171,12 @@ def whole_job_gbs(nbytes, t_ms, world):
     return world * nbytes / (t_ms * 1e-3) / 1e9
 
 
+def launch_note(args):
+    if args.launch == "graph":
+        return "the %d timed steps captured as one CUDA graph, replayed once" % args.steps
+    return "the %d timed steps launched one by one on one stream" % args.steps
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -264,9 +272,9 @@ def run_ours(args, world, rank, local):
     ws = pgd.alloc_workspace(pool, w.B, w.Hq, 0)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def step(s=None):
         pgd.paged_gqa_decode(pool, w.q, w.block_table, w.seq_lens, w.scale, out=out,
-                             workspace=ws, stream=stream)
+                             workspace=ws, stream=s or stream)
 
     op_note = "decode: one query token per sequence"
     if args.op == "decode_ex":
@@ -280,9 +288,9 @@ def run_ours(args, world, rank, local):
         ws = torch.zeros(max(256, pgd.paged_gqa_workspace_size_ex(pool, w.B, args.q_len, w.Hq)),
                          dtype=torch.uint8, device=dev)
 
-        def step():
+        def step(s=None):
             pgd.paged_gqa_decode_ex(pool, q_ex, w.block_table, w.seq_lens, w.scale,
-                                    window=args.window, out=out, workspace=ws, stream=stream)
+                                    window=args.window, out=out, workspace=ws, stream=s or stream)
 
         op_note = "decode_ex: %d query tokens per sequence, window %d" % (args.q_len, args.window)
     elif args.op == "append":
@@ -294,8 +302,8 @@ def run_ours(args, world, rank, local):
         slots = torch.arange(w.B, dtype=torch.int32, device=dev) * w.block_size
         nbytes = 2 * 2 * k_new.numel() * k_new.element_size() + 4 * w.B
 
-        def step():
-            pgd.paged_kv_append(pool, k_new, v_new, slots, stream=stream)
+        def step(s=None):
+            pgd.paged_kv_append(pool, k_new, v_new, slots, stream=s or stream)
 
         op_note = "append: one new token per sequence (read + write of K and V rows)"
 
@@ -327,13 +335,30 @@ def run_ours(args, world, rank, local):
             if n % 64 == 0:
                 torch.cuda.synchronize()
         torch.cuda.synchronize()
+        graph = None
+        if args.launch == "graph":
+            # the K timed steps as one CUDA graph (as a serving loop replays its
+            # decode step); replayed once untimed first
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(stream)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(cap):
+                with torch.cuda.graph(graph, stream=cap):
+                    for _ in range(args.steps):
+                        step(cap)
+            stream.wait_stream(cap)
+            graph.replay()
+            torch.cuda.synchronize()
         barrier(world)
         torch.cuda.synchronize()
         ev0 = torch.cuda.Event(enable_timing=True)
         ev1 = torch.cuda.Event(enable_timing=True)
         ev0.record(stream)
-        for _ in range(args.steps):
-            step()
+        if graph is not None:
+            graph.replay()
+        else:
+            for _ in range(args.steps):
+                step()
         ev1.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -354,7 +379,7 @@ def run_ours(args, world, rank, local):
                 "ms_per_step": round(t_ms, 5), "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
                 "config": {"workload": describe(w), "op": op_note,
-                           "algorithmic_bytes_per_step": nbytes},
+                           "launch": launch_note(args), "algorithmic_bytes_per_step": nbytes},
                 "pct_of_peak": round(100 * gbs / world / peak, 2),
                 "peak_source": "%s (%.0f GB/s)" % (peak_src, peak),
                 "clocks": clk.summary()}), flush=True)
@@ -405,6 +430,7 @@ def run_ours(args, world, rank, local):
         "config": {"workload": describe(w), "parallelism": "replicas x%d" % world,
                    "l2": "no flush: each step streams %.0f MB of K/V, above the 126 MB L2"
                          % (nbytes / 1e6),
+                   "launch": launch_note(args),
                    "algorithmic_bytes_per_step": nbytes},
         "pct_of_peak": round(100 * per_gpu / peak, 2),
         "pct_of_nominal_8tbs": round(100 * per_gpu / NOMINAL_HBM_GBS, 2),
@@ -412,12 +438,12 @@ def run_ours(args, world, rank, local):
         "tokens_per_s_per_layer": round(world * w.B / (t_ms * 1e-3), 1),
         "roofline": {"bound": "hbm", "achieved": round(per_gpu, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(per_gpu / peak, 4), "traffic": ncu_traffic(args.config),
-                     "note": "bf16 steps are one kernel launch (split-KV merge fused), so "
-                             "achieved = algorithmic bytes / event-timed step"},
+                     "note": "bf16 and 8-bit steps are one kernel launch (split-KV merge "
+                             "fused), so achieved = algorithmic bytes / event-timed step"},
         "e2e": {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * (1 if w.dtype == "bf16" else 2),
+        "gpu_launches": args.steps * (2 if w.dtype == "f32" else 1),
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
@@ -441,6 +467,9 @@ def main():
                          "window), append (KV write path)")
     ap.add_argument("--q-len", type=int, default=4)
     ap.add_argument("--window", type=int, default=0)
+    ap.add_argument("--launch", default="graph", choices=["graph", "stream"],
+                    help="timed steps replayed as one CUDA graph (default) or launched one "
+                         "by one from Python")
     ap.add_argument("--profile", action="store_true",
                     help="only W + K step launches (for ncu); prints no bench line")
     args = ap.parse_args()
