@@ -66,7 +66,7 @@ bool encode_pool_map(CUtensorMap* map, const void* base, int64_t num_blocks, int
     const int row_elems = 128 / elt;                        // elements in a 128-byte row
     const int rows_per_head = d * elt / 128;                // 128-byte rows of one head
     const cuuint64_t row_bytes = (cuuint64_t)hkv * d * elt;  // one slot, all heads
-    const int tile = 128 / hg;
+    const int tile = (fp8 ? 256 : 128) / hg;  // tokens per tile of the decode kernel
     cuuint64_t dims[4] = {(cuuint64_t)row_elems, (cuuint64_t)bs,
                           (cuuint64_t)hkv * rows_per_head, (cuuint64_t)num_blocks};
     cuuint64_t strides[3] = {row_bytes, 128, row_bytes * bs};
@@ -291,7 +291,7 @@ int paged_gqa_decode_ex(pgd_pool_t pool, const void* q, int B, int q_len, int Hq
     a.auto_parts = num_splits == 0;
     a.hg = hg;
     a.units = p.hkv / hg;
-    a.tile_tokens = p.dtype != PGD_F32 ? 128 / hg : kSimpleTileTokens;
+    a.tile_tokens = p.dtype == PGD_F32 ? kSimpleTileTokens : (p.dtype == PGD_FP8_E4M3 ? 256 : 128) / hg;
     a.err = p.err;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     a.counters = reinterpret_cast<int*>(ws + wl.counters_off);

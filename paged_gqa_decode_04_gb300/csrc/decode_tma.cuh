@@ -201,10 +201,15 @@ struct Cfg {
     // 128-byte rows of a head in a page box: D/64 for bf16, 1 for 8-bit D = 128
     static constexpr int HALVES = FP8 ? D / 128 : D / 64;
     static constexpr int HH = HG * HALVES;    // 128-byte head rows per token in a tile
-    static constexpr int T = 128 / HG;        // tokens per tile
+    // tokens per tile: 128 token-heads per stage tensor (16 KB of 8-bit rows
+    // would leave the consumers' per-tile work too thin: 256 there)
+    static constexpr int T = (FP8 ? 256 : 128) / HG;
     static constexpr int NC = HG * MT * TG;   // consumer warps
     static constexpr int THREADS = (NC + 1) * 32;
     static constexpr int TW = T / TG;         // tokens per consumer warp per tile
+    // a warp's slice is processed in chunks of CH tokens (8-bit pages: at
+    // most 32, which bounds the score registers)
+    static constexpr int CH = (FP8 && TW > 32) ? 32 : TW;
     static constexpr int TENSOR_BYTES = HH * T * 128;   // K (or V) bytes of a stage
     static constexpr int STAGE_BYTES = 2 * TENSOR_BYTES;
     static constexpr int ROWS = ROWS16 ? 16 : 8;
@@ -218,6 +223,7 @@ struct Cfg {
     static_assert(!FP8 || D == 128, "8-bit pages: head_dim 128");
     static_assert(STAGES >= 2, "pipeline needs at least two stages");
     static_assert(TW % 16 == 0, "a warp's token slice must be whole k16 steps");
+    static_assert(TW % CH == 0 && CH % 16 == 0, "chunks must split the slice in k16 steps");
     static_assert(THREADS <= 288, "at most 8 consumer warps");
 };
 
@@ -633,172 +639,176 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
 
         if (active) {
-            // ---- S = q K^T over this warp's TW tokens
-            float sc[C::TW / 8][4];
+#pragma unroll 1
+            for (int c0 = tw0; c0 < tw0 + C::TW; c0 += C::CH) {  // CH-token chunks of my slice
+                if (c0 >= n_valid || c0 + C::CH <= v_lo) continue;
+                // ---- S = q K^T over the chunk's CH tokens
+                float sc[C::CH / 8][4];
 #pragma unroll
-            for (int j = 0; j < C::TW / 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-            if constexpr (C::FP8) {
-                // lane (gid, tig) needs bytes 16 ks + 4 tig .. +3 of token row
-                // tw0 + 8 j + gid, widened to the two f16 B registers: one
-                // ldmatrix.x4 brings them for n-tiles (jp, jp + 1) x k-steps
-                // (ks, ks + 1)
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ks += 2) {
-#pragma unroll
-                    for (int jp = 0; jp < C::TW / 8; jp += 2) {
-                        const int tok = tw0 + (jp + (lm_mi & 1)) * 8 + lm_i;
-                        const int kc = ks + (lm_mi >> 1);
-                        uint32_t w[4];
-                        ldsm_x4(k_u + row_off(tok, 0) + ((kc ^ lm_i) << 4), w[0], w[1], w[2],
-                                w[3]);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            mma_f16(sc[jp + (q & 1)], qa[ks + (q >> 1)],
-                                    e4m3x2_to_f16x2((uint16_t)(w[q] & 0xffffu)),
-                                    e4m3x2_to_f16x2((uint16_t)(w[q] >> 16)));
-                        }
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const int h = ks / 4;
-                    const int kc = (ks % 4) * 2 + (lm_mi & 1);
-#pragma unroll
-                    for (int np = 0; np < C::TW / 16; ++np) {
-                        const int tok = tw0 + np * 16 + (lm_mi >> 1) * 8 + lm_i;
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4(k_u + row_off(tok, h) + ((kc ^ lm_i) << 4), b0, b1, b2, b3);
-                        mma_bf16(sc[2 * np], qa[ks], b0, b1);
-                        mma_bf16(sc[2 * np + 1], qa[ks], b2, b3);
-                    }
-                }
-            }
-            // ---- mask (causal / window, per row), scale to base-2 units, running max
-            const int hi0 = dsc.L - a.q_len + qi0 + 1 - dsc.tok0;   // tile-local bounds
-            const int hi1 = dsc.L - a.q_len + qi1 + 1 - dsc.tok0;
-            const int lo0 = a.window > 0 ? hi0 - a.window : INT_MIN;
-            const int lo1 = a.window > 0 ? hi1 - a.window : INT_MIN;
-            float mx0 = -INFINITY, mx1 = -INFINITY;
-            // every row sees all of this warp's tokens (the usual case): no mask
-            const bool full = tw0 + C::TW <= dsc.L - a.q_len + 1 - dsc.tok0 &&
-                              (a.window == 0 || tw0 >= dsc.L - a.window - dsc.tok0);
-            if (full) {
-#pragma unroll
-                for (int j = 0; j < C::TW / 8; ++j) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        sc[j][e] *= s_mul;
-                        sc[j][2 + e] *= s_mul;
-                        mx0 = fmaxf(mx0, sc[j][e]);
-                        mx1 = fmaxf(mx1, sc[j][2 + e]);
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < C::TW / 8; ++j) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int tok = tw0 + j * 8 + tig * 2 + e;
-                        const bool v0 = tok < hi0 && tok >= lo0;
-                        const bool v1 = tok < hi1 && tok >= lo1;
-                        sc[j][e] = v0 ? sc[j][e] * s_mul : -INFINITY;
-                        sc[j][2 + e] = v1 ? sc[j][2 + e] * s_mul : -INFINITY;
-                        mx0 = fmaxf(mx0, sc[j][e]);
-                        mx1 = fmaxf(mx1, sc[j][2 + e]);
-                    }
-                }
-            }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            if (C::ROWS16) {
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            }
-            const float mn0 = fmaxf(m0, mx0);
-            const float mn1 = C::ROWS16 ? fmaxf(m1, mx1) : 0.f;
-            const float base0 = mn0 == -INFINITY ? 0.f : mn0;
-            const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-            const float alpha0 = fast_exp2(m0 - base0);
-            const float alpha1 = C::ROWS16 ? fast_exp2(m1 - base1) : 1.f;
-            m0 = mn0;
-            if (C::ROWS16) m1 = mn1;
-            float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-            for (int j = 0; j < C::TW / 8; ++j) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    sc[j][e] = fast_exp2(sc[j][e] - base0);
-                    ps0 += sc[j][e];
-                    if (C::ROWS16) {
-                        sc[j][2 + e] = fast_exp2(sc[j][2 + e] - base1);
-                        ps1 += sc[j][2 + e];
-                    } else {
-                        sc[j][2 + e] = 0.f;
-                    }
-                }
-            }
-            l0 = l0 * alpha0 + ps0;
-            if (C::ROWS16) l1 = l1 * alpha1 + ps1;
-            if (__any_sync(0xffffffffu, alpha0 != 1.f || alpha1 != 1.f)) {
-#pragma unroll
-                for (int n = 0; n < D / 8; ++n) {
-                    o[n][0] *= alpha0;
-                    o[n][1] *= alpha0;
-                    o[n][2] *= alpha1;
-                    o[n][3] *= alpha1;
-                }
-            }
-            // ---- O += P V
-#pragma unroll
-            for (int kk = 0; kk < C::TW / 16; ++kk) {
+                for (int j = 0; j < C::CH / 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
                 if constexpr (C::FP8) {
-                    // 8-bit V straight from the stage: a transposed 16-bit ldmatrix
-                    // gives lane (gid, tig) tokens (2 tig, 2 tig + 1) x bytes
-                    // d = (2 gid, 2 gid + 1) of a 16-byte chunk; one byte permute
-                    // puts the two tokens of d = 2 gid in the low half and those of
-                    // 2 gid + 1 in the high half, each an e4m3x2 B operand.  n-tile
-                    // 2 c + par then holds d = 16 c + 2 j + par for B column j, so
-                    // the output columns come out permuted (undone where O is stored).
-                    uint32_t pa[4];
-                    pa[0] = pack_f16(sc[2 * kk][0], sc[2 * kk][1]);
-                    pa[1] = pack_f16(sc[2 * kk][2], sc[2 * kk][3]);
-                    pa[2] = pack_f16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-                    pa[3] = pack_f16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
-                    const int tok = tw0 + kk * 16 + (lm_mi & 1) * 8 + lm_i;
+                    // lane (gid, tig) needs bytes 16 ks + 4 tig .. +3 of token row
+                    // c0 + 8 j + gid, widened to the two f16 B registers: one
+                    // ldmatrix.x4 brings them for n-tiles (jp, jp + 1) x k-steps
+                    // (ks, ks + 1)
 #pragma unroll
-                    for (int c2 = 0; c2 < D / 32; ++c2) {
-                        const int vc = c2 * 2 + (lm_mi >> 1);
-                        uint32_t r[4];
-                        ldsm_x4_t(v_u + row_off(tok, 0) + ((vc ^ lm_i) << 4), r[0], r[1], r[2],
-                                  r[3]);
+                    for (int ks = 0; ks < D / 16; ks += 2) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) r[q] = __byte_perm(r[q], 0u, 0x3120);
+                        for (int jp = 0; jp < C::CH / 8; jp += 2) {
+                            const int tok = c0 + (jp + (lm_mi & 1)) * 8 + lm_i;
+                            const int kc = ks + (lm_mi >> 1);
+                            uint32_t w[4];
+                            ldsm_x4(k_u + row_off(tok, 0) + ((kc ^ lm_i) << 4), w[0], w[1], w[2],
+                                    w[3]);
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {  // chunk 2 c2 + h: r[2h] tokens 0-7, r[2h+1] 8-15
-                            const int n = 4 * c2 + 2 * h;
-                            mma_f16(o[n], pa, e4m3x2_to_f16x2((uint16_t)(r[2 * h] & 0xffffu)),
-                                    e4m3x2_to_f16x2((uint16_t)(r[2 * h + 1] & 0xffffu)));
-                            mma_f16(o[n + 1], pa, e4m3x2_to_f16x2((uint16_t)(r[2 * h] >> 16)),
-                                    e4m3x2_to_f16x2((uint16_t)(r[2 * h + 1] >> 16)));
+                            for (int q = 0; q < 4; ++q) {
+                                mma_f16(sc[jp + (q & 1)], qa[ks + (q >> 1)],
+                                        e4m3x2_to_f16x2((uint16_t)(w[q] & 0xffffu)),
+                                        e4m3x2_to_f16x2((uint16_t)(w[q] >> 16)));
+                            }
                         }
                     }
-                    continue;
-                }
-                uint32_t pa[4];
-                pa[0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
-                pa[1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
-                pa[2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-                pa[3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
-                const int tok = tw0 + kk * 16 + (lm_mi & 1) * 8 + lm_i;
+                } else {
 #pragma unroll
-                for (int dp = 0; dp < D / 16; ++dp) {
-                    const int h = dp / 4;
-                    const int vc = (dp % 4) * 2 + (lm_mi >> 1);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(v_u + row_off(tok, h) + ((vc ^ lm_i) << 4), b0, b1, b2, b3);
-                    mma_bf16(o[2 * dp], pa, b0, b1);
-                    mma_bf16(o[2 * dp + 1], pa, b2, b3);
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const int h = ks / 4;
+                        const int kc = (ks % 4) * 2 + (lm_mi & 1);
+#pragma unroll
+                        for (int np = 0; np < C::CH / 16; ++np) {
+                            const int tok = c0 + np * 16 + (lm_mi >> 1) * 8 + lm_i;
+                            uint32_t b0, b1, b2, b3;
+                            ldsm_x4(k_u + row_off(tok, h) + ((kc ^ lm_i) << 4), b0, b1, b2, b3);
+                            mma_bf16(sc[2 * np], qa[ks], b0, b1);
+                            mma_bf16(sc[2 * np + 1], qa[ks], b2, b3);
+                        }
+                    }
+                }
+                // ---- mask (causal / window, per row), scale to base-2 units, running max
+                const int hi0 = dsc.L - a.q_len + qi0 + 1 - dsc.tok0;   // tile-local bounds
+                const int hi1 = dsc.L - a.q_len + qi1 + 1 - dsc.tok0;
+                const int lo0 = a.window > 0 ? hi0 - a.window : INT_MIN;
+                const int lo1 = a.window > 0 ? hi1 - a.window : INT_MIN;
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+                // every row sees all of this warp's tokens (the usual case): no mask
+                const bool full = c0 + C::CH <= dsc.L - a.q_len + 1 - dsc.tok0 &&
+                                  (a.window == 0 || c0 >= dsc.L - a.window - dsc.tok0);
+                if (full) {
+#pragma unroll
+                    for (int j = 0; j < C::CH / 8; ++j) {
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            sc[j][e] *= s_mul;
+                            sc[j][2 + e] *= s_mul;
+                            mx0 = fmaxf(mx0, sc[j][e]);
+                            mx1 = fmaxf(mx1, sc[j][2 + e]);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < C::CH / 8; ++j) {
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int tok = c0 + j * 8 + tig * 2 + e;
+                            const bool v0 = tok < hi0 && tok >= lo0;
+                            const bool v1 = tok < hi1 && tok >= lo1;
+                            sc[j][e] = v0 ? sc[j][e] * s_mul : -INFINITY;
+                            sc[j][2 + e] = v1 ? sc[j][2 + e] * s_mul : -INFINITY;
+                            mx0 = fmaxf(mx0, sc[j][e]);
+                            mx1 = fmaxf(mx1, sc[j][2 + e]);
+                        }
+                    }
+                }
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                if (C::ROWS16) {
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                }
+                const float mn0 = fmaxf(m0, mx0);
+                const float mn1 = C::ROWS16 ? fmaxf(m1, mx1) : 0.f;
+                const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+                const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+                const float alpha0 = fast_exp2(m0 - base0);
+                const float alpha1 = C::ROWS16 ? fast_exp2(m1 - base1) : 1.f;
+                m0 = mn0;
+                if (C::ROWS16) m1 = mn1;
+                float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+                for (int j = 0; j < C::CH / 8; ++j) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        sc[j][e] = fast_exp2(sc[j][e] - base0);
+                        ps0 += sc[j][e];
+                        if (C::ROWS16) {
+                            sc[j][2 + e] = fast_exp2(sc[j][2 + e] - base1);
+                            ps1 += sc[j][2 + e];
+                        } else {
+                            sc[j][2 + e] = 0.f;
+                        }
+                    }
+                }
+                l0 = l0 * alpha0 + ps0;
+                if (C::ROWS16) l1 = l1 * alpha1 + ps1;
+                if (__any_sync(0xffffffffu, alpha0 != 1.f || alpha1 != 1.f)) {
+#pragma unroll
+                    for (int n = 0; n < D / 8; ++n) {
+                        o[n][0] *= alpha0;
+                        o[n][1] *= alpha0;
+                        o[n][2] *= alpha1;
+                        o[n][3] *= alpha1;
+                    }
+                }
+                // ---- O += P V
+#pragma unroll
+                for (int kk = 0; kk < C::CH / 16; ++kk) {
+                    if constexpr (C::FP8) {
+                        // 8-bit V straight from the stage: a transposed 16-bit ldmatrix
+                        // gives lane (gid, tig) tokens (2 tig, 2 tig + 1) x bytes
+                        // d = (2 gid, 2 gid + 1) of a 16-byte chunk; one byte permute
+                        // puts the two tokens of d = 2 gid in the low half and those of
+                        // 2 gid + 1 in the high half, each an e4m3x2 B operand.  n-tile
+                        // 2 c + par then holds d = 16 c + 2 j + par for B column j, so
+                        // the output columns come out permuted (undone where O is stored).
+                        uint32_t pa[4];
+                        pa[0] = pack_f16(sc[2 * kk][0], sc[2 * kk][1]);
+                        pa[1] = pack_f16(sc[2 * kk][2], sc[2 * kk][3]);
+                        pa[2] = pack_f16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+                        pa[3] = pack_f16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+                        const int tok = c0 + kk * 16 + (lm_mi & 1) * 8 + lm_i;
+#pragma unroll
+                        for (int c2 = 0; c2 < D / 32; ++c2) {
+                            const int vc = c2 * 2 + (lm_mi >> 1);
+                            uint32_t r[4];
+                            ldsm_x4_t(v_u + row_off(tok, 0) + ((vc ^ lm_i) << 4), r[0], r[1], r[2],
+                                      r[3]);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) r[q] = __byte_perm(r[q], 0u, 0x3120);
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {  // chunk 2 c2 + h: r[2h] tokens 0-7, r[2h+1] 8-15
+                                const int n = 4 * c2 + 2 * h;
+                                mma_f16(o[n], pa, e4m3x2_to_f16x2((uint16_t)(r[2 * h] & 0xffffu)),
+                                        e4m3x2_to_f16x2((uint16_t)(r[2 * h + 1] & 0xffffu)));
+                                mma_f16(o[n + 1], pa, e4m3x2_to_f16x2((uint16_t)(r[2 * h] >> 16)),
+                                        e4m3x2_to_f16x2((uint16_t)(r[2 * h + 1] >> 16)));
+                            }
+                        }
+                        continue;
+                    }
+                    uint32_t pa[4];
+                    pa[0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
+                    pa[1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
+                    pa[2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+                    pa[3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+                    const int tok = c0 + kk * 16 + (lm_mi & 1) * 8 + lm_i;
+#pragma unroll
+                    for (int dp = 0; dp < D / 16; ++dp) {
+                        const int h = dp / 4;
+                        const int vc = (dp % 4) * 2 + (lm_mi >> 1);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(v_u + row_off(tok, h) + ((vc ^ lm_i) << 4), b0, b1, b2, b3);
+                        mma_bf16(o[2 * dp], pa, b0, b1);
+                        mma_bf16(o[2 * dp + 1], pa, b2, b3);
+                    }
                 }
             }
         }
@@ -1020,16 +1030,17 @@ cudaError_t launch_cfg(const DecodeArgs& a, const CUtensorMap& mk, const CUtenso
     return cudaGetLastError();
 }
 
-// Token groups per tile for (HG, MT): up to 8 consumer warps, >= 16 tokens each.
-constexpr int token_groups(int hg, int mt) {
-    const int by_tokens = (128 / hg) / 16;
+// Token groups per tile of t tokens for (HG, MT): up to 8 consumer warps, >= 16
+// tokens each.
+constexpr int token_groups(int t, int hg, int mt) {
+    const int by_tokens = t / 16;
     const int by_warps = 8 / (hg * mt) > 0 ? 8 / (hg * mt) : 1;
     return by_tokens < by_warps ? by_tokens : by_warps;
 }
 
 template <int D, int HG, int MT, bool R16, bool FP8>
 cudaError_t launch_hg(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
-    constexpr int TG = token_groups(HG, MT);
+    constexpr int TG = token_groups((FP8 ? 256 : 128) / HG, HG, MT);
     const int idx = HG == 1 ? 0 : HG == 2 ? 1 : HG == 4 ? 2 : 3;
     return launch_cfg<Cfg<D, HG, MT, TG, R16, FP8>>(a, p.tmap_k[idx], p.tmap_v[idx], s);
 }
