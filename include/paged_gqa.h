@@ -121,8 +121,9 @@ int paged_kv_pool_destroy(pgd_pool_t pool);
  * Workspace bytes paged_gqa_decode needs for B sequences, Hq query heads and
  * `num_splits` (same meaning as in paged_gqa_decode; 0 = automatic).  Written
  * to *bytes.  The workspace holds per-split partial results, the tile prefix
- * table and one counter per split run.  It must be zero-filled before its
- * first use; every call that completes leaves it zero-filled again, so a
+ * table and one counter word per split run.  It must be zero-filled before
+ * its first use; every call that completes leaves it ready for the next one
+ * (each run's count back at zero; a flag bit beside it alternates), so a
  * workspace can be reused call after call.  After a call that latched
  * PGD_ERR_TIMEOUT, zero it again.
  */

@@ -127,7 +127,7 @@ def paged_gqa_auto_splits(pool):
 def alloc_workspace(pool, B, Hq, num_splits=0):
     """A zero-filled workspace tensor of the right size on the pool's device.
 
-    Reusable across calls: every completed call leaves it zero-filled."""
+    Reusable across calls: every completed call leaves it ready for the next."""
     nbytes = paged_gqa_workspace_size(pool, B, Hq, num_splits)
     return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=pool.k_pool.device)
 

@@ -105,6 +105,34 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     return true;
 }
 
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(int* p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// A split run's counter word: pieces arrived in the low bits, and a flag bit
+// that the last arriver flips as it sets the count back to zero.
+constexpr int kRunFlagShift = 30;
+constexpr int kRunCountMask = (1 << kRunFlagShift) - 1;
+
+// Bounded wait until the flag bit of the run word at p differs from `old`
+// (acquire, GPU scope).  Only used under a cooperative launch, where the CTA
+// that flips it is resident; false after kWaitNs.
+__device__ __forceinline__ bool wait_flip(const int* p, int old) {
+    if (((ld_acquire(p) >> kRunFlagShift) & 1) != old) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        __nanosleep(32);
+        if (((ld_acquire(p) >> kRunFlagShift) & 1) != old) return true;
+        if (global_ns() - t0 > kWaitNs) return false;
+    }
+}
+
 // L2 policy for data read exactly once per call (the K/V pages).
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
@@ -190,7 +218,7 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
 }
 
 // ----------------------------------------------------------------- configuration
-template <int D_, int HG_, int MT_, int TG_, bool ROWS16_, bool FP8_ = false>
+template <int D_, int HG_, int MT_, int TG_, bool ROWS16_, bool FP8_ = false, bool SHARE_ = false>
 struct Cfg {
     static constexpr int D = D_;
     static constexpr int HG = HG_;            // KV heads per unit of work
@@ -198,6 +226,9 @@ struct Cfg {
     static constexpr int TG = TG_;            // token groups per tile
     static constexpr bool ROWS16 = ROWS16_;   // rows 8..15 of an m-tile in use
     static constexpr bool FP8 = FP8_;         // 8-bit (e4m3) K/V pages, f16 products
+    // cooperative launch: a split run with a large merge is merged by all its
+    // pieces' warps together
+    static constexpr bool SHARE = SHARE_;
     // 128-byte rows of a head in a page box: D/64 for bf16, 1 for 8-bit D = 128
     static constexpr int HALVES = FP8 ? D / 128 : D / 64;
     static constexpr int HH = HG * HALVES;    // 128-byte head rows per token in a tile
@@ -234,6 +265,8 @@ struct MergeJob {
     int npieces;
     int first_is_tail;
     int b, kvh;     // b < 0: no job
+    int k;          // shared merge: this warp's piece of the run; -1: merge all rows
+    int flag;       // shared merge: the run's flag before this piece arrived
 };
 
 // What the producer tells the consumers about the tile in a stage.
@@ -253,9 +286,8 @@ __device__ __forceinline__ int64_t qrow_offset(const DecodeArgs& a, int b, int k
     return (((int64_t)b * a.q_len + r / G) * a.hq + (int64_t)kvh * G + r % G) * a.d;
 }
 
-// Merge the pieces of a split run for the query rows one consumer warp owns
-// (m-tile `mt` of head `hgi` of the group, KV head `kvh` of sequence `b`) and
-// write them to `out`.  Log-sum-exp combination in base 2: with lse_k = m_k +
+// Merge the pieces of a split run for query rows [r_lo, r_hi) of head `hgi` of
+// the group (KV head `kvh` of sequence `b`) and write them to `out`.  Log-sum-exp combination in base 2: with lse_k = m_k +
 // log2 l_k and o_k the normalised partial of piece k,
 //     out = sum_k 2^(lse_k - M) o_k / sum_k 2^(lse_k - M),  M = max_k lse_k,
 // accumulated online.  The lanes cover a row's columns with float4 reads, and
@@ -266,6 +298,7 @@ __device__ __forceinline__ int64_t qrow_offset(const DecodeArgs& a, int b, int k
 // flight.  Runs after the tile loop, when the loop's accumulators are dead.
 constexpr int kPieceBatch = 4;
 constexpr int kMergeRows = 4;
+static_assert(kShareMinLoads == 6 * kMergeRows * kPieceBatch, "six batches of merge loads");
 
 __device__ __forceinline__ void lse_fold(float& M, float& W, float4& acc, float e, float w,
                                          float4 v) {
@@ -286,7 +319,7 @@ __device__ __forceinline__ void lse_fold(float& M, float& W, float4& acc, float 
 template <class C, bool PHASED>
 __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int64_t t0, int64_t N, int64_t P,
                                           int64_t c0, int npieces, bool first_is_tail, int hgi,
-                                          int mt, int b, int kvh) {
+                                          int r_lo, int r_hi, int b, int kvh) {
     constexpr int D = C::D;
     constexpr int CPR = D / 4;             // float4 chunks per row
     constexpr int RPP = 32 / CPR;          // rows per pass
@@ -295,8 +328,6 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int64_t t0, in
     const int lane = threadIdx.x % 32;
     const int rows = a.q_len * a.group;    // query rows per KV head
     const int piece_rows = C::HG * rows;
-    const int r_lo = mt * 16;
-    const int r_hi = min(rows, r_lo + C::ROWS);
     const int col = (lane % CPR) * 4;
     constexpr int npe = PHASED ? 1 : RU;  // row passes per round
     constexpr int rep = RU / npe;          // piece phases per row pass
@@ -974,9 +1005,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     pl[prow1] = seg_bad ? 0.f : (lt1 > 0.f ? m1 + fast_log2(lt1) : -INFINITY);
             }
         }
-        // Publish the partial, count it; the warp that brings the run's count
-        // to its number of pieces merges them (log-sum-exp) and resets the
-        // counter, so no second kernel and no waiting.
+        // Publish the partial and count it; the warp that brings the count to
+        // the number of pieces sets it back to zero and flips the run's flag
+        // bit.  Shared merge (cooperative launch, a merge of more than six
+        // batches of loads whose rows split): every piece's warp, after its tile
+        // loop, waits for the flip and merges a share of the rows.  Otherwise
+        // the last warp merges all rows.  No second kernel, no atomics at the
+        // end.
         __threadfence();
         __syncwarp();
         const int64_t t0 = dsc.run_start;
@@ -988,45 +1023,111 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int npieces = P > N ? dsc.n_b : (int)(span_owner(t0 + dsc.n_b - 1, N, P) - c0 + 1);
         const bool first_is_tail = P <= N && span_begin(c0, N, P) < t0;
         if (lane == 0) {
-            int* ctr = a.counters + ((int64_t)dsc.b * a.hkv + kvh) * C::MT + mt;
-            if (atomicAdd(ctr, 1) == npieces - 1) {
-                atomicExch(ctr, 0);
-                // one piece per partial slot and CTA, so one job per slot
-                jobs[warp][(dsc.flags & kSegSlot1) ? 1 : 0] =
-                    MergeJob{t0, c0, npieces, first_is_tail ? 1 : 0, dsc.b, kvh};
+            int* word = a.counters + ((int64_t)dsc.b * a.hkv + kvh) * C::MT + mt;
+            const int js = (dsc.flags & kSegSlot1) ? 1 : 0;  // one piece per partial slot and CTA
+            const int old = atomicAdd(word, 1);
+            const int flag = (old >> kRunFlagShift) & 1;  // cannot flip before I arrive
+            const bool last = (old & kRunCountMask) == npieces - 1;
+            if constexpr (C::SHARE) {
+                const int nr = min(rows - mt * 16, C::ROWS);
+                constexpr int RPP = 32 / (D / 4);          // rows per merge pass
+                const bool shared = min(npieces, nr) >= 2 &&
+                                    (nr + RPP - 1) / RPP * npieces > kShareMinLoads;
+                if (last) {
+                    if (shared) {
+                        __threadfence();  // every piece's partial is visible before the flip
+                        st_release(word, (flag ^ 1) << kRunFlagShift);
+                    } else {
+                        *word = (flag ^ 1) << kRunFlagShift;  // nobody waits on this flip
+                    }
+                }
+                if (shared) {
+                    const int k = P > N ? (int)(ss.r0 - t0) : (int)(blockIdx.x - c0);
+                    jobs[warp][js] =
+                        MergeJob{t0, c0, npieces, first_is_tail ? 1 : 0, dsc.b, kvh, k, flag};
+                } else if (last) {
+                    jobs[warp][js] =
+                        MergeJob{t0, c0, npieces, first_is_tail ? 1 : 0, dsc.b, kvh, -1, 0};
+                }
+            } else if (last) {
+                *word = (flag ^ 1) << kRunFlagShift;
+                jobs[warp][js] =
+                    MergeJob{t0, c0, npieces, first_is_tail ? 1 : 0, dsc.b, kvh, -1, 0};
             }
         }
     }
-    // ---- merge the runs this warp completed
+    // ---- merge the split runs recorded above
     __syncwarp();
     if (aborted) return;
+    constexpr int RPP = 32 / (D / 4);  // rows per merge pass
+    const int r_mine = mt * 16, r_end = min(rows, r_mine + C::ROWS);
 #pragma unroll 1
     for (int j = 0; j < 2; ++j) {
         const MergeJob jb = jobs[warp][j];
         if (jb.b < 0) continue;
+        int m_lo = r_mine, m_hi = r_end;
+        if (C::SHARE && jb.k >= 0) {
+            // the first min(pieces, rows) pieces' warps each merge a share of
+            // the rows, once every piece is in
+            const int nr = r_end - r_mine;
+            const int nm = min(jb.npieces, nr);
+            if (jb.k >= nm) continue;
+            m_lo = r_mine + jb.k * nr / nm;
+            m_hi = r_mine + (jb.k + 1) * nr / nm;
+            int ok = 1;
+            if (lane == 0)
+                ok = wait_flip(a.counters + ((int64_t)jb.b * a.hkv + jb.kvh) * C::MT + mt,
+                               jb.flag) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) latch_error(a.err, PGD_ERR_TIMEOUT);
+                return;
+            }
+        }
         __threadfence();
-        constexpr int RPP = 32 / (D / 4);  // rows per merge pass
-        if (min(rows - mt * 16, C::ROWS) <= RPP)
+        if (m_hi - m_lo <= RPP)
             merge_pieces<C, true>(a, jb.t0, ss.n_total, ss.parts, jb.c0, jb.npieces,
-                                  jb.first_is_tail != 0, hgi, mt, jb.b, jb.kvh);
+                                  jb.first_is_tail != 0, hgi, m_lo, m_hi, jb.b, jb.kvh);
         else
             merge_pieces<C, false>(a, jb.t0, ss.n_total, ss.parts, jb.c0, jb.npieces,
-                                   jb.first_is_tail != 0, hgi, mt, jb.b, jb.kvh);
+                                   jb.first_is_tail != 0, hgi, m_lo, m_hi, jb.b, jb.kvh);
     }
 }
 
 template <class C>
 cudaError_t launch_cfg(const DecodeArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
-                       cudaStream_t s) {
+                       int num_sms, cudaStream_t s) {
     static bool attr_done = false;  // per instantiation; a repeated set is harmless
+    static int per_sm = 0;          // co-resident CTAs per SM
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(decode_tma_kernel<C>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_tma_kernel<C>,
+                                                          C::THREADS, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    decode_tma_kernel<C><<<a.num_parts, C::THREADS, C::SMEM_BYTES, s>>>(mk, mv, a);
+    if constexpr (C::SHARE) {
+        // the shared merge waits on other CTAs: only a grid resident at once,
+        // launched cooperatively
+        if (a.num_parts > per_sm * num_sms) return cudaErrorCooperativeLaunchTooLarge;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(a.num_parts);
+        cfg.blockDim = dim3(C::THREADS);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tma_kernel<C>, mk, mv, a);
+        if (e != cudaSuccess) return e;
+    } else {
+        decode_tma_kernel<C><<<a.num_parts, C::THREADS, C::SMEM_BYTES, s>>>(mk, mv, a);
+    }
     return cudaGetLastError();
 }
 
@@ -1038,37 +1139,40 @@ constexpr int token_groups(int t, int hg, int mt) {
     return by_tokens < by_warps ? by_tokens : by_warps;
 }
 
-template <int D, int HG, int MT, bool R16, bool FP8>
+template <int D, int HG, int MT, bool R16, bool FP8, bool SHARE>
 cudaError_t launch_hg(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
     constexpr int TG = token_groups((FP8 ? 256 : 128) / HG, HG, MT);
     const int idx = HG == 1 ? 0 : HG == 2 ? 1 : HG == 4 ? 2 : 3;
-    return launch_cfg<Cfg<D, HG, MT, TG, R16, FP8>>(a, p.tmap_k[idx], p.tmap_v[idx], s);
+    return launch_cfg<Cfg<D, HG, MT, TG, R16, FP8, SHARE>>(a, p.tmap_k[idx], p.tmap_v[idx],
+                                                          p.num_sms, s);
 }
 
-template <int D, int MT, bool R16, bool FP8>
+template <int D, int MT, bool R16, bool FP8, bool SHARE>
 cudaError_t launch_mt(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
     switch (a.hg) {
-        case 1: return launch_hg<D, 1, MT, R16, FP8>(a, p, s);
-        case 2: return launch_hg<D, 2, MT, R16, FP8>(a, p, s);
+        case 1: return launch_hg<D, 1, MT, R16, FP8, SHARE>(a, p, s);
+        case 2: return launch_hg<D, 2, MT, R16, FP8, SHARE>(a, p, s);
         case 4:
-            if constexpr (MT <= 2) return launch_hg<D, 4, MT, R16, FP8>(a, p, s);
+            if constexpr (MT <= 2) return launch_hg<D, 4, MT, R16, FP8, SHARE>(a, p, s);
             break;
         case 8:
-            if constexpr (MT == 1) return launch_hg<D, 8, MT, R16, FP8>(a, p, s);
+            if constexpr (MT == 1) return launch_hg<D, 8, MT, R16, FP8, SHARE>(a, p, s);
             break;
     }
     return cudaErrorInvalidValue;
 }
 
 // FP8: 8-bit (e4m3) K/V pages (head_dim 128 only).
-template <int D, bool FP8 = false>
+// SHARE: the shared-merge variant (cooperative launch); returns
+// cudaErrorCooperativeLaunchTooLarge when the grid cannot be resident at once.
+template <int D, bool FP8, bool SHARE>
 cudaError_t launch_tma_d(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
     const int rows = a.q_len * a.group;  // query rows per KV head
-    if (rows <= 8) return launch_mt<D, 1, false, FP8>(a, p, s);
-    if (rows <= 16) return launch_mt<D, 1, true, FP8>(a, p, s);
-    if (rows <= 32) return launch_mt<D, 2, true, FP8>(a, p, s);
-    if (rows <= 48) return launch_mt<D, 3, true, FP8>(a, p, s);
-    return launch_mt<D, 4, true, FP8>(a, p, s);
+    if (rows <= 8) return launch_mt<D, 1, false, FP8, SHARE>(a, p, s);
+    if (rows <= 16) return launch_mt<D, 1, true, FP8, SHARE>(a, p, s);
+    if (rows <= 32) return launch_mt<D, 2, true, FP8, SHARE>(a, p, s);
+    if (rows <= 48) return launch_mt<D, 3, true, FP8, SHARE>(a, p, s);
+    return launch_mt<D, 4, true, FP8, SHARE>(a, p, s);
 }
 
 }  // namespace tma

@@ -1,20 +1,34 @@
-// The TMA decode kernel instantiated for head_dim 128, and the dispatch on
-// head_dim (head_dim 64 lives in decode_tma_d64.cu).
+// The TMA decode kernel instantiated for head_dim 128 (bf16 pages), and the
+// dispatch on head_dim, page type and merge variant.  The other instantiations
+// live in their own translation units so that they compile in parallel.
 #include "decode_tma.cuh"
 
 namespace pgd {
 namespace tma {
-template cudaError_t launch_tma_d<128>(const DecodeArgs&, const Pool&, cudaStream_t);
-extern template cudaError_t launch_tma_d<64>(const DecodeArgs&, const Pool&, cudaStream_t);
-extern template cudaError_t launch_tma_d<128, true>(const DecodeArgs&, const Pool&, cudaStream_t);
+template cudaError_t launch_tma_d<128, false, false>(const DecodeArgs&, const Pool&, cudaStream_t);
+extern template cudaError_t launch_tma_d<128, false, true>(const DecodeArgs&, const Pool&,
+                                                           cudaStream_t);
+extern template cudaError_t launch_tma_d<64, false, false>(const DecodeArgs&, const Pool&,
+                                                           cudaStream_t);
+extern template cudaError_t launch_tma_d<128, true, false>(const DecodeArgs&, const Pool&,
+                                                           cudaStream_t);
+extern template cudaError_t launch_tma_d<128, true, true>(const DecodeArgs&, const Pool&,
+                                                          cudaStream_t);
 }  // namespace tma
 
 cudaError_t launch_decode_tma(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
     const int idx = a.hg == 1 ? 0 : a.hg == 2 ? 1 : a.hg == 4 ? 2 : 3;
     if (!p.tmap_ok[idx]) return cudaErrorInvalidValue;
-    if (p.dtype == PGD_FP8_E4M3) return tma::launch_tma_d<128, true>(a, p, s);
-    if (a.d == 64) return tma::launch_tma_d<64>(a, p, s);
-    return tma::launch_tma_d<128>(a, p, s);
+    const bool fp8 = p.dtype == PGD_FP8_E4M3;
+    if (a.share_merge && a.d == 128) {
+        const cudaError_t e = fp8 ? tma::launch_tma_d<128, true, true>(a, p, s)
+                                  : tma::launch_tma_d<128, false, true>(a, p, s);
+        if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+        cudaGetLastError();  // not resident at once: the last-arriver variant instead
+    }
+    if (fp8) return tma::launch_tma_d<128, true, false>(a, p, s);
+    if (a.d == 64) return tma::launch_tma_d<64, false, false>(a, p, s);
+    return tma::launch_tma_d<128, false, false>(a, p, s);
 }
 
 }  // namespace pgd

@@ -14,6 +14,11 @@ constexpr int kSimpleTileTokens = 64;
 
 // Largest query-head group the kernels handle (4 m16 row tiles).
 constexpr int kMaxGroup = 64;
+// A split run is merged by all its pieces' warps (shared merge, cooperative
+// launch) only when one warp would need more than this many float4 loads per
+// lane (six batches of 4 row passes x 4 pieces): below that, the waits and the
+// second merge per CTA cost more than they save (measured).
+constexpr int kShareMinLoads = 96;
 
 struct Pool {
     const void* k;
@@ -64,7 +69,10 @@ struct DecodeArgs {
     int tile_tokens;       // tokens per tile
     int* err;
     // workspace carve-up
-    int* counters;         // [B][Hkv][m-tiles] pieces finished per split run (kept zero between calls)
+    int* counters;         // [B][Hkv][m-tiles] per split run: pieces finished (zero between
+                           // calls) and a flag bit flipped when the last piece arrives
+    int share_merge;       // host's choice: launch the shared-merge kernel variant (merges
+                           // expected large); it falls back when the grid cannot be resident
     int64_t* tile_base;    // [B + 1] first flat tile of each sequence
     float* part_o;         // [num_parts][2][hg * group][d] normalised partial outputs
     float* part_lse;       // [num_parts][2][hg * group]    partial log2-sum-exp
