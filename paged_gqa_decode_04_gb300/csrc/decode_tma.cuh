@@ -55,7 +55,7 @@ namespace tma {
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
 // With automatic splits, use fewer spans than CTAs when the call has fewer than
 // this many tiles per CTA: tiny calls then split runs into fewer pieces.
-constexpr int kMinTilesPerCta = 4;
+constexpr int kMinTilesPerCta = 2;
 constexpr int kSmemBudget = 227 * 1024;
 
 // ----------------------------------------------------------------- PTX wrappers
