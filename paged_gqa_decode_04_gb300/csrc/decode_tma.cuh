@@ -1,6 +1,7 @@
-// bfloat16 paged GQA decode: TMA page staging, mbarrier pipeline, tensor-core
-// tile products, online softmax.  sm_103a.  Included by decode_tma_d64.cu and
-// decode_tma_d128.cu, which instantiate it for one head dimension each.
+// Paged GQA decode over bfloat16 or 8-bit (e4m3) K/V pages: TMA page staging,
+// mbarrier pipeline, tensor-core tile products, online softmax, fused split
+// merge.  sm_103a.  Included by the decode_tma_*.cu files, each of which
+// instantiates one (head dimension, page type, merge variant).
 //
 // Decode attention reads every cached K/V byte once and does G multiply-adds
 // per element, far below the tensor cores' ridge point, so the kernel is built
@@ -21,7 +22,8 @@
 // Structure of a CTA (one per span of the tile sequence, see partition.cuh;
 // the grid is one CTA per SM):
 //   * warp NC (producer): walks the span's tiles (T = 128 / HG tokens of one
-//     (sequence, head group)), keeps a 32-entry window of block ids in
+//     (sequence, head group); 256 / HG for 8-bit pages, so that a stage holds
+//     64 KB either way), keeps a 32-entry window of block ids in
 //     registers (plus the next window in flight), and issues one
 //     cp.async.bulk.tensor per page for K and one for V into a ring of stages
 //     guarded by "full" (transaction bytes) and "empty" mbarriers.  Reading the
@@ -35,8 +37,14 @@
 //     accumulators in base-2 units.  When TG > 1 the token groups of a head
 //     combine through shared memory at the end of a piece; the tg == 0 warps
 //     then write the output rows (whole run) or a normalised partial and its
-//     log2-sum-exp (split run); the warp that completes a split run's count
-//     merges its pieces.
+//     log2-sum-exp (split run).  After the tile loop a split run is merged by
+//     the warp whose arrival completed it, or, in the shared-merge variant
+//     (cooperative launch, long runs), by all its pieces' warps, each taking
+//     a share of the rows.
+//   * 8-bit pages: K and V fragments come straight from the stage by
+//     ldmatrix and are widened to f16 in registers (cvt.rn.f16x2.e4m3x2);
+//     both products run on f16 mma.sync, the per-head scales fold into the
+//     logit multiplier and the epilogue.
 //
 // Every wait is bounded (kWaitNs); a wait that gives up latches
 // PGD_ERR_TIMEOUT, marks the CTA aborted and lets every warp leave.
