@@ -296,13 +296,17 @@ int paged_gqa_decode_ex(pgd_pool_t pool, const void* q, int B, int q_len, int Hq
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     a.counters = reinterpret_cast<int*>(ws + wl.counters_off);
     {
-        // Shared merge when a split run's merge is expected to be large: about
+        // Merge variant from the expected size of a split run's merge: about
         // parts / runs + 1 pieces per run, times the row passes of one warp.
         const int runs = B * a.units;
         const int nr = rows < 16 ? rows : 16;          // rows of one warp's m-tile
         const int passes = (nr * p.d + 127) / 128;     // 128 / D rows per merge pass
-        a.share_merge = p.dtype != PGD_F32 && p.d == 128 && nr >= 2 &&
-                        (int64_t)passes * (parts / runs + 1) > kShareMinLoads;
+        const int64_t loads = (int64_t)passes * (parts / runs + 1);
+        a.merge_variant = 0;
+        if (p.dtype != PGD_F32 && p.d == 128) {
+            if (nr >= 2 && loads > kShareMinLoads) a.merge_variant = 1;
+            else if (nr >= 8 && loads > kStageMinLoads) a.merge_variant = 2;
+        }
     }
     a.tile_base = reinterpret_cast<int64_t*>(ws + wl.tile_base_off);
     a.part_lse = reinterpret_cast<float*>(ws + wl.part_lse_off);

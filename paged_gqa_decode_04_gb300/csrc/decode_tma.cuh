@@ -162,6 +162,22 @@ __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders this thread's generic global accesses with its async-proxy ones (the
+// split partials are stored by plain stores and read back by bulk copies).
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Untiled bulk copy global -> shared, completing on an mbarrier's transaction
+// count.  Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -226,7 +242,7 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
 }
 
 // ----------------------------------------------------------------- configuration
-template <int D_, int HG_, int MT_, int TG_, bool ROWS16_, bool FP8_ = false, bool SHARE_ = false>
+template <int D_, int HG_, int MT_, int TG_, bool ROWS16_, bool FP8_ = false, int MV_ = 0>
 struct Cfg {
     static constexpr int D = D_;
     static constexpr int HG = HG_;            // KV heads per unit of work
@@ -234,9 +250,13 @@ struct Cfg {
     static constexpr int TG = TG_;            // token groups per tile
     static constexpr bool ROWS16 = ROWS16_;   // rows 8..15 of an m-tile in use
     static constexpr bool FP8 = FP8_;         // 8-bit (e4m3) K/V pages, f16 products
-    // cooperative launch: a split run with a large merge is merged by all its
-    // pieces' warps together
-    static constexpr bool SHARE = SHARE_;
+    // merge variant of split runs: 0 the last arriver merges with register
+    // loads; 1 (SHARE, cooperative launch) all pieces' warps merge a share of
+    // the rows; 2 (STAGE) the last arriver stages the pieces through the idle
+    // ring with bulk copies, a group of rows per round
+    static constexpr int MV = MV_;
+    static constexpr bool SHARE = MV_ == 1;
+    static constexpr bool STAGE = MV_ == 2;
     // 128-byte rows of a head in a page box: D/64 for bf16, 1 for 8-bit D = 128
     static constexpr int HALVES = FP8 ? D / 128 : D / 64;
     static constexpr int HH = HG * HALVES;    // 128-byte head rows per token in a tile
@@ -259,6 +279,10 @@ struct Cfg {
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     // dynamic smem: [1024 align slack][stages][comb]
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + COMB_BYTES;
+    // STAGE: after the tile loop the merging warps (token group 0 of each head
+    // and m-tile) each own a slice of the ring and the combine buffer
+    static constexpr uint32_t MERGE_SLICE =
+        (uint32_t)((STAGES * STAGE_BYTES + COMB_BYTES) / (HG * MT)) & ~15u;
     static_assert(!FP8 || D == 128, "8-bit pages: head_dim 128");
     static_assert(STAGES >= 2, "pipeline needs at least two stages");
     static_assert(TW % 16 == 0, "a warp's token slice must be whole k16 steps");
@@ -399,6 +423,77 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int64_t t0, in
     }
 }
 
+// Staged merge (STAGE variant) of rows [r_lo, r_hi): rounds of `cnt` rows; in
+// each round every piece's rows [rb, rb + cnt) (contiguous in its partial) are
+// bulk-copied into the warp's slice on one mbarrier, the log2-sum-exp values
+// loaded beside them, and each row folded from shared memory.  Rows are
+// independent, so nothing carries over between rounds.  Returns 0 when done,
+// 1 when even one row of every piece does not fit the slice (the caller merges
+// with register loads instead), -1 when the staging wait gave up.
+template <class C>
+__device__ __forceinline__ int merge_staged(const DecodeArgs& a, int64_t t0, int64_t N, int64_t P,
+                                         int64_t c0, int npieces, bool first_is_tail, int hgi,
+                                         int r_lo, int r_hi, int b, int kvh, uint8_t* slice,
+                                         uint32_t bar, uint32_t& phase) {
+    constexpr int D = C::D;
+    constexpr int CPR = D / 4;                  // float4 chunks per row
+    constexpr int RPP = 32 / CPR;               // rows per pass
+    constexpr uint32_t ROW = D * 4;             // bytes of a partial row
+    const int lane = threadIdx.x % 32;
+    const int rows = a.q_len * a.group;         // query rows per KV head
+    const int piece_rows = C::HG * rows;
+    const int per_row = npieces * (ROW + 4);    // one row of every piece, and its lse
+    const int nrr = (int)(C::MERGE_SLICE / (uint32_t)per_row);
+    if (nrr < 1) return 1;
+    float* lse_base = nullptr;
+    const uint32_t slice_u = smem_u32(slice);
+    const int col = (lane % CPR) * 4;
+    const int rp = lane / CPR;
+    auto slot_of = [&](int k) -> int64_t {
+        const int64_t c = P > N ? span_owner(t0 + k, N, P) : c0 + k;
+        return c * 2 + ((first_is_tail && k == 0) ? 1 : 0);
+    };
+    fence_proxy_async_global();  // the partials were stored by generic stores
+    for (int rb = r_lo; rb < r_hi; rb += nrr) {
+        const int cnt = min(nrr, r_hi - rb);
+        const uint32_t bytes = (uint32_t)cnt * ROW;  // one piece's rows of this round
+        lse_base = reinterpret_cast<float*>(slice + (size_t)npieces * bytes);
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar, (uint32_t)npieces * bytes);
+            for (int k = 0; k < npieces; ++k)
+                bulk_load(slice_u + k * bytes,
+                          a.part_o + (slot_of(k) * piece_rows + hgi * rows + rb) * D, bytes, bar);
+        }
+        for (int i = lane; i < npieces * cnt; i += 32) {
+            const int k = i / cnt, r = i % cnt;
+            lse_base[i] = __ldcg(a.part_lse + slot_of(k) * piece_rows + hgi * rows + rb + r);
+        }
+        __syncwarp();
+        if (!mbar_wait(bar, phase)) return -1;
+        phase ^= 1u;
+        for (int r = rp; r < cnt; r += RPP) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            float M = -INFINITY, W = 0.f;
+#pragma unroll 4
+            for (int k = 0; k < npieces; ++k) {
+                const float4 v = *reinterpret_cast<const float4*>(slice + k * bytes +
+                                                                  (r * D + col) * 4);
+                lse_fold(M, W, acc, lse_base[k * cnt + r], 1.f, v);
+            }
+            const float w = W > 0.f ? 1.f / W : 0.f;  // no token in any piece: zeros
+            uint2 pk;
+            pk.x = pack_bf16(acc.x * w, acc.y * w);
+            pk.y = pack_bf16(acc.z * w, acc.w * w);
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) +
+                                      qrow_offset(a, b, kvh, rb + r) + col) = pk;
+        }
+        // the next round's bulk copies overwrite what these reads saw
+        __syncwarp();
+        fence_proxy_async();
+    }
+    return 0;
+}
+
 // ----------------------------------------------------------------- the kernel
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
@@ -415,6 +510,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     __shared__ __align__(8) uint64_t comb_bar;
     __shared__ StageDesc desc[S];
     __shared__ MergeJob jobs[C::NC][2];  // per consumer warp and partial slot
+    __shared__ __align__(8) uint64_t merge_bar[C::STAGE ? C::NC : 1];  // STAGE: staging barriers
     __shared__ volatile int aborted;
 
     uint8_t* stage_base = reinterpret_cast<uint8_t*>(
@@ -434,6 +530,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_init(smem_u32(&empty_bar[s]), C::NC * 32);
         }
         mbar_init(smem_u32(&comb_bar), C::NC * 32);
+        if constexpr (C::STAGE)
+            for (int w = 0; w < C::NC; ++w) mbar_init(smem_u32(&merge_bar[w]), 1);
         for (int w = 0; w < C::NC; ++w) jobs[w][0].b = jobs[w][1].b = -1;
         aborted = 0;
         fence_barrier_init();
@@ -1013,6 +1111,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     pl[prow1] = seg_bad ? 0.f : (lt1 > 0.f ? m1 + fast_log2(lt1) : -INFINITY);
             }
         }
+        if constexpr (C::STAGE) fence_proxy_async_global();  // read back by bulk copies
         // Publish the partial and count it; the warp that brings the count to
         // the number of pieces sets it back to zero and flips the run's flag
         // bit.  Shared merge (cooperative launch, a merge of more than six
@@ -1069,6 +1168,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (aborted) return;
     constexpr int RPP = 32 / (D / 4);  // rows per merge pass
     const int r_mine = mt * 16, r_end = min(rows, r_mine + C::ROWS);
+    uint32_t mphase = 0;
+    if constexpr (C::STAGE) {
+        // every consumer warp past the ring (so every copy into it has landed
+        // and been read): from here each merging warp owns a slice of it
+        fence_proxy_async();
+        mbar_arrive(smem_u32(&comb_bar));
+        if (!mbar_wait(smem_u32(&comb_bar), comb_phase)) {
+            if (lane == 0) latch_error(a.err, PGD_ERR_TIMEOUT);
+            return;
+        }
+    }
 #pragma unroll 1
     for (int j = 0; j < 2; ++j) {
         const MergeJob jb = jobs[warp][j];
@@ -1093,6 +1203,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
         }
         __threadfence();
+        if constexpr (C::STAGE) {
+            const int st = merge_staged<C>(a, jb.t0, ss.n_total, ss.parts, jb.c0, jb.npieces,
+                                           jb.first_is_tail != 0, hgi, m_lo, m_hi, jb.b, jb.kvh,
+                                           stage_base + (warp / C::TG) * C::MERGE_SLICE,
+                                           smem_u32(&merge_bar[warp]), mphase);
+            if (st < 0) {
+                if (lane == 0) latch_error(a.err, PGD_ERR_TIMEOUT);
+                return;
+            }
+            if (st == 0) continue;
+        }
         if (m_hi - m_lo <= RPP)
             merge_pieces<C, true>(a, jb.t0, ss.n_total, ss.parts, jb.c0, jb.npieces,
                                   jb.first_is_tail != 0, hgi, m_lo, m_hi, jb.b, jb.kvh);
@@ -1147,40 +1268,40 @@ constexpr int token_groups(int t, int hg, int mt) {
     return by_tokens < by_warps ? by_tokens : by_warps;
 }
 
-template <int D, int HG, int MT, bool R16, bool FP8, bool SHARE>
+template <int D, int HG, int MT, bool R16, bool FP8, int MV>
 cudaError_t launch_hg(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
     constexpr int TG = token_groups((FP8 ? 256 : 128) / HG, HG, MT);
     const int idx = HG == 1 ? 0 : HG == 2 ? 1 : HG == 4 ? 2 : 3;
-    return launch_cfg<Cfg<D, HG, MT, TG, R16, FP8, SHARE>>(a, p.tmap_k[idx], p.tmap_v[idx],
+    return launch_cfg<Cfg<D, HG, MT, TG, R16, FP8, MV>>(a, p.tmap_k[idx], p.tmap_v[idx],
                                                           p.num_sms, s);
 }
 
-template <int D, int MT, bool R16, bool FP8, bool SHARE>
+template <int D, int MT, bool R16, bool FP8, int MV>
 cudaError_t launch_mt(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
     switch (a.hg) {
-        case 1: return launch_hg<D, 1, MT, R16, FP8, SHARE>(a, p, s);
-        case 2: return launch_hg<D, 2, MT, R16, FP8, SHARE>(a, p, s);
+        case 1: return launch_hg<D, 1, MT, R16, FP8, MV>(a, p, s);
+        case 2: return launch_hg<D, 2, MT, R16, FP8, MV>(a, p, s);
         case 4:
-            if constexpr (MT <= 2) return launch_hg<D, 4, MT, R16, FP8, SHARE>(a, p, s);
+            if constexpr (MT <= 2) return launch_hg<D, 4, MT, R16, FP8, MV>(a, p, s);
             break;
         case 8:
-            if constexpr (MT == 1) return launch_hg<D, 8, MT, R16, FP8, SHARE>(a, p, s);
+            if constexpr (MT == 1) return launch_hg<D, 8, MT, R16, FP8, MV>(a, p, s);
             break;
     }
     return cudaErrorInvalidValue;
 }
 
 // FP8: 8-bit (e4m3) K/V pages (head_dim 128 only).
-// SHARE: the shared-merge variant (cooperative launch); returns
+// MV: merge variant (see Cfg).  The shared variant (1) returns
 // cudaErrorCooperativeLaunchTooLarge when the grid cannot be resident at once.
-template <int D, bool FP8, bool SHARE>
+template <int D, bool FP8, int MV>
 cudaError_t launch_tma_d(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
     const int rows = a.q_len * a.group;  // query rows per KV head
-    if (rows <= 8) return launch_mt<D, 1, false, FP8, SHARE>(a, p, s);
-    if (rows <= 16) return launch_mt<D, 1, true, FP8, SHARE>(a, p, s);
-    if (rows <= 32) return launch_mt<D, 2, true, FP8, SHARE>(a, p, s);
-    if (rows <= 48) return launch_mt<D, 3, true, FP8, SHARE>(a, p, s);
-    return launch_mt<D, 4, true, FP8, SHARE>(a, p, s);
+    if (rows <= 8) return launch_mt<D, 1, false, FP8, MV>(a, p, s);
+    if (rows <= 16) return launch_mt<D, 1, true, FP8, MV>(a, p, s);
+    if (rows <= 32) return launch_mt<D, 2, true, FP8, MV>(a, p, s);
+    if (rows <= 48) return launch_mt<D, 3, true, FP8, MV>(a, p, s);
+    return launch_mt<D, 4, true, FP8, MV>(a, p, s);
 }
 
 }  // namespace tma

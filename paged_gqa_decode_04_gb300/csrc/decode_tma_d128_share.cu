@@ -3,6 +3,6 @@
 
 namespace pgd {
 namespace tma {
-template cudaError_t launch_tma_d<128, false, true>(const DecodeArgs&, const Pool&, cudaStream_t);
+template cudaError_t launch_tma_d<128, false, 1>(const DecodeArgs&, const Pool&, cudaStream_t);
 }  // namespace tma
 }  // namespace pgd

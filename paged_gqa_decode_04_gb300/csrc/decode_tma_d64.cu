@@ -3,6 +3,6 @@
 
 namespace pgd {
 namespace tma {
-template cudaError_t launch_tma_d<64, false, false>(const DecodeArgs&, const Pool&, cudaStream_t);
+template cudaError_t launch_tma_d<64, false, 0>(const DecodeArgs&, const Pool&, cudaStream_t);
 }  // namespace tma
 }  // namespace pgd

@@ -4,6 +4,6 @@
 
 namespace pgd {
 namespace tma {
-template cudaError_t launch_tma_d<128, true, true>(const DecodeArgs&, const Pool&, cudaStream_t);
+template cudaError_t launch_tma_d<128, true, 1>(const DecodeArgs&, const Pool&, cudaStream_t);
 }  // namespace tma
 }  // namespace pgd

@@ -19,6 +19,9 @@ constexpr int kMaxGroup = 64;
 // lane (six batches of 4 row passes x 4 pieces): below that, the waits and the
 // second merge per CTA cost more than they save (measured).
 constexpr int kShareMinLoads = 96;
+// Staged merge (many query rows per head, few pieces): when one warp would need
+// more than two batches of register loads.
+constexpr int kStageMinLoads = 32;
 
 struct Pool {
     const void* k;
@@ -71,8 +74,9 @@ struct DecodeArgs {
     // workspace carve-up
     int* counters;         // [B][Hkv][m-tiles] per split run: pieces finished (zero between
                            // calls) and a flag bit flipped when the last piece arrives
-    int share_merge;       // host's choice: launch the shared-merge kernel variant (merges
-                           // expected large); it falls back when the grid cannot be resident
+    int merge_variant;     // host's choice of split-merge kernel variant: 0 last arriver,
+                           // 1 shared (long runs; falls back to 0 when the grid cannot be
+                           // resident), 2 staged through shared memory (many rows)
     int64_t* tile_base;    // [B + 1] first flat tile of each sequence
     float* part_o;         // [num_parts][2][hg * group][d] normalised partial outputs
     float* part_lse;       // [num_parts][2][hg * group]    partial log2-sum-exp
