@@ -132,7 +132,8 @@ int paged_gqa_workspace_size(pgd_pool_t pool, int B, int Hq, int num_splits, siz
 /*
  * Enqueue one decode step on `stream` (a cudaStream_t; NULL = legacy default
  * stream).
- *   q, out       [B, Hq, D] in the pool's dtype; out may not alias q
+ *   q, out       [B, Hq, D] in the pool's dtype (bfloat16 for 8-bit pools); out
+ *                may not alias q
  *   block_table  [B, max_blocks] int32; entries past ceil(Lb / block_size) are
  *                never read and may hold anything
  *   seq_lens     [B] int32, cached tokens per sequence; Lb == 0 gives zeros
@@ -141,10 +142,16 @@ int paged_gqa_workspace_size(pgd_pool_t pool, int B, int Hq, int num_splits, siz
  *                256-byte aligned, zero-filled before first use (see above);
  *                calls that may overlap on the GPU need distinct workspaces
  *   num_splits   how many equal spans the total KV work (all sequences times
- *                KV heads, in 64-token tiles) is cut into, one CTA each; a
- *                sequence crossing a span boundary is finished by a
- *                log-sum-exp merge.  0 = automatic (one span per SM).
+ *                KV heads, in tiles of 16 tokens for 8 KV heads at a time with
+ *                bfloat16 pages, 32 with 8-bit pages, 64 tokens of one head with
+ *                float32) is cut into, one CTA each; a sequence crossing a span
+ *                boundary is finished by a log-sum-exp merge.  0 = automatic
+ *                (one span per SM, at least two tiles per span).
  * The result does not depend on num_splits beyond float32 rounding.
+ * One kernel launch per call (two for float32 pools).  When the splits leave
+ * long runs to merge and the grid fits on the device at once, the launch is
+ * cooperative (the CTAs that share a run merge it together); if the driver
+ * refuses that, the ordinary launch is used.
  */
 int paged_gqa_decode(pgd_pool_t pool, const void *q, int B, int Hq, const int32_t *block_table,
                      int max_blocks, const int32_t *seq_lens, float scale, void *out,
