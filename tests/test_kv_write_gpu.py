@@ -24,14 +24,24 @@ def rand_rows(n, hkv, d, dtype, g):
     return torch.randn((n, hkv, d), generator=g, device=DEV, dtype=torch.float32).to(dtype)
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+FP8 = torch.float8_e4m3fn
+
+
+def make_pool(k, v):
+    if k.dtype == FP8:   # 8-bit pages: unit scales (the rows are codes already)
+        ones = torch.ones(k.shape[2], dtype=torch.float32, device=DEV)
+        return pgd.PagedKVPool(k, v, ones, ones.clone())
+    return pgd.PagedKVPool(k, v)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32, FP8])
 def test_append_and_copy_match_reference(dtype):
     g = torch.Generator(device=DEV)
     g.manual_seed(3)
     nb, bs, hkv, d = 20, 16, 8, 128
     k = torch.randn((nb, bs, hkv, d), generator=g, device=DEV).to(dtype)
     v = torch.randn((nb, bs, hkv, d), generator=g, device=DEV).to(dtype)
-    pool = pgd.PagedKVPool(k, v)
+    pool = make_pool(k, v)
     try:
         slots = torch.tensor([5, 16 * 3 + 7, 319, 0, 200], dtype=torch.int32, device=DEV)
         kn, vn = rand_rows(5, hkv, d, dtype, g), rand_rows(5, hkv, d, dtype, g)
@@ -55,18 +65,18 @@ def test_append_and_copy_match_reference(dtype):
         pool.close()
 
 
-@pytest.mark.parametrize("hkv,hq,d", [(2, 8, 64), (8, 32, 128)])
-def test_cache_lifecycle_decode_matches_oracle(hkv, hq, d):
+@pytest.mark.parametrize("hkv,hq,d,dtype", [(2, 8, 64, torch.bfloat16),
+                                            (8, 32, 128, torch.bfloat16), (8, 32, 128, FP8)])
+def test_cache_lifecycle_decode_matches_oracle(hkv, hq, d, dtype):
     """Prompts appended token by token, two forks sharing a prefix, twenty
     generated tokens with copy-on-write, then one decode step; every unwritten
     slot of the pool is NaN, so a read of the wrong slot shows."""
     g = torch.Generator(device=DEV)
     g.manual_seed(11)
-    rng = np.random.default_rng(11)
-    nb, bs, dtype = 96, 16, torch.bfloat16
+    nb, bs = 96, 16
     k = torch.full((nb, bs, hkv, d), float("nan"), device=DEV, dtype=dtype)
     v = torch.full_like(k, float("nan"))
-    pool = pgd.PagedKVPool(k, v)
+    pool = make_pool(k, v)
     m = pgd.KVBlockManager(nb, bs, max_seqs=8, max_blocks_per_seq=16)
     rows = {}                                     # seq -> list of (k_row, v_row) host bits
 
@@ -101,20 +111,25 @@ def test_cache_lifecycle_decode_matches_oracle(hkv, hq, d):
 
         seqs = list(range(6))
         table, lens = m.block_tables(seqs, 16)
-        q = torch.randn((6, hq, d), generator=g, device=DEV).to(dtype)
+        q = torch.randn((6, hq, d), generator=g, device=DEV).to(torch.bfloat16)
         out = pgd.paged_gqa_decode(pool, q, torch.from_numpy(table).to(DEV),
                                    torch.from_numpy(lens).to(DEV), 1.0 / np.sqrt(d))
         assert pgd.paged_gqa_get_error(pool) == 0
         # oracle on the logical sequences, laid out contiguously (one block each)
         L = max(len(rows[s]) for s in seqs)
-        kc = np.zeros((6, L, hkv, d), dtype=np.uint16)
+        kc = np.zeros((6, L, hkv, d), dtype=np.uint8 if dtype == FP8 else np.uint16)
         vc = np.zeros_like(kc)
         for i, s in enumerate(seqs):
             assert len(rows[s]) == lens[i]
             for t, (kr, vr) in enumerate(rows[s]):
                 kc[i, t], vc[i, t] = kr, vr
-        want, rc = oracle.decode_f64(bits(q), kc, vc, np.arange(6, dtype=np.int32)[:, None],
-                                     lens, 1.0 / np.sqrt(d))
+        one_block = np.arange(6, dtype=np.int32)[:, None]
+        if dtype == FP8:
+            unit = np.ones(hkv, dtype=np.float32)
+            want, rc = oracle.decode_kv8_f64(bits(q), kc, vc, unit, unit, one_block, lens,
+                                             1.0 / np.sqrt(d))
+        else:
+            want, rc = oracle.decode_f64(bits(q), kc, vc, one_block, lens, 1.0 / np.sqrt(d))
         assert rc == 0
         assert_close(out, want, "bf16", "lifecycle")
         for s in seqs:
