@@ -759,8 +759,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int lo_min = a.window > 0 ? max(0, dsc.L - a.q_len - a.window + 1) : 0;
         const int v_lo = max(0, lo_min - dsc.tok0);
         const bool active = tw0 < n_valid && tw0 + C::TW > v_lo;
-        const int z_hi = min(tw0 + C::TW, max(tw0, v_lo));  // zero [tw0, z_hi) ...
-        const int z_lo2 = max(tw0, n_valid);                // ... and [z_lo2, tw0 + TW)
+        // (both ends clamped to my slice: with several token groups or chunks
+        // a slice can end before n_valid while the window starts inside it)
+        const int z_hi = min(tw0 + C::TW, max(tw0, v_lo));        // zero [tw0, z_hi) ...
+        const int z_lo2 = min(tw0 + C::TW, max(tw0, n_valid));    // ... and [z_lo2, tw0 + TW)
         const bool zeroed = active && (z_hi > tw0 || z_lo2 < tw0 + C::TW);
         if (zeroed) {
             const int n1 = z_hi - tw0;

@@ -50,6 +50,9 @@ CASES = [
     ("sweep_bs128", dict(B=8, lens=("lognormal", 300.0, 1.0, 1, 900), max_len=1024), 2, 200),
     ("llama3_8b_fp8", dict(B=6, lens=("uniform", 50, 900), max_len=1024), 4, 0),
     ("llama3_8b_fp8", dict(B=6, lens=("uniform", 50, 900), max_len=1024), 2, 100),
+    ("llama3_8b", dict(B=4, D=64, lens=[5, 100, 260, 64], max_len=320), 3, 50),   # head_dim 64
+    ("llama3_8b", dict(B=3, Hq=16, Hkv=4, lens=[90, 200, 17], max_len=256), 4, 0),  # 4 heads/unit
+    ("llama3_8b_fp8", dict(B=3, Hq=16, Hkv=4, lens=[90, 300, 17], max_len=320), 2, 64),
 ]
 
 
@@ -122,3 +125,31 @@ def test_f32_rejects_extensions():
                                 w.scale, window=4)
     assert e.value.status == pgd._lib.PGD_ERR_UNSUPPORTED
     pool.close()
+
+
+def test_stale_shared_memory_never_reaches_windowed_outputs():
+    """Pages wholly before a window are not fetched, so their rows in the stage
+    hold whatever an earlier kernel left there; their V rows must be zeroed
+    even when a warp's token slice ends before the tile's last valid token
+    (several token groups per tile: 8-bit pages at 4 KV heads per unit, and
+    MQA).  A decode over an all-NaN pool first leaves NaN in every SM's
+    stages."""
+    filler = gen.make("llama3_8b", device=DEV, B=64, lens=[4096] * 64, max_len=4096)
+    filler.k_pool.fill_(float("nan"))
+    filler.v_pool.fill_(float("nan"))
+    fp = pgd.PagedKVPool(filler.k_pool, filler.v_pool)
+    cases = [("llama3_8b_fp8", dict(B=3, Hq=16, Hkv=4, lens=[90, 300, 17], max_len=320), 2, 64),
+             ("mqa_13b_b8", dict(B=2, lens=[300, 77], max_len=512), 1, 20),
+             ("llama3_8b", dict(B=3, Hq=16, Hkv=4, lens=[90, 300, 40], max_len=320), 1, 33)]
+    try:
+        for recipe, over, q_len, window in cases:
+            pgd.paged_gqa_decode(fp, filler.q, filler.block_table, filler.seq_lens, 0.1)
+            torch.cuda.synchronize()
+            w = gen.make(recipe, device=DEV, poison=True, **over)
+            q = make_q(w, q_len)
+            out = run_ex(w, q, window)
+            want, rc = oracle_ex(w, q, window)
+            assert rc == 0
+            assert_close(out, want, "bf16", "%s after a NaN filler" % recipe)
+    finally:
+        fp.close()

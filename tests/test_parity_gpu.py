@@ -37,6 +37,12 @@ SMALL = {
     "group24": ("llama3_8b", dict(B=3, Hq=48, Hkv=2, lens=[90, 200, 17], max_len=256)),
     "group64": ("llama3_8b", dict(B=2, Hq=64, Hkv=1, lens=[150, 9], max_len=256)),
     "bs256": ("llama3_8b", dict(B=3, block_size=256, lens=[700, 256, 3], max_len=768)),
+    # head-group sizes 4 and 2 with several units per sequence, and head_dim 64
+    "hkv4": ("llama3_8b", dict(B=5, Hq=16, Hkv=4, lens=[1, 65, 130, 64, 300], max_len=320)),
+    "hkv4_g16": ("llama3_8b", dict(B=3, Hq=64, Hkv=4, lens=[90, 200, 17], max_len=256)),
+    "hkv6": ("llama3_8b", dict(B=3, Hq=24, Hkv=6, lens=[90, 200, 17], max_len=256)),
+    "hkv12": ("llama3_8b", dict(B=3, Hq=48, Hkv=12, lens=[300, 20, 150], max_len=320)),
+    "d64_hkv4": ("llama3_8b", dict(B=3, D=64, Hq=16, Hkv=4, lens=[70, 200, 5], max_len=256)),
     # 8-bit (e4m3) pages with per-head scales, bfloat16 q and out
     "fp8_llama3_small": ("llama3_8b_fp8", dict(B=8, lens=("uniform", 1, 700), max_len=1024)),
     "fp8_long_small": ("long_70b_fp8", dict(B=2, lens=("uniform", 2000, 4100), max_len=4224)),
@@ -46,6 +52,10 @@ SMALL = {
                                       max_len=1024)),
     "fp8_bs128": ("llama3_8b_fp8", dict(B=12, block_size=128,
                                         lens=("lognormal", 200.0, 1.0, 1, 900), max_len=1024)),
+    "fp8_hkv4": ("llama3_8b_fp8", dict(B=5, Hq=16, Hkv=4, lens=[1, 65, 130, 64, 300],
+                                       max_len=320)),
+    "fp8_hkv2_g16": ("llama3_8b_fp8", dict(B=3, Hq=32, Hkv=2, lens=[90, 200, 17], max_len=256)),
+    "fp8_hkv6": ("llama3_8b_fp8", dict(B=3, Hq=24, Hkv=6, lens=[90, 300, 17], max_len=320)),
 }
 
 
