@@ -53,6 +53,12 @@ CASES = [
     ("llama3_8b", dict(B=4, D=64, lens=[5, 100, 260, 64], max_len=320), 3, 50),   # head_dim 64
     ("llama3_8b", dict(B=3, Hq=16, Hkv=4, lens=[90, 200, 17], max_len=256), 4, 0),  # 4 heads/unit
     ("llama3_8b_fp8", dict(B=3, Hq=16, Hkv=4, lens=[90, 300, 17], max_len=320), 2, 64),
+    ("llama3_8b", dict(B=3, lens=[700, 33, 300], max_len=768), 16, 0),           # 64 rows / head
+    ("long_70b", dict(B=2, lens=[3000, 1000], max_len=4096), 8, 100),           # 64 rows, window
+    ("llama3_8b_fp8", dict(B=6, block_size=8, lens=("lognormal", 200.0, 1.0, 1, 900),
+                           max_len=1024), 3, 40),                                # 8-token blocks
+    ("mqa_13b_b8", dict(B=2, block_size=128, lens=[900, 300], max_len=1024), 1, 100),
+    ("mha_13b_b8", dict(B=3, lens=[1000, 5, 260], max_len=1024), 2, 0),
 ]
 
 
