@@ -224,6 +224,37 @@ int paged_gqa_decode_noalloc(pgd_pool_t pool, const void *q, int B, int Hq,
 size_t paged_gqa_noalloc_scratch_bytes(void);
 
 /*
+ * paged_gqa_decode_ex with the step's inputs (q, block_table, seq_lens) and
+ * its output in HOST memory; the pools stay in device memory.  (The pages
+ * describe no such entry point; it is a property of this library.)
+ *
+ * Each of the four host buffers that is page-locked (cudaHostAlloc /
+ * cudaMallocHost / cudaHostRegister, so mapped into the device's address
+ * space) and aligned as paged_gqa_decode_ex requires (16 bytes for q and out,
+ * 4 for the int32 arrays) is read or written by the kernel itself through its
+ * mapped address, over the host link; every other buffer is staged through
+ * the workspace with cudaMemcpyAsync on `stream` (for pageable memory that
+ * copy may block the calling thread).  Either way the call is ordered on
+ * `stream`, and h_out holds the result once the stream has synchronised; the
+ * inputs must stay unchanged until then.
+ *   workspace    device buffer of at least paged_gqa_workspace_size_host
+ *                bytes, 256-byte aligned; its first
+ *                paged_gqa_workspace_size_ex bytes are the decode workspace
+ *                (zero-filled before first use, reusable as described there),
+ *                the rest is staging room for q, block_table, seq_lens and out
+ * Arguments, shapes, results and errors otherwise as paged_gqa_decode_ex.
+ * Returns PGD_ERR_CUDA if a staging copy cannot be enqueued.
+ */
+int paged_gqa_decode_host(pgd_pool_t pool, const void *h_q, int B, int q_len, int Hq,
+                          const int32_t *h_block_table, int max_blocks,
+                          const int32_t *h_seq_lens, int window, float scale, void *h_out,
+                          void *workspace, size_t workspace_bytes, int num_splits, void *stream);
+
+/* Workspace bytes for paged_gqa_decode_host (decode workspace + staging room). */
+int paged_gqa_workspace_size_host(pgd_pool_t pool, int B, int q_len, int Hq, int max_blocks,
+                                  int num_splits, size_t *bytes);
+
+/*
  * Diagnostic of the failure path: launch one thread that waits, with the
  * bounded wait the pipeline kernels use and a limit of limit_us microseconds
  * (1 .. 1e6), on a barrier nothing arrives on.  The wait gives up, latches

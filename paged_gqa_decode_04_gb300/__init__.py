@@ -19,6 +19,7 @@ __all__ = [
     "paged_gqa_workspace_size", "paged_gqa_decode", "paged_gqa_get_error",
     "paged_gqa_auto_splits", "paged_gqa_decode_ex", "paged_gqa_workspace_size_ex",
     "paged_gqa_decode_noalloc", "paged_gqa_noalloc_scratch_bytes",
+    "paged_gqa_decode_host", "paged_gqa_workspace_size_host",
     "strerror", "decode", "KVBlockManager", "paged_kv_append", "paged_kv_copy_blocks",
 ]
 
@@ -227,6 +228,58 @@ def paged_gqa_decode_noalloc(pool, q, block_table, seq_lens, scale, out, num_spl
 
 def paged_gqa_noalloc_scratch_bytes():
     return int(_lib.load().paged_gqa_noalloc_scratch_bytes())
+
+
+def paged_gqa_workspace_size_host(pool, B, q_len, Hq, max_blocks, num_splits=0):
+    n = ctypes.c_size_t()
+    _check(_lib.load().paged_gqa_workspace_size_host(pool.handle, int(B), int(q_len), int(Hq),
+                                                     int(max_blocks), int(num_splits),
+                                                     ctypes.byref(n)),
+           "paged_gqa_workspace_size_host")
+    return n.value
+
+
+def paged_gqa_decode_host(pool, q, block_table, seq_lens, scale, window=0, out=None,
+                          workspace=None, num_splits=0, stream=None):
+    """Decode with the step's inputs and output in host memory.
+
+    q [B, Hq, D] or [B, q_len, Hq, D], block_table [B, max_blocks] int32 and
+    seq_lens [B] int32 are contiguous CPU tensors; `out` (allocated like q,
+    page-locked when q is, if not given) receives the result.  Page-locked
+    tensors are read and written by the kernel in place; pageable ones are
+    staged through the workspace (a CUDA uint8 tensor of at least
+    paged_gqa_workspace_size_host bytes, zero-filled before first use).  The
+    call is asynchronous on `stream`: `out` is ready after that stream
+    synchronises.
+    """
+    lib = _lib.load()
+    if q.dim() not in (3, 4) or block_table.dim() != 2 or seq_lens.dim() != 1:
+        raise ValueError("q must be [B,(q_len,)Hq,D], block_table [B,max_blocks], seq_lens [B]")
+    if q.dtype != pool.q_dtype:
+        raise TypeError("q must be %s for this pool" % pool.q_dtype)
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    for t in (q, block_table, seq_lens):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CPU tensors")
+    B, Hq, D = q.shape[0], q.shape[-2], q.shape[-1]
+    q_len = q.shape[1] if q.dim() == 4 else 1
+    if D != pool.head_dim or block_table.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("shape mismatch between q, tables and pool")
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=q.is_pinned())
+    if out.is_cuda or not out.is_contiguous() or out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("out must be a contiguous CPU tensor shaped and typed like q")
+    max_blocks = block_table.shape[1]
+    if workspace is None:
+        nbytes = paged_gqa_workspace_size_host(pool, B, q_len, Hq, max_blocks, num_splits)
+        workspace = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=pool.k_pool.device)
+    _check(lib.paged_gqa_decode_host(pool.handle, q.data_ptr(), B, q_len, Hq,
+                                     block_table.data_ptr(), max_blocks, seq_lens.data_ptr(),
+                                     int(window), float(scale), out.data_ptr(),
+                                     workspace.data_ptr(), workspace.numel(), int(num_splits),
+                                     _stream_handle(stream)), "paged_gqa_decode_host")
+    return out
 
 
 def paged_gqa_get_error(pool, stream=None):

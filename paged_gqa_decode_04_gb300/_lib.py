@@ -76,6 +76,12 @@ def load(path=LIB_PATH):
     lib.paged_gqa_selftest_wait_timeout.restype = i32
     lib.paged_gqa_noalloc_scratch_bytes.argtypes = []
     lib.paged_gqa_noalloc_scratch_bytes.restype = sz
+    lib.paged_gqa_decode_host.argtypes = [vp, vp, i32, i32, i32, vp, i32, vp, i32,
+                                          ctypes.c_float, vp, vp, sz, i32, vp]
+    lib.paged_gqa_decode_host.restype = i32
+    lib.paged_gqa_workspace_size_host.argtypes = [vp, i32, i32, i32, i32, i32,
+                                                  ctypes.POINTER(sz)]
+    lib.paged_gqa_workspace_size_host.restype = i32
     # KV write path (include/paged_kv_manager.h)
     pi32 = ctypes.POINTER(ctypes.c_int32)
     pint = ctypes.POINTER(ctypes.c_int)

@@ -330,6 +330,97 @@ int paged_gqa_decode(pgd_pool_t pool, const void* q, int B, int Hq, const int32_
                                out, workspace, workspace_bytes, num_splits, stream);
 }
 
+// Staging room for paged_gqa_decode_host, after the decode workspace.
+struct HostLayout {
+    size_t io_bytes;   // q or out
+    size_t bt_bytes;   // block_table
+    size_t q_off, bt_off, sl_off, out_off, total;
+};
+
+static HostLayout host_layout(const Pool& p, size_t decode_bytes, int B, int q_len, int Hq,
+                              int max_blocks) {
+    HostLayout h;
+    const size_t elt = p.dtype == PGD_F32 ? 4 : 2;
+    h.io_bytes = (size_t)B * q_len * Hq * p.d * elt;
+    h.bt_bytes = (size_t)B * max_blocks * sizeof(int32_t);
+    h.q_off = round_up(decode_bytes, 256);
+    h.bt_off = h.q_off + round_up(h.io_bytes, 256);
+    h.sl_off = h.bt_off + round_up(h.bt_bytes, 256);
+    h.out_off = h.sl_off + round_up((size_t)B * sizeof(int32_t), 256);
+    h.total = h.out_off + round_up(h.io_bytes, 256);
+    return h;
+}
+
+// The address through which kernels on `dev` reach `h`, when `h` is
+// page-locked host memory mapped into the device's address space (or memory
+// of `dev` itself, or managed memory) and aligned to `align`; nullptr when it
+// has to be staged (pageable host memory, another device's memory).
+static const void* kernel_address(const void* h, uintptr_t align, int dev) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, h) != cudaSuccess) {
+        cudaGetLastError();  // the failed query's error is not sticky: clear it
+        return nullptr;
+    }
+    if (at.type == cudaMemoryTypeUnregistered || !at.devicePointer) return nullptr;
+    if (at.type == cudaMemoryTypeDevice && at.device != dev) return nullptr;
+    return aligned(at.devicePointer, align) ? at.devicePointer : nullptr;
+}
+
+int paged_gqa_workspace_size_host(pgd_pool_t pool, int B, int q_len, int Hq, int max_blocks,
+                                  int num_splits, size_t* bytes) {
+    if (!pool || !bytes || max_blocks < 0) return PGD_ERR_ARG;
+    size_t dec = 0;
+    const int rc = paged_gqa_workspace_size_ex(pool, B, q_len, Hq, num_splits, &dec);
+    if (rc != PGD_OK) return rc;
+    *bytes = host_layout(pool->p, dec, B, q_len, Hq, max_blocks).total;
+    return PGD_OK;
+}
+
+int paged_gqa_decode_host(pgd_pool_t pool, const void* h_q, int B, int q_len, int Hq,
+                          const int32_t* h_block_table, int max_blocks,
+                          const int32_t* h_seq_lens, int window, float scale, void* h_out,
+                          void* workspace, size_t workspace_bytes, int num_splits,
+                          void* stream) {
+    if (!pool || max_blocks < 0) return PGD_ERR_ARG;
+    size_t dec = 0;
+    int rc = paged_gqa_workspace_size_ex(pool, B, q_len, Hq, num_splits, &dec);
+    if (rc != PGD_OK) return rc;
+    if (B == 0)
+        return paged_gqa_decode_ex(pool, h_q, B, q_len, Hq, h_block_table, max_blocks,
+                                   h_seq_lens, window, scale, h_out, workspace, workspace_bytes,
+                                   num_splits, stream);
+    if (!h_q || !h_out || !h_block_table || !h_seq_lens || !workspace) return PGD_ERR_ARG;
+    const Pool& p = pool->p;
+    const HostLayout hl = host_layout(p, dec, B, q_len, Hq, max_blocks);
+    if (!aligned(workspace, 256) || workspace_bytes < hl.total) return PGD_ERR_WORKSPACE;
+
+    DeviceGuard g(p.device);
+    if (!g.ok) return PGD_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    // Inputs: read in place through the mapped address, else copied in first.
+    auto input = [&](const void* h, uintptr_t align, size_t off, size_t n) -> const void* {
+        if (const void* d = kernel_address(h, align, p.device)) return d;
+        if (n && cudaMemcpyAsync(ws + off, h, n, cudaMemcpyDefault, s) != cudaSuccess)
+            return nullptr;
+        return ws + off;
+    };
+    const void* q = input(h_q, 16, hl.q_off, hl.io_bytes);
+    const void* bt = input(h_block_table, 4, hl.bt_off, hl.bt_bytes);
+    const void* sl = input(h_seq_lens, 4, hl.sl_off, (size_t)B * sizeof(int32_t));
+    if (!q || !bt || !sl) return PGD_ERR_CUDA;
+    void* out = const_cast<void*>(kernel_address(h_out, 16, p.device));
+    const bool copy_out = out == nullptr;
+    if (copy_out) out = ws + hl.out_off;
+    rc = paged_gqa_decode_ex(pool, q, B, q_len, Hq, static_cast<const int32_t*>(bt), max_blocks,
+                             static_cast<const int32_t*>(sl), window, scale, out, workspace, dec,
+                             num_splits, stream);
+    if (rc != PGD_OK) return rc;
+    if (copy_out && cudaMemcpyAsync(h_out, out, hl.io_bytes, cudaMemcpyDefault, s) != cudaSuccess)
+        return PGD_ERR_CUDA;
+    return PGD_OK;
+}
+
 int paged_gqa_get_error(pgd_pool_t pool, void* stream) {
     if (!pool) return PGD_ERR_ARG;
     DeviceGuard g(pool->p.device);

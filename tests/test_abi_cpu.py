@@ -64,6 +64,10 @@ def test_null_handles_rejected(lib):
     assert lib.paged_kv_pool_destroy(None) == _lib.PGD_OK
     k = ctypes.c_int()
     assert lib.paged_gqa_auto_splits(None, ctypes.byref(k)) == _lib.PGD_ERR_ARG
+    assert lib.paged_gqa_workspace_size_host(None, 1, 1, 8, 4, 0,
+                                             ctypes.byref(n)) == _lib.PGD_ERR_ARG
+    assert lib.paged_gqa_decode_host(None, None, 1, 1, 8, None, 1, None, 0, 1.0, None, None, 0,
+                                     0, None) == _lib.PGD_ERR_ARG
 
 
 def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
