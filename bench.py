@@ -24,6 +24,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -89,12 +90,13 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "bench_clocks_%d.csv" % os.getpid())
+        self.path = None
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
+            self.f = tempfile.NamedTemporaryFile("w", prefix="bench_clocks_", suffix=".csv",
+                                                 delete=False)
+            self.path = self.f.name
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index),
                                           "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
                                           "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
@@ -117,15 +119,20 @@ class ClockSampler:
         if self.proc is None:
             return None
         rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
-                except ValueError:
-                    continue
+        try:
+            with open(self.path) as f:
+                lines = f.readlines()
+            os.unlink(self.path)
+        except OSError:
+            return None
+        for line in lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+            except ValueError:
+                continue
         if not rows:
             return None
         busy = [r for r in rows if r[2] > 1.5 * min(x[2] for x in rows)] or rows
