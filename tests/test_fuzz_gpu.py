@@ -16,7 +16,7 @@ from gpu_cases import assert_close, run_oracle
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 64
+N_CASES = 96
 
 
 def draw(case):
