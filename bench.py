@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -40,7 +41,7 @@ from paged_gqa_decode_04_gb300 import accounting  # noqa: E402
 METRIC = "paged GQA decode KV GB/s and % of GB300 HBM peak; tokens/s per layer"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SRC = os.path.join(ROOT, "paged_gqa_decode_04_gb300", "csrc", "decode_tma.cuh")
+CSRC = os.path.join(ROOT, "paged_gqa_decode_04_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -61,9 +62,23 @@ def peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_hash():
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+_COMMENT_OR_STRING = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\])*"', re.S)
+
+
+def kernel_hash(csrc=CSRC):
+    """Hash of the decode kernel's code: every device-side source of it
+    (decode_tma*, partition.cuh, pgd_internal.h) with comments dropped and
+    whitespace collapsed, so that an edit of comments alone keeps it."""
+    names = sorted(n for n in os.listdir(csrc)
+                   if (n.startswith("decode_tma") and n.endswith((".cu", ".cuh")))
+                   or n in ("partition.cuh", "pgd_internal.h"))
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(csrc, n)) as f:
+            text = f.read()
+        code = _COMMENT_OR_STRING.sub(lambda m: m.group(0) if m.group(0)[0] == '"' else " ", text)
+        h.update(n.encode() + b"\0" + " ".join(code.split()).encode() + b"\0")
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(config):

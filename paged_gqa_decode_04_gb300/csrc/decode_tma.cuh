@@ -38,9 +38,11 @@
 //     combine through shared memory at the end of a piece; the tg == 0 warps
 //     then write the output rows (whole run) or a normalised partial and its
 //     log2-sum-exp (split run).  After the tile loop a split run is merged by
-//     the warp whose arrival completed it, or, in the shared-merge variant
-//     (cooperative launch, long runs), by all its pieces' warps, each taking
-//     a share of the rows.
+//     the warp whose arrival completed it, with register loads of the pieces
+//     (merge variant 0) or, for many query rows and few pieces, through bulk
+//     copies of the pieces into its slice of the then idle stage ring
+//     (variant 2); in the shared-merge variant (1: cooperative launch, long
+//     runs) all its pieces' warps merge it, each taking a share of the rows.
 //   * 8-bit pages: K and V fragments come straight from the stage by
 //     ldmatrix and are widened to f16 in registers (cvt.rn.f16x2.e4m3x2);
 //     both products run on f16 mma.sync, the per-head scales fold into the
