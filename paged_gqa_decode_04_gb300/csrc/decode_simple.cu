@@ -11,7 +11,8 @@
 // which is the exact softmax of the Attention(Q,K,V) equation evaluated in one
 // pass ("Modern LLM Inference ...", "Linear Attention vs. FlashAttention
 // (Online Softmax)": FlashAttention keeps the softmax exact).  This kernel is
-// the float32 path; the bfloat16 path is the TMA pipeline in decode_tma.cu.
+// the float32 path; bfloat16 and 8-bit pages take the TMA pipeline of
+// decode_tma.cuh.
 #include <cuda_bf16.h>
 #include <math.h>
 

@@ -14,7 +14,8 @@
 // the length mix.  A (b, u) run that lies inside one span is finished by that
 // CTA; a run cut by span boundaries leaves one partial result per piece, in
 // slot 0 of a CTA (the piece that starts the CTA's span) or slot 1 (the piece
-// that ends it), and the merge kernel combines them with a log-sum-exp.
+// that ends it), and a log-sum-exp merge combines them (inside the TMA kernel,
+// after its tile loop; a separate merge kernel after the CUDA-core kernel).
 // This is the split-KV scheme of FlashDecoding ("Modern LLM Inference ...",
 // section 8.3 lists FlashDecoding kernels) with the splits placed by work
 // rather than per sequence.
@@ -70,11 +71,12 @@ struct SpanStart {
     int64_t b_base;    // tile_base[b]
 };
 
-// Every thread of the block must call this; blockDim.x is a multiple of 32 and at
-// most 1024.  `scratch` is >= 64 int64 of shared memory, `out` a shared SpanStart.  With min_tiles > 1 the spans in
-// use are min(parts, ceil(N / min_tiles)) (at least 1) and CTAs beyond them get
-// an empty span; with min_tiles == 1 all `parts` spans are used.  CTA 0 also writes tile_base[0..B] to global memory for the merge
-// kernel.
+// Every thread of the block must call this; blockDim.x is a multiple of 32 and
+// at most 1024.  `scratch` is >= 64 int64 of shared memory, `out` a shared
+// SpanStart.  With min_tiles > 1 the spans in use are min(parts,
+// ceil(N / min_tiles)) (at least 1) and CTAs beyond them get an empty span;
+// with min_tiles == 1 all `parts` spans are used.  CTA 0 also writes
+// tile_base[0..B] to global memory for the merge kernel.
 __device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int B, int units,
                                        int T, int q_len, int window, int max_blocks,
                                        int block_size, int64_t parts, int min_tiles,
