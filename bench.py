@@ -206,10 +206,14 @@ def barrier(world):
         dist.barrier()
 
 
-def cpu_oracle_rate(w, budget_s, rows_cap=None):
-    """Run the oracle over the whole workload (or a row subset) until
-    `budget_s` has passed; returns (GB/s over algorithmic bytes, sample, cores)."""
+def cpu_oracle_rate(w, budget_s, threads=0):
+    """Run the oracle over the whole workload until `budget_s` has passed, on
+    `threads` host cores (0: all); returns (GB/s over algorithmic bytes,
+    sample, cores, sequences/s)."""
     import oracle
+
+    if threads > 0:
+        oracle.set_num_threads(threads)
 
     q, k, v = gen.to_numpy_bits(w.q), gen.to_numpy_bits(w.k_pool), gen.to_numpy_bits(w.v_pool)
     elt, q_elt = accounting.ELT[w.dtype], accounting.Q_ELT[w.dtype]
@@ -227,7 +231,8 @@ def cpu_oracle_rate(w, budget_s, rows_cap=None):
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    sample = "%d full pass(es) of the workload (all %d x %d rows) in %.1f s" % (reps, w.B, w.Hq, dt)
+    sample = ("%d full pass(es) of the workload (all %d x %d rows) in %.1f s on %d host core(s)"
+              % (reps, w.B, w.Hq, dt, oracle.num_threads()))
     return nbytes * reps / dt / 1e9, sample, oracle.num_threads(), w.B * reps / dt
 
 
@@ -240,6 +245,9 @@ def run_reference(args, world, rank):
     nbytes = accounting.algorithmic_bytes(w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt, q_elt)
     import oracle
 
+    if args.cpu_threads > 0:
+        oracle.set_num_threads(args.cpu_threads)
+    cores = oracle.num_threads()
     q, k, v = gen.to_numpy_bits(w.q), gen.to_numpy_bits(w.k_pool), gen.to_numpy_bits(w.v_pool)
     # One step = the oracle over a bounded sample: every sequence, a subset of
     # query heads (whole KV groups) so that K+W steps fit in a few minutes.
@@ -251,15 +259,15 @@ def run_reference(args, world, rank):
                                              w.lens_np[:nb], w.scale)
         frac = accounting.algorithmic_bytes(w.lens_np[:nb], w.Hq, w.Hkv, w.D, w.block_size, elt,
                                             q_elt) / nbytes
-        sample = ("each step: sequences 0..%d of %d, every query head, float64, host cores"
-                  % (nb - 1, w.B))
+        sample = ("each step: sequences 0..%d of %d, every query head, float64, %d host "
+                  "core(s)" % (nb - 1, w.B, cores))
     else:
         heads = max(w.G, min(w.Hq, (w.Hq // 8) // w.G * w.G or w.G))
         rows = np.array([[b, h] for b in range(w.B) for h in range(heads)], dtype=np.int32)
         frac = heads / w.Hq
         step = lambda: oracle.decode_rows_f64(q, k, v, w.table_np, w.lens_np, w.scale, rows)
         sample = ("each step: every sequence, query heads 0..%d of %d (%.1f%% of the rows), "
-                  "float64, host cores" % (heads - 1, w.Hq, 100 * frac))
+                  "float64, %d host core(s)" % (heads - 1, w.Hq, 100 * frac, cores))
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
@@ -272,8 +280,8 @@ def run_reference(args, world, rank):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": describe(w), "parallelism": "host cores"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+        "config": {"workload": describe(w), "parallelism": "%d host core(s)" % cores},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -496,7 +504,7 @@ def run_ours(args, world, rank, local):
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
-        rate, sample, cores, _ = cpu_oracle_rate(w, args.cpu_seconds)
+        rate, sample, cores, _ = cpu_oracle_rate(w, args.cpu_seconds, args.cpu_threads)
         line["cpu_baseline"] = {"value": round(rate, 4), "unit": "GB/s", "cores": cores,
                                 "kind": "oracle", "sample": sample}
     print(json.dumps(line), flush=True)
@@ -511,6 +519,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-threads", type=int, default=0,
+                    help="host cores the CPU oracle runs on (cpu_baseline and --impl "
+                         "reference); 0 = all")
     ap.add_argument("--op", default="decode", choices=["decode", "decode_ex", "append"],
                     help="decode (the headline), decode_ex (several query tokens and/or a "
                          "window), append (KV write path)")

@@ -69,11 +69,18 @@ class Oracle:
         lib.oracle_decode_kv8_f64.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+        lib.oracle_set_num_threads.restype = ctypes.c_int
         self.lib = lib
         self.path = path
 
     def num_threads(self):
         return int(self.lib.oracle_num_threads())
+
+    def set_num_threads(self, n):
+        """Rows computed at once from now on (the arithmetic of a row does not
+        change); returns the count in effect."""
+        return int(self.lib.oracle_set_num_threads(int(n)))
 
     def decode_f64(self, q, k_pool, v_pool, block_table, seq_lens, scale):
         """All rows.  Returns (out[B,Hq,D] float64, status)."""
@@ -175,6 +182,10 @@ def default():
 
 def num_threads():
     return default().num_threads()
+
+
+def set_num_threads(n):
+    return default().set_num_threads(n)
 
 
 def decode_f64(q, k_pool, v_pool, block_table, seq_lens, scale):

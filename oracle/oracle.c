@@ -331,3 +331,16 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/* Use n threads from now on (n >= 1; ignored without OpenMP); returns the
+ * count in effect.  Changes only how many rows run at once, never the
+ * arithmetic of a row. */
+int oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+    return oracle_num_threads();
+}

@@ -52,3 +52,19 @@ def test_whole_job_value():
     import bench
 
     assert bench.whole_job_gbs(nbytes=1e9, t_ms=2.0, world=4) == pytest.approx(2000.0)
+
+
+def test_reference_arm_reports_its_core_count():
+    """`--impl reference --cpu-threads 1` times the oracle on one host core and
+    says so; without the flag it uses every core OpenMP offers."""
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--config",
+           "tiny", "--steps", "3", "--warmup", "3"]
+    one = json.loads(subprocess.run(cmd + ["--cpu-threads", "1"], capture_output=True, text=True,
+                                    check=True, cwd=root).stdout.strip().splitlines()[-1])
+    assert one["impl"] == "reference" and one["cpu_baseline"]["cores"] == 1
+    assert "1 host core" in one["cpu_baseline"]["sample"] and one["value"] > 0
