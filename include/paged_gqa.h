@@ -250,6 +250,30 @@ int paged_gqa_decode_host(pgd_pool_t pool, const void *h_q, int B, int q_len, in
                           const int32_t *h_seq_lens, int window, float scale, void *h_out,
                           void *workspace, size_t workspace_bytes, int num_splits, void *stream);
 
+/*
+ * The launch plan paged_gqa_decode_ex would use for these shapes, computed on
+ * the host from the shapes alone (no device, no pool): dtype, num_kv_heads and
+ * head_dim as for paged_kv_pool_create, num_sms the SM count of the device
+ * (152 on GB300), the other arguments as for paged_gqa_decode_ex.  Writes five
+ * ints to plan:
+ *   plan[0]  KV heads per unit of work (the head group one tile covers)
+ *   plan[1]  m16 row tiles of one KV head's q_len * Hq / Hkv query rows
+ *   plan[2]  tokens per tile
+ *   plan[3]  CTAs of the grid; with num_splits = 0 the kernel then uses
+ *            min(plan[3], ceil(tiles / 2)) of them, tiles counted from the
+ *            lengths on the device
+ *   plan[4]  split merge: 0 by the warp whose piece completes a run, 1 shared
+ *            among all the run's pieces under a cooperative launch (the
+ *            library falls back to 0 if the device refuses that launch), 2 by
+ *            the completing warp through bulk copies into shared memory, 3 a
+ *            separate merge kernel (float32 pools)
+ * Returns the status paged_gqa_decode_ex returns for these shapes before any
+ * pointer is looked at (PGD_ERR_SHAPE, PGD_ERR_UNSUPPORTED, ...).  A
+ * diagnostic of this library; the pages have no counterpart.
+ */
+int paged_gqa_plan(int dtype, int num_kv_heads, int head_dim, int num_sms, int B, int q_len,
+                   int Hq, int num_splits, int window, int *plan);
+
 /* Workspace bytes for paged_gqa_decode_host (decode workspace + staging room). */
 int paged_gqa_workspace_size_host(pgd_pool_t pool, int B, int q_len, int Hq, int max_blocks,
                                   int num_splits, size_t *bytes);

@@ -19,7 +19,7 @@ __all__ = [
     "paged_gqa_workspace_size", "paged_gqa_decode", "paged_gqa_get_error",
     "paged_gqa_auto_splits", "paged_gqa_decode_ex", "paged_gqa_workspace_size_ex",
     "paged_gqa_decode_noalloc", "paged_gqa_noalloc_scratch_bytes",
-    "paged_gqa_decode_host", "paged_gqa_workspace_size_host",
+    "paged_gqa_decode_host", "paged_gqa_workspace_size_host", "paged_gqa_plan",
     "strerror", "decode", "KVBlockManager", "paged_kv_append", "paged_kv_copy_blocks",
 ]
 
@@ -280,6 +280,26 @@ def paged_gqa_decode_host(pool, q, block_table, seq_lens, scale, window=0, out=N
                                      workspace.data_ptr(), workspace.numel(), int(num_splits),
                                      _stream_handle(stream)), "paged_gqa_decode_host")
     return out
+
+
+PLAN_MERGE = {0: "last arriver", 1: "shared (cooperative)", 2: "staged", 3: "merge kernel"}
+
+
+def paged_gqa_plan(dtype, num_kv_heads, head_dim, B, Hq, q_len=1, num_splits=0, window=0,
+                   num_sms=None):
+    """The launch plan a decode with these shapes would use (host only, no device
+    needed when num_sms is given): dict with head_group, m_tiles, tile_tokens,
+    grid and merge (see paged_gqa.h)."""
+    if num_sms is None:
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    if isinstance(dtype, torch.dtype):
+        dtype = _lib.PGD_FP8_E4M3 if dtype in _FP8 else _DTYPES[dtype]
+    plan = (ctypes.c_int * 5)()
+    _check(_lib.load().paged_gqa_plan(int(dtype), int(num_kv_heads), int(head_dim), int(num_sms),
+                                      int(B), int(q_len), int(Hq), int(num_splits), int(window),
+                                      plan), "paged_gqa_plan")
+    return {"head_group": plan[0], "m_tiles": plan[1], "tile_tokens": plan[2], "grid": plan[3],
+            "merge": PLAN_MERGE[plan[4]]}
 
 
 def paged_gqa_get_error(pool, stream=None):

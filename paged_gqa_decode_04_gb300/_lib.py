@@ -79,6 +79,8 @@ def load(path=LIB_PATH):
     lib.paged_gqa_decode_host.argtypes = [vp, vp, i32, i32, i32, vp, i32, vp, i32,
                                           ctypes.c_float, vp, vp, sz, i32, vp]
     lib.paged_gqa_decode_host.restype = i32
+    lib.paged_gqa_plan.argtypes = [i32] * 9 + [ctypes.POINTER(i32)]
+    lib.paged_gqa_plan.restype = i32
     lib.paged_gqa_workspace_size_host.argtypes = [vp, i32, i32, i32, i32, i32,
                                                   ctypes.POINTER(sz)]
     lib.paged_gqa_workspace_size_host.restype = i32

@@ -88,13 +88,57 @@ int resolve_parts(const Pool& p, int num_splits) {
 
 const Pool& pool_desc(pgd_pool_t h) { return h->p; }
 
-int choose_hg(const Pool& p, int rows) {
-    if (p.dtype == PGD_F32) return 1;
+static int choose_hg_for(int dtype, int hkv, int rows) {
+    if (dtype == PGD_F32) return 1;
     const int mt = (rows + 15) / 16;
     const int cap = mt == 1 ? 8 : mt == 2 ? 4 : 2;  // at most 8 consumer warps
     int hg = 8;
-    while (hg > 1 && (p.hkv % hg != 0 || hg > cap)) hg /= 2;
+    while (hg > 1 && (hkv % hg != 0 || hg > cap)) hg /= 2;
     return hg;
+}
+
+int choose_hg(const Pool& p, int rows) { return choose_hg_for(p.dtype, p.hkv, rows); }
+
+// The launch plan of a decode call, from shapes alone.  Status as the decode
+// entry points return it for these shapes.
+struct Plan {
+    int hg;             // KV heads per unit of work
+    int m_tiles;        // m16 row tiles of one head's query rows
+    int tile_tokens;    // tokens per tile
+    int parts;          // CTAs of the grid (spans of the tile sequence)
+    int merge_variant;  // 0 last arriver, 1 shared (cooperative), 2 staged, 3 separate kernel
+};
+
+static int make_plan(int dtype, int hkv, int d, int num_sms, int B, int q_len, int Hq,
+                     int num_splits, int window, Plan* out) {
+    if (hkv < 1 || Hq < 1 || B < 0 || q_len < 1 || num_sms < 1 || num_splits < 0 ||
+        num_splits > (1 << 20) || window < 0)
+        return PGD_ERR_ARG;
+    if (dtype != PGD_F32 && dtype != PGD_BF16 && dtype != PGD_FP8_E4M3) return PGD_ERR_DTYPE;
+    if (d != 64 && d != 128) return PGD_ERR_SHAPE;
+    if (dtype == PGD_FP8_E4M3 && d != 128) return PGD_ERR_SHAPE;
+    if (Hq % hkv != 0) return PGD_ERR_SHAPE;
+    const int rows = q_len * (Hq / hkv);
+    if (rows > kMaxGroup) return PGD_ERR_SHAPE;
+    if (dtype == PGD_F32 && (q_len > 1 || window > 0)) return PGD_ERR_UNSUPPORTED;
+    Plan pl;
+    pl.hg = choose_hg_for(dtype, hkv, rows);
+    pl.m_tiles = (rows + 15) / 16;
+    pl.tile_tokens = dtype == PGD_F32 ? kSimpleTileTokens : (dtype == PGD_FP8_E4M3 ? 256 : 128) / pl.hg;
+    pl.parts = num_splits > 0 ? num_splits : num_sms;
+    // Merge variant from the expected size of a split run's merge: about
+    // parts / runs + 1 pieces per run, times the row passes of one warp.
+    pl.merge_variant = dtype == PGD_F32 ? 3 : 0;
+    if (dtype != PGD_F32 && d == 128 && B > 0) {
+        const int runs = B * (hkv / pl.hg);
+        const int nr = rows < 16 ? rows : 16;          // rows of one warp's m-tile
+        const int passes = (nr * d + 127) / 128;       // 128 / D rows per merge pass
+        const int64_t loads = (int64_t)passes * (pl.parts / runs + 1);
+        if (nr >= 2 && loads > kShareMinLoads) pl.merge_variant = 1;
+        else if (nr >= 8 && loads > kStageMinLoads) pl.merge_variant = 2;
+    }
+    *out = pl;
+    return PGD_OK;
 }
 
 WorkspaceLayout workspace_layout(int B, int hkv, int rows_per_head, int hg, int d, int parts) {
@@ -240,11 +284,14 @@ int paged_gqa_decode_ex(pgd_pool_t pool, const void* q, int B, int q_len, int Hq
         return PGD_ERR_ARG;
     if (!isfinite(scale)) return PGD_ERR_ARG;
     const Pool& p = pool->p;
-    if (Hq % p.hkv != 0) return PGD_ERR_SHAPE;
+    Plan plan;
+    {
+        const int rc = make_plan(p.dtype, p.hkv, p.d, p.num_sms, B, q_len, Hq, num_splits,
+                                 window, &plan);
+        if (rc != PGD_OK) return rc;
+    }
     const int G = Hq / p.hkv;
     const int rows = q_len * G;
-    if (rows > kMaxGroup) return PGD_ERR_SHAPE;
-    if (p.dtype == PGD_F32 && (q_len > 1 || window > 0)) return PGD_ERR_UNSUPPORTED;
     if ((int64_t)max_blocks * p.block_size > INT32_MAX) return PGD_ERR_SHAPE;
     if (B == 0) return PGD_OK;
     if (!q || !out || !block_table || !seq_lens || !workspace) return PGD_ERR_ARG;
@@ -258,8 +305,8 @@ int paged_gqa_decode_ex(pgd_pool_t pool, const void* q, int B, int q_len, int Hq
     if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_table, 4) ||
         !aligned(seq_lens, 4))
         return PGD_ERR_ALIGN;
-    const int parts = resolve_parts(p, num_splits);
-    const int hg = choose_hg(p, rows);
+    const int parts = plan.parts;
+    const int hg = plan.hg;
     const WorkspaceLayout wl = workspace_layout(B, p.hkv, rows, hg, p.d, parts);
     if (!aligned(workspace, 256) || workspace_bytes < wl.total) return PGD_ERR_WORKSPACE;
 
@@ -291,23 +338,11 @@ int paged_gqa_decode_ex(pgd_pool_t pool, const void* q, int B, int q_len, int Hq
     a.auto_parts = num_splits == 0;
     a.hg = hg;
     a.units = p.hkv / hg;
-    a.tile_tokens = p.dtype == PGD_F32 ? kSimpleTileTokens : (p.dtype == PGD_FP8_E4M3 ? 256 : 128) / hg;
+    a.tile_tokens = plan.tile_tokens;
     a.err = p.err;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     a.counters = reinterpret_cast<int*>(ws + wl.counters_off);
-    {
-        // Merge variant from the expected size of a split run's merge: about
-        // parts / runs + 1 pieces per run, times the row passes of one warp.
-        const int runs = B * a.units;
-        const int nr = rows < 16 ? rows : 16;          // rows of one warp's m-tile
-        const int passes = (nr * p.d + 127) / 128;     // 128 / D rows per merge pass
-        const int64_t loads = (int64_t)passes * (parts / runs + 1);
-        a.merge_variant = 0;
-        if (p.dtype != PGD_F32 && p.d == 128) {
-            if (nr >= 2 && loads > kShareMinLoads) a.merge_variant = 1;
-            else if (nr >= 8 && loads > kStageMinLoads) a.merge_variant = 2;
-        }
-    }
+    a.merge_variant = plan.merge_variant == 3 ? 0 : plan.merge_variant;
     a.tile_base = reinterpret_cast<int64_t*>(ws + wl.tile_base_off);
     a.part_lse = reinterpret_cast<float*>(ws + wl.part_lse_off);
     a.part_o = reinterpret_cast<float*>(ws + wl.part_o_off);
@@ -418,6 +453,21 @@ int paged_gqa_decode_host(pgd_pool_t pool, const void* h_q, int B, int q_len, in
     if (rc != PGD_OK) return rc;
     if (copy_out && cudaMemcpyAsync(h_out, out, hl.io_bytes, cudaMemcpyDefault, s) != cudaSuccess)
         return PGD_ERR_CUDA;
+    return PGD_OK;
+}
+
+int paged_gqa_plan(int dtype, int num_kv_heads, int head_dim, int num_sms, int B, int q_len,
+                   int Hq, int num_splits, int window, int* plan) {
+    if (!plan) return PGD_ERR_ARG;
+    Plan pl;
+    const int rc = make_plan(dtype, num_kv_heads, head_dim, num_sms, B, q_len, Hq, num_splits,
+                             window, &pl);
+    if (rc != PGD_OK) return rc;
+    plan[0] = pl.hg;
+    plan[1] = pl.m_tiles;
+    plan[2] = pl.tile_tokens;
+    plan[3] = pl.parts;
+    plan[4] = pl.merge_variant;
     return PGD_OK;
 }
 

@@ -1,0 +1,89 @@
+"""The host's launch plan (paged_gqa_plan), on CPU: head grouping, row tiles,
+tile sizes, grid and split-merge choice for every workload shape, and the
+statuses a decode returns for shapes it does not take.  The decode entry points
+use the same planning function, so this pins the host side of every launch."""
+import pytest
+import torch
+
+import paged_gqa_decode_04_gb300 as pgd
+from paged_gqa_decode_04_gb300 import _lib
+
+BF16, FP8, F32 = torch.bfloat16, torch.float8_e4m3fn, torch.float32
+
+
+def plan(dtype, hkv, d, B, Hq, **kw):
+    return pgd.paged_gqa_plan(dtype, hkv, d, B, Hq, num_sms=152, **kw)
+
+
+# (name, args, kwargs, expected (head_group, m_tiles, tile_tokens, grid, merge))
+CASES = [
+    ("llama3_8b", (BF16, 8, 128, 64, 32), {}, (8, 1, 16, 152, "last arriver")),
+    ("long_70b", (BF16, 8, 128, 8, 64), {}, (8, 1, 16, 152, "shared (cooperative)")),
+    ("mha_13b_b1", (BF16, 40, 128, 1, 40), {}, (8, 1, 16, 152, "last arriver")),
+    ("mqa_13b_b1", (BF16, 1, 128, 1, 40), {}, (1, 3, 128, 152, "shared (cooperative)")),
+    ("mqa_13b_b8", (BF16, 1, 128, 8, 40), {}, (1, 3, 128, 152, "shared (cooperative)")),
+    ("sweep B 256", (BF16, 8, 128, 256, 32), {}, (8, 1, 16, 152, "last arriver")),
+    ("4 query tokens, B 64", (BF16, 8, 128, 64, 32), dict(q_len=4), (8, 1, 16, 152, "staged")),
+    ("4 query tokens, B 24", (BF16, 8, 128, 24, 32), dict(q_len=4),
+     (8, 1, 16, 152, "shared (cooperative)")),
+    # 32 / 64 rows per head: 128 / 256 runs over 152 spans, so a run has at most
+    # 152 // runs + 1 = 2 / 1 pieces and a warp's 16 rows x 2 pieces stay within
+    # two batches of loads: the last arriver merges
+    ("8 query rows x 4 tokens", (BF16, 8, 128, 64, 64), dict(q_len=4),
+     (4, 2, 32, 152, "last arriver")),
+    ("64 query rows", (BF16, 8, 128, 64, 128), dict(q_len=4), (2, 4, 64, 152, "last arriver")),
+    ("32 rows, B 8", (BF16, 8, 128, 8, 64), dict(q_len=4), (4, 2, 32, 152, "shared (cooperative)")),
+    ("8-bit llama3", (FP8, 8, 128, 64, 32), {}, (8, 1, 32, 152, "last arriver")),
+    ("8-bit long_70b", (FP8, 8, 128, 8, 64), {}, (8, 1, 32, 152, "shared (cooperative)")),
+    ("head_dim 64", (BF16, 2, 64, 4, 8), {}, (2, 1, 64, 152, "last arriver")),
+    ("Hkv 6", (BF16, 6, 128, 4, 24), {}, (2, 1, 64, 152, "last arriver")),
+    ("float32 tiny", (F32, 2, 64, 4, 8), {}, (1, 1, 64, 152, "merge kernel")),
+    ("explicit splits", (BF16, 8, 128, 64, 32), dict(num_splits=500),
+     (8, 1, 16, 500, "last arriver")),
+]
+
+
+@pytest.mark.parametrize("name,args,kw,want", CASES, ids=[c[0] for c in CASES])
+def test_plan_of_each_shape(name, args, kw, want):
+    p = plan(*args, **kw)
+    assert (p["head_group"], p["m_tiles"], p["tile_tokens"], p["grid"], p["merge"]) == want
+
+
+def test_plan_invariants():
+    for dtype in (BF16, FP8):
+        for hkv in (1, 2, 3, 4, 5, 6, 8, 40):
+            for G in (1, 2, 4, 8, 16, 40, 64):
+                for q_len in (1, 2, 4):
+                    if q_len * G > 64:
+                        continue
+                    p = plan(dtype, hkv, 128, 16, hkv * G, q_len=q_len)
+                    hg, mt, T = p["head_group"], p["m_tiles"], p["tile_tokens"]
+                    assert hkv % hg == 0 and hg in (1, 2, 4, 8)
+                    assert mt == (q_len * G + 15) // 16
+                    assert hg * mt <= 8                       # at most 8 consumer warps
+                    assert T * hg == (256 if dtype == FP8 else 128)  # 64 KB stages
+
+
+@pytest.mark.parametrize("args,kw,status", [
+    ((BF16, 8, 128, 4, 30), {}, _lib.PGD_ERR_SHAPE),             # Hq % Hkv
+    ((BF16, 1, 128, 4, 65), {}, _lib.PGD_ERR_SHAPE),             # 65 rows per head
+    ((BF16, 8, 128, 4, 32), dict(q_len=17), _lib.PGD_ERR_SHAPE),  # 68 rows per head
+    ((BF16, 8, 96, 4, 32), {}, _lib.PGD_ERR_SHAPE),              # head_dim 96
+    ((FP8, 8, 64, 4, 32), {}, _lib.PGD_ERR_SHAPE),               # 8-bit pages: head_dim 128
+    ((F32, 2, 64, 4, 8), dict(q_len=2), _lib.PGD_ERR_UNSUPPORTED),
+    ((F32, 2, 64, 4, 8), dict(window=16), _lib.PGD_ERR_UNSUPPORTED),
+    ((BF16, 8, 128, -1, 32), {}, _lib.PGD_ERR_ARG),
+    ((BF16, 8, 128, 4, 32), dict(num_splits=-1), _lib.PGD_ERR_ARG),
+])
+def test_plan_rejects_what_the_decode_rejects(args, kw, status):
+    with pytest.raises(pgd.PagedGQAError) as e:
+        plan(*args, **kw)
+    assert e.value.status == status
+
+
+def test_plan_null_output_and_bad_dtype():
+    lib = _lib.load()
+    assert lib.paged_gqa_plan(1, 8, 128, 152, 4, 1, 32, 0, 0, None) == _lib.PGD_ERR_ARG
+    import ctypes
+    out = (ctypes.c_int * 5)()
+    assert lib.paged_gqa_plan(7, 8, 128, 152, 4, 1, 32, 0, 0, out) == _lib.PGD_ERR_DTYPE
