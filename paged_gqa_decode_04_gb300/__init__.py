@@ -133,6 +133,24 @@ def alloc_workspace(pool, B, Hq, num_splits=0):
     return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=pool.k_pool.device)
 
 
+def _check_decode_args(pool, q, block_table, seq_lens, q_dims):
+    """Shapes, dtypes and placement of a decode call's tensors (q has q_dims
+    dimensions: [B, Hq, D] or [B, q_len, Hq, D])."""
+    if q.dim() != q_dims or block_table.dim() != 2 or seq_lens.dim() != 1:
+        raise ValueError("q must be [B,%sHq,D], block_table [B,max_blocks], seq_lens [B]"
+                         % ("q_len," if q_dims == 4 else ""))
+    if q.dtype != pool.q_dtype:
+        raise TypeError("q must be %s for this pool" % pool.q_dtype)
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    if (q.shape[-1] != pool.head_dim or block_table.shape[0] != q.shape[0] or
+            seq_lens.shape[0] != q.shape[0]):
+        raise ValueError("shape mismatch between q, tables and pool")
+    for t in (q, block_table, seq_lens):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+
+
 def paged_gqa_decode(pool, q, block_table, seq_lens, scale, out=None, workspace=None,
                      num_splits=0, stream=None):
     """Enqueue one decode step; returns `out` ([B, Hq, D], q's dtype).
@@ -142,18 +160,8 @@ def paged_gqa_decode(pool, q, block_table, seq_lens, scale, out=None, workspace=
     error; device-side errors are reported by paged_gqa_get_error.
     """
     lib = _lib.load()
-    if q.dim() != 3 or block_table.dim() != 2 or seq_lens.dim() != 1:
-        raise ValueError("q must be [B,Hq,D], block_table [B,max_blocks], seq_lens [B]")
-    if q.dtype != pool.q_dtype:
-        raise TypeError("q must be %s for this pool" % pool.q_dtype)
-    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
-        raise TypeError("block_table and seq_lens must be int32")
-    for t in (q, block_table, seq_lens):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("inputs must be contiguous CUDA tensors")
+    _check_decode_args(pool, q, block_table, seq_lens, 3)
     B, Hq, D = q.shape
-    if D != pool.head_dim or block_table.shape[0] != B or seq_lens.shape[0] != B:
-        raise ValueError("shape mismatch between q, tables and pool")
     if out is None:
         out = torch.empty_like(q)
     if workspace is None:
@@ -182,18 +190,8 @@ def paged_gqa_decode_ex(pool, q, block_table, seq_lens, scale, window=0, out=Non
     `window` most recent ones when window > 0.  Returns out [B, q_len, Hq, D].
     """
     lib = _lib.load()
-    if q.dim() != 4 or block_table.dim() != 2 or seq_lens.dim() != 1:
-        raise ValueError("q must be [B,q_len,Hq,D], block_table [B,max_blocks], seq_lens [B]")
-    if q.dtype != pool.q_dtype:
-        raise TypeError("q must be %s for this pool" % pool.q_dtype)
-    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
-        raise TypeError("block_table and seq_lens must be int32")
-    for t in (q, block_table, seq_lens):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("inputs must be contiguous CUDA tensors")
+    _check_decode_args(pool, q, block_table, seq_lens, 4)
     B, q_len, Hq, D = q.shape
-    if D != pool.head_dim or block_table.shape[0] != B or seq_lens.shape[0] != B:
-        raise ValueError("shape mismatch between q, tables and pool")
     if out is None:
         out = torch.empty_like(q)
     if workspace is None:
@@ -218,6 +216,10 @@ def paged_gqa_decode_noalloc(pool, q, block_table, seq_lens, scale, out, num_spl
     PGD_ERR_TOO_LARGE when the request needs more scratch than the array holds.
     """
     lib = _lib.load()
+    _check_decode_args(pool, q, block_table, seq_lens, 3)
+    if (not isinstance(out, torch.Tensor) or out.shape != q.shape or out.dtype != q.dtype or
+            not out.is_cuda or not out.is_contiguous()):
+        raise ValueError("out must be a contiguous CUDA tensor shaped and typed like q")
     B, Hq, _ = q.shape
     _check(lib.paged_gqa_decode_noalloc(pool.handle, q.data_ptr(), B, Hq, block_table.data_ptr(),
                                         block_table.shape[1], seq_lens.data_ptr(), float(scale),

@@ -88,3 +88,36 @@ def test_fp8_pool_create_rejects(lib):
     assert lib.paged_kv_pool_create_fp8(ctypes.byref(h), 256, 256, 258, 256, 10, 16, 8,
                                         128) == _lib.PGD_ERR_ALIGN
     assert h.value is None
+
+
+def test_binding_checks_decode_arguments_before_the_library():
+    """The Python face rejects malformed tensors before any call into the
+    library: wrong ranks, dtypes, shapes, then anything not a contiguous CUDA
+    tensor (checked on CPU tensors here, so that last check is what passes)."""
+    import types
+
+    import torch
+
+    import paged_gqa_decode_04_gb300 as pgd
+
+    pool = types.SimpleNamespace(q_dtype=torch.bfloat16, head_dim=128)
+    q = torch.zeros(2, 8, 128, dtype=torch.bfloat16)
+    bt = torch.zeros(2, 4, dtype=torch.int32)
+    sl = torch.zeros(2, dtype=torch.int32)
+    check = pgd._check_decode_args
+    with pytest.raises(ValueError, match="q must be"):
+        check(pool, q.unsqueeze(1), bt, sl, 3)
+    with pytest.raises(ValueError, match="q must be"):
+        check(pool, q, bt, sl, 4)
+    with pytest.raises(TypeError, match="q must be"):
+        check(pool, q.float(), bt, sl, 3)
+    with pytest.raises(TypeError, match="int32"):
+        check(pool, q, bt.long(), sl, 3)
+    with pytest.raises(ValueError, match="shape mismatch"):
+        check(pool, q[..., :64], bt, sl, 3)
+    with pytest.raises(ValueError, match="shape mismatch"):
+        check(pool, q, bt[:1], sl, 3)
+    with pytest.raises(ValueError, match="CUDA"):
+        check(pool, q, bt, sl, 3)
+    with pytest.raises(ValueError, match="CUDA"):
+        check(pool, q.unsqueeze(1).expand(2, 3, 8, 128), bt, sl, 4)

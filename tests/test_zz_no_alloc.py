@@ -55,6 +55,13 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
         # The first call on a device may map the library's static array (module
         # loading); the second call takes no device memory at all.
         assert taken[1] == 0
+        # the Python face gives the same bytes, and checks `out` before the call
+        again = pgd.paged_gqa_decode_noalloc(pool, w.q, w.block_table, w.seq_lens, w.scale,
+                                             out=torch.empty_like(w.q))
+        assert torch.equal(again, outs[1])
+        with pytest.raises(ValueError):
+            pgd.paged_gqa_decode_noalloc(pool, w.q, w.block_table, w.seq_lens, w.scale,
+                                         out=torch.empty_like(w.q)[:1])
         # a request beyond the fixed scratch is refused before anything runs
         big = torch.zeros_like(w.q)
         rc = _noalloc(lib, pool, w, big, 1 << 20, stream)
