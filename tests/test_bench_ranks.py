@@ -68,3 +68,35 @@ def test_reference_arm_reports_its_core_count():
                                     check=True, cwd=root).stdout.strip().splitlines()[-1])
     assert one["impl"] == "reference" and one["cpu_baseline"]["cores"] == 1
     assert "1 host core" in one["cpu_baseline"]["sample"] and one["value"] > 0
+
+
+def test_kernel_hash_tracks_code_not_comments(tmp_path):
+    """The committed DRAM-traffic counters are reported only while the decode
+    kernel's code is the code they were taken on: an edit of comments or
+    whitespace keeps bench.kernel_hash(), any code edit changes it."""
+    import shutil
+
+    import bench
+
+    src = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                       "paged_gqa_decode_04_gb300", "csrc")
+    work = tmp_path / "csrc"
+    shutil.copytree(src, work)
+    base = bench.kernel_hash(str(work))
+    assert base == bench.kernel_hash(src)
+    cuh = work / "decode_tma.cuh"
+    text = cuh.read_text()
+    cuh.write_text("// a new comment line\n" + text.replace("\n\n", "\n\n\n", 3))
+    assert bench.kernel_hash(str(work)) == base
+    cuh.write_text(text.replace("kMinTilesPerCta = 2;", "kMinTilesPerCta = 3;"))
+    assert bench.kernel_hash(str(work)) != base
+    cuh.write_text(text)
+    (work / "partition.cuh").write_text((work / "partition.cuh").read_text() + "\nint x;\n")
+    assert bench.kernel_hash(str(work)) != base
+    # a string literal is code: a "//" inside one is not a comment
+    (work / "partition.cuh").write_text((work / "partition.cuh").read_text().replace(
+        "int x;", 'const char* s = "a // b";'))
+    h1 = bench.kernel_hash(str(work))
+    (work / "partition.cuh").write_text((work / "partition.cuh").read_text().replace(
+        '"a // b"', '"a // c"'))
+    assert bench.kernel_hash(str(work)) != h1
