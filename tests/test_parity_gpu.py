@@ -56,6 +56,13 @@ SMALL = {
                                        max_len=320)),
     "fp8_hkv2_g16": ("llama3_8b_fp8", dict(B=3, Hq=32, Hkv=2, lens=[90, 200, 17], max_len=256)),
     "fp8_hkv6": ("llama3_8b_fp8", dict(B=3, Hq=24, Hkv=6, lens=[90, 300, 17], max_len=320)),
+    "fp8_bs256": ("llama3_8b_fp8", dict(B=3, block_size=256, lens=[700, 256, 3], max_len=768)),
+    # an odd KV head count (one head per unit) with an odd group
+    "hkv5_g3": ("llama3_8b", dict(B=4, Hq=15, Hkv=5, lens=[333, 1, 48, 97], max_len=384)),
+    # lengths on and next to tile and block boundaries (16-token tiles and blocks)
+    "tile_edges": ("llama3_8b", dict(B=8, lens=[15, 16, 17, 31, 32, 33, 127, 128], max_len=160)),
+    "fp8_tile_edges": ("llama3_8b_fp8", dict(B=8, lens=[31, 32, 33, 63, 64, 65, 255, 256],
+                                             max_len=288)),
 }
 
 
