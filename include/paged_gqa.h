@@ -208,7 +208,9 @@ const char *paged_gqa_strerror(int status);
  * bytes (16 MiB) of static device memory in this library, reserved on every
  * device that loads it until the process exits.  Requests whose workspace
  * (paged_gqa_workspace_size) exceeds that return PGD_ERR_TOO_LARGE before
- * anything is enqueued.  Nothing is allocated: the first call on a device
+ * anything is enqueued, and so does every argument error (with the status
+ * paged_gqa_decode gives it): a refused call never touches the array.
+ * Nothing is allocated: the first call on a device
  * looks up the array's device address with that device made current (make
  * that first call before any stream capture), and every call clears the
  * array's counters with cudaMemsetAsync on `stream` before the kernel.
@@ -263,8 +265,10 @@ int paged_gqa_decode_host(pgd_pool_t pool, const void *h_q, int B, int q_len, in
  *            min(plan[3], ceil(tiles / 2)) of them, tiles counted from the
  *            lengths on the device
  *   plan[4]  split merge: 0 by the warp whose piece completes a run, 1 shared
- *            among all the run's pieces under a cooperative launch (the
- *            library falls back to 0 if the device refuses that launch), 2 by
+ *            among all the run's pieces under a cooperative launch (only
+ *            when the grid, one CTA per SM, fits at once: plan[3] <= num_sms;
+ *            should the device still refuse that launch, the library runs 0
+ *            instead), 2 by
  *            the completing warp through bulk copies into shared memory, 3 a
  *            separate merge kernel (float32 pools)
  * Returns the status paged_gqa_decode_ex returns for these shapes before any

@@ -44,21 +44,6 @@ def flops(lens, hq, d):
     return 4 * int(np.sum(lens)) * hq * d
 
 
-def contiguous_waste(reserved_tokens, generated_tokens):
-    """Slots left unused by a contiguous reservation of `reserved_tokens`."""
-    return max(0, reserved_tokens - generated_tokens)
-
-
-def paged_waste(length, block_size):
-    """Slots left unused in the last block of a paged sequence (< block_size)."""
-    return (-length) % block_size
-
-
-def flattened_tokens(lengths):
-    """Tokens of a batch packed with no padding."""
-    return int(np.sum(lengths))
-
-
 def tokens_read(L, q_len=1, window=0):
     """Cached tokens a call reads for one sequence: from the earliest token any
     of its q_len queries attends to (window W: max(0, L - q_len - W + 1)) to the

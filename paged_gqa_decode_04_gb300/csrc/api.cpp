@@ -39,16 +39,20 @@ struct DeviceGuard {
     }
 };
 
+PFN_cuTensorMapEncodeTiled_v12000 lookup_encode_fn() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return nullptr;
+}
+
+// The driver's tensor-map encoder, looked up once (a function-local static is
+// initialised once even when several threads create pools together).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = lookup_encode_fn();
     return fn;
 }
 
@@ -101,14 +105,6 @@ int choose_hg(const Pool& p, int rows) { return choose_hg_for(p.dtype, p.hkv, ro
 
 // The launch plan of a decode call, from shapes alone.  Status as the decode
 // entry points return it for these shapes.
-struct Plan {
-    int hg;             // KV heads per unit of work
-    int m_tiles;        // m16 row tiles of one head's query rows
-    int tile_tokens;    // tokens per tile
-    int parts;          // CTAs of the grid (spans of the tile sequence)
-    int merge_variant;  // 0 last arriver, 1 shared (cooperative), 2 staged, 3 separate kernel
-};
-
 static int make_plan(int dtype, int hkv, int d, int num_sms, int B, int q_len, int Hq,
                      int num_splits, int window, Plan* out) {
     if (hkv < 1 || Hq < 1 || B < 0 || q_len < 1 || num_sms < 1 || num_splits < 0 ||
@@ -136,6 +132,10 @@ static int make_plan(int dtype, int hkv, int d, int num_sms, int B, int q_len, i
         const int64_t loads = (int64_t)passes * (pl.parts / runs + 1);
         if (nr >= 2 && loads > kShareMinLoads) pl.merge_variant = 1;
         else if (nr >= 8 && loads > kStageMinLoads) pl.merge_variant = 2;
+        // the shared merge waits on other CTAs, so its grid must be resident
+        // at once; the TMA kernel's shared memory (over half an SM's) allows
+        // one CTA per SM, so a grid above the SM count takes the last arriver
+        if (pl.merge_variant == 1 && pl.parts > num_sms) pl.merge_variant = 0;
     }
     *out = pl;
     return PGD_OK;
@@ -151,6 +151,37 @@ WorkspaceLayout workspace_layout(int B, int hkv, int rows_per_head, int hg, int 
     w.part_o_off = w.part_lse_off + round_up((size_t)parts * 2 * rows * sizeof(float), 256);
     w.total = w.part_o_off + round_up((size_t)parts * 2 * rows * d * sizeof(float), 256);
     return w;
+}
+
+int check_decode(const Pool& p, const void* q, int B, int q_len, int Hq,
+                 const int32_t* block_table, int max_blocks, const int32_t* seq_lens, int window,
+                 float scale, const void* out, const void* workspace, size_t workspace_bytes,
+                 int num_splits, Plan* plan, WorkspaceLayout* wl) {
+    if (B < 0 || q_len < 1 || Hq < 1 || max_blocks < 0 || num_splits < 0 ||
+        num_splits > (1 << 20) || window < 0)
+        return PGD_ERR_ARG;
+    if (!isfinite(scale)) return PGD_ERR_ARG;
+    {
+        const int rc = make_plan(p.dtype, p.hkv, p.d, p.num_sms, B, q_len, Hq, num_splits,
+                                 window, plan);
+        if (rc != PGD_OK) return rc;
+    }
+    if ((int64_t)max_blocks * p.block_size > INT32_MAX) return PGD_ERR_SHAPE;
+    if (B == 0) return PGD_OK;
+    if (!q || !out || !block_table || !seq_lens || !workspace) return PGD_ERR_ARG;
+    if (max_blocks < 1) return PGD_ERR_SHAPE;
+    const size_t elt = p.dtype == PGD_F32 ? 4 : 2;  // q / out element (bf16 for 8-bit pages)
+    const size_t qbytes = (size_t)B * q_len * Hq * p.d * elt;
+    {
+        const uintptr_t q0 = reinterpret_cast<uintptr_t>(q), o0 = reinterpret_cast<uintptr_t>(out);
+        if (q0 < o0 + qbytes && o0 < q0 + qbytes) return PGD_ERR_ARG;  // out aliases q
+    }
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_table, 4) ||
+        !aligned(seq_lens, 4))
+        return PGD_ERR_ALIGN;
+    *wl = workspace_layout(B, p.hkv, q_len * (Hq / p.hkv), plan->hg, p.d, plan->parts);
+    if (!aligned(workspace, 256) || workspace_bytes < wl->total) return PGD_ERR_WORKSPACE;
+    return PGD_OK;
 }
 
 }  // namespace pgd
@@ -193,7 +224,7 @@ static int pool_create(pgd_pool_t* out, const void* k_pool, const void* v_pool,
     p.dtype = dtype;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
-    if (cudaGetDevice(&p.device) != cudaSuccess ||
+    if (cudaGetDevice(&p.device) != cudaSuccess || p.device >= kMaxDevices ||
         cudaDeviceGetAttribute(&p.num_sms, cudaDevAttrMultiProcessorCount, p.device) !=
             cudaSuccess ||
         cudaMalloc(reinterpret_cast<void**>(&p.err), sizeof(int)) != cudaSuccess) {
@@ -279,36 +310,20 @@ int paged_gqa_decode_ex(pgd_pool_t pool, const void* q, int B, int q_len, int Hq
                         const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
                         int window, float scale, void* out, void* workspace,
                         size_t workspace_bytes, int num_splits, void* stream) {
-    if (!pool || B < 0 || q_len < 1 || Hq < 1 || max_blocks < 0 || num_splits < 0 ||
-        num_splits > (1 << 20) || window < 0)
-        return PGD_ERR_ARG;
-    if (!isfinite(scale)) return PGD_ERR_ARG;
+    if (!pool) return PGD_ERR_ARG;
     const Pool& p = pool->p;
     Plan plan;
+    WorkspaceLayout wl;
     {
-        const int rc = make_plan(p.dtype, p.hkv, p.d, p.num_sms, B, q_len, Hq, num_splits,
-                                 window, &plan);
+        const int rc = check_decode(p, q, B, q_len, Hq, block_table, max_blocks, seq_lens, window,
+                                    scale, out, workspace, workspace_bytes, num_splits, &plan,
+                                    &wl);
         if (rc != PGD_OK) return rc;
     }
-    const int G = Hq / p.hkv;
-    const int rows = q_len * G;
-    if ((int64_t)max_blocks * p.block_size > INT32_MAX) return PGD_ERR_SHAPE;
     if (B == 0) return PGD_OK;
-    if (!q || !out || !block_table || !seq_lens || !workspace) return PGD_ERR_ARG;
-    if (max_blocks < 1) return PGD_ERR_SHAPE;
-    const size_t elt = p.dtype == PGD_F32 ? 4 : 2;  // q / out element (bf16 for 8-bit pages)
-    const size_t qbytes = (size_t)B * q_len * Hq * p.d * elt;
-    {
-        const uintptr_t q0 = reinterpret_cast<uintptr_t>(q), o0 = reinterpret_cast<uintptr_t>(out);
-        if (q0 < o0 + qbytes && o0 < q0 + qbytes) return PGD_ERR_ARG;  // out aliases q
-    }
-    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_table, 4) ||
-        !aligned(seq_lens, 4))
-        return PGD_ERR_ALIGN;
+    const int G = Hq / p.hkv;
     const int parts = plan.parts;
     const int hg = plan.hg;
-    const WorkspaceLayout wl = workspace_layout(B, p.hkv, rows, hg, p.d, parts);
-    if (!aligned(workspace, 256) || workspace_bytes < wl.total) return PGD_ERR_WORKSPACE;
 
     DeviceGuard g(p.device);
     if (!g.ok) return PGD_ERR_CUDA;

@@ -57,6 +57,9 @@
 #include <limits.h>
 #include <math.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "partition.cuh"
 
 namespace pgd {
@@ -113,6 +116,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
         if (global_ns() - t0 > limit_ns) return false;
     }
     return true;
+}
+
+// The same wait taken by a whole warp: every lane waits (so every lane sees
+// the phase complete), then the warp takes one decision.  Without the vote,
+// lanes near the limit could decide differently and the ones that went on
+// would meet the warp's next shuffle or mma without the others.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -471,7 +482,7 @@ __device__ __forceinline__ int merge_staged(const DecodeArgs& a, int64_t t0, int
             lse_base[i] = __ldcg(a.part_lse + slot_of(k) * piece_rows + hgi * rows + rb + r);
         }
         __syncwarp();
-        if (!mbar_wait(bar, phase)) return -1;
+        if (!mbar_wait_warp(bar, phase)) return -1;
         phase ^= 1u;
         for (int r = rp; r < cnt; r += RPP) {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -609,14 +620,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const int flags =
                 segment_flags(x, cur.run_start, cur.n_b, r0, r1) | (bad ? kTileBad : 0);
 
-            if (!mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1u)) {
+            if (!mbar_wait_warp(smem_u32(&empty_bar[s]), ph ^ 1u)) {
                 if (lane == 0) {
                     latch_error(a.err, PGD_ERR_TIMEOUT);
                     aborted = 1;
                 }
                 break;
             }
-            if (aborted) break;
+            if (__any_sync(0xffffffffu, aborted)) break;
             const uint32_t fb = smem_u32(&full_bar[s]);
             if (lane == 0) {
                 desc[s] = StageDesc{cur.run_start, cur.b, cur.unit, n_valid, flags, cur.n_b,
@@ -728,14 +739,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     for (int it = 0; it < n_tiles; ++it) {
         const int s = it % S;
         const uint32_t ph = (uint32_t)(it / S) & 1u;
-        if (!mbar_wait(smem_u32(&full_bar[s]), ph)) {
+        if (!mbar_wait_warp(smem_u32(&full_bar[s]), ph)) {
             if (lane == 0) {
                 latch_error(a.err, PGD_ERR_TIMEOUT);
                 aborted = 1;
             }
             break;
         }
-        if (aborted) break;
+        if (__any_sync(0xffffffffu, aborted)) break;
         const StageDesc dsc = desc[s];
         uint8_t* st = stage_base + s * C::STAGE_BYTES;
         const uint32_t k_u = smem_u32(st);
@@ -989,7 +1000,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
             }
             mbar_arrive(smem_u32(&comb_bar));
-            if (!mbar_wait(smem_u32(&comb_bar), comb_phase)) {
+            if (!mbar_wait_warp(smem_u32(&comb_bar), comb_phase)) {
                 if (lane == 0) {
                     latch_error(a.err, PGD_ERR_TIMEOUT);
                     aborted = 1;
@@ -1033,7 +1044,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
             }
             mbar_arrive(smem_u32(&comb_bar));
-            if (!mbar_wait(smem_u32(&comb_bar), comb_phase)) {
+            if (!mbar_wait_warp(smem_u32(&comb_bar), comb_phase)) {
                 if (lane == 0) {
                     latch_error(a.err, PGD_ERR_TIMEOUT);
                     aborted = 1;
@@ -1168,8 +1179,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
     }
     // ---- merge the split runs recorded above
-    __syncwarp();
-    if (aborted) return;
+    if (__any_sync(0xffffffffu, aborted)) return;
     constexpr int RPP = 32 / (D / 4);  // rows per merge pass
     const int r_mine = mt * 16, r_end = min(rows, r_mine + C::ROWS);
     uint32_t mphase = 0;
@@ -1178,7 +1188,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // and been read): from here each merging warp owns a slice of it
         fence_proxy_async();
         mbar_arrive(smem_u32(&comb_bar));
-        if (!mbar_wait(smem_u32(&comb_bar), comb_phase)) {
+        if (!mbar_wait_warp(smem_u32(&comb_bar), comb_phase)) {
             if (lane == 0) latch_error(a.err, PGD_ERR_TIMEOUT);
             return;
         }
@@ -1227,21 +1237,46 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
 }
 
+// Co-resident CTAs per SM of one instantiation on `dev` (the current device),
+// after setting its dynamic shared memory limit there.  The attribute applies
+// to the current device only, so both are kept per device; the first launch
+// on a device does the set-up under a lock (two host threads may make their
+// first launch together), later ones read one atomic.  0 on failure.
+template <class C>
+int resident_per_sm(int dev, cudaError_t* err) {
+    static std::atomic<int> per_sm[kMaxDevices] = {};
+    static std::mutex mu;
+    *err = cudaSuccess;
+    if (dev < 0 || dev >= kMaxDevices) {
+        *err = cudaErrorInvalidDevice;
+        return 0;
+    }
+    int n = per_sm[dev].load(std::memory_order_acquire);
+    if (n > 0) return n;
+    std::lock_guard<std::mutex> lock(mu);
+    n = per_sm[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    cudaError_t e = cudaFuncSetAttribute(decode_tma_kernel<C>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_tma_kernel<C>, C::THREADS,
+                                                          C::SMEM_BYTES);
+    if (e == cudaSuccess && n < 1) e = cudaErrorLaunchOutOfResources;
+    if (e != cudaSuccess) {
+        *err = e;
+        return 0;
+    }
+    per_sm[dev].store(n, std::memory_order_release);
+    return n;
+}
+
 template <class C>
 cudaError_t launch_cfg(const DecodeArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
-                       int num_sms, cudaStream_t s) {
-    static bool attr_done = false;  // per instantiation; a repeated set is harmless
-    static int per_sm = 0;          // co-resident CTAs per SM
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(decode_tma_kernel<C>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_tma_kernel<C>,
-                                                          C::THREADS, C::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+                       int num_sms, int dev, cudaStream_t s) {
+    cudaError_t e0;
+    const int per_sm = resident_per_sm<C>(dev, &e0);
+    if (per_sm < 1) return e0;
     if constexpr (C::SHARE) {
         // the shared merge waits on other CTAs: only a grid resident at once,
         // launched cooperatively
@@ -1277,7 +1312,7 @@ cudaError_t launch_hg(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
     constexpr int TG = token_groups((FP8 ? 256 : 128) / HG, HG, MT);
     const int idx = HG == 1 ? 0 : HG == 2 ? 1 : HG == 4 ? 2 : 3;
     return launch_cfg<Cfg<D, HG, MT, TG, R16, FP8, MV>>(a, p.tmap_k[idx], p.tmap_v[idx],
-                                                          p.num_sms, s);
+                                                          p.num_sms, p.device, s);
 }
 
 template <int D, int MT, bool R16, bool FP8, int MV>

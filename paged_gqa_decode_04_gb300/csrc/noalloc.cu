@@ -30,7 +30,6 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
@@ -72,15 +71,16 @@ extern "C" int paged_gqa_decode_noalloc(pgd_pool_t pool, const void* q, int B, i
     const int dev = p.device;
     unsigned char* scratch = static_cast<unsigned char*>(pgd::scratch_on(dev));
     if (!scratch) return PGD_ERR_CUDA;
+    // Every argument check before anything is enqueued: a refused call must
+    // not touch the shared array, which another call may be using.
+    pgd::Plan plan;
+    pgd::WorkspaceLayout wl;
+    rc = pgd::check_decode(p, q, B, 1, Hq, block_table, max_blocks, seq_lens, 0, scale, out,
+                           scratch, pgd::kNoAllocScratchBytes, num_splits, &plan, &wl);
+    if (rc != PGD_OK) return rc;
 
     // The array keeps whatever the previous call left; only the counters must
     // start at zero.
-    int parts = 0;
-    if (paged_gqa_auto_splits(pool, &parts) != PGD_OK) return PGD_ERR_ARG;
-    if (num_splits > 0) parts = num_splits;
-    const int rows = Hq / p.hkv;  // one query token per sequence
-    const pgd::WorkspaceLayout wl =
-        pgd::workspace_layout(B, p.hkv, rows, pgd::choose_hg(p, rows), p.d, parts);
     int prev = -1;
     if (cudaGetDevice(&prev) != cudaSuccess) return PGD_ERR_CUDA;
     if (prev != dev && cudaSetDevice(dev) != cudaSuccess) return PGD_ERR_CUDA;

@@ -9,6 +9,10 @@
 
 namespace pgd {
 
+// Devices a process may use this library on (per-device state is kept in
+// arrays of this size; pools on a device ordinal at or above it are refused).
+constexpr int kMaxDevices = 64;
+
 // Tokens per tile of the CUDA-core kernel (the TMA kernel uses 128 / HG).
 constexpr int kSimpleTileTokens = 64;
 
@@ -82,12 +86,30 @@ struct DecodeArgs {
     float* part_lse;       // [num_parts][2][hg * group]    partial log2-sum-exp
 };
 
+// The launch plan of a decode call, from shapes alone.
+struct Plan {
+    int hg;             // KV heads per unit of work
+    int m_tiles;        // m16 row tiles of one head's query rows
+    int tile_tokens;    // tokens per tile
+    int parts;          // CTAs of the grid (spans of the tile sequence)
+    int merge_variant;  // 0 last arriver, 1 shared (cooperative), 2 staged, 3 separate kernel
+};
+
 // Workspace layout for (B, G, D, parts); returns total bytes and fills offsets.
 struct WorkspaceLayout {
     size_t counters_off, tile_base_off, part_lse_off, part_o_off, total;
 };
 // `rows` = query rows per KV head: q_len * G.
 WorkspaceLayout workspace_layout(int B, int hkv, int rows, int hg, int d, int parts);
+
+// Every argument check of a decode call (paged_gqa_decode_ex's contract), in
+// the order the entry points apply them; fills the plan and, for B > 0, the
+// workspace layout.  PGD_OK, or the status the call returns before anything
+// is enqueued.
+int check_decode(const Pool& p, const void* q, int B, int q_len, int Hq,
+                 const int32_t* block_table, int max_blocks, const int32_t* seq_lens, int window,
+                 float scale, const void* out, const void* workspace, size_t workspace_bytes,
+                 int num_splits, Plan* plan, WorkspaceLayout* wl);
 
 // KV heads per unit of work for this pool and rows per KV head.
 int choose_hg(const Pool& p, int rows);

@@ -40,6 +40,14 @@ CASES = [
     ("float32 tiny", (F32, 2, 64, 4, 8), {}, (1, 1, 64, 152, "merge kernel")),
     ("explicit splits", (BF16, 8, 128, 64, 32), dict(num_splits=500),
      (8, 1, 16, 500, "last arriver")),
+    # the shared merge needs its grid resident at once (one CTA per SM): a
+    # split count above the SM count takes the last arriver instead
+    ("long_70b, 152 splits", (BF16, 8, 128, 8, 64), dict(num_splits=152),
+     (8, 1, 16, 152, "shared (cooperative)")),
+    ("long_70b, 153 splits", (BF16, 8, 128, 8, 64), dict(num_splits=153),
+     (8, 1, 16, 153, "last arriver")),
+    ("mqa B 1, 1000 splits", (BF16, 1, 128, 1, 40), dict(num_splits=1000),
+     (1, 3, 128, 1000, "last arriver")),
 ]
 
 
