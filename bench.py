@@ -14,8 +14,11 @@ from Python instead).  Rank 0 prints one JSON line.
 
 --impl reference times the float64 CPU oracle on the host cores instead (the
 comparison arm), over the same workload.
-Multi-GPU (torchrun): every rank runs its own replica of the workload (seed +
-rank), no data-path collective; value = all ranks' bytes / max time.
+Multi-GPU: every rank runs its own replica of the workload (seed + rank), no
+data-path collective; value = all ranks' bytes / max time.  `--gpus N` with
+N > 1 outside a launcher re-launches this script under torch.distributed.run
+with N processes on this node (127.0.0.1); under a launcher the world size
+must equal N.
 """
 import argparse
 import hashlib
@@ -173,6 +176,33 @@ def dist_setup():
     return world, rank, local
 
 
+def free_port():
+    import socket
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def relaunch_cmd(argv, gpus, port):
+    """This script under torch.distributed.run: `gpus` ranks on this node."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+            "--nproc-per-node", str(gpus), "--master-addr", "127.0.0.1",
+            "--master-port", str(port), os.path.abspath(__file__)] + list(argv)
+
+
+def gather_over_ranks(x, world, device):
+    """Every rank's value of x, in rank order (on every rank)."""
+    if world == 1:
+        return [x]
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    parts = [torch.zeros_like(t) for _ in range(world)]
+    dist.all_gather(parts, t)
+    return [float(p.item()) for p in parts]
+
+
 def max_over_ranks(x, world, device):
     if world == 1:
         return x
@@ -193,6 +223,33 @@ def whole_job_gbs(nbytes, t_ms, world):
     return world * nbytes / (t_ms * 1e-3) / 1e9
 
 
+def cold_median_ms(step, stream, dev, reps=50):
+    """Median device time of `reps` single launches of `step`, each preceded by
+    a read of a buffer twice the L2 size, so that the launch finds none of its
+    inputs in L2 (a read rather than a write: a written buffer would leave L2
+    full of dirty lines whose write-back the timed launch would pay for);
+    events bracket the launch alone."""
+    if reps <= 0:
+        return None
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size or (126 << 20)
+    flush = torch.ones(2 * l2 // 4, dtype=torch.int32, device=dev)
+    acc = torch.zeros((), dtype=torch.int64, device=dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for e0, e1 in evs:
+            acc += flush.sum()
+            e0.record(stream)
+            step()
+            e1.record(stream)
+    torch.cuda.synchronize()
+    if int(acc.item()) != reps * flush.numel():
+        raise RuntimeError("L2 flush read back a wrong sum")
+    times = [e0.elapsed_time(e1) for e0, e1 in evs]
+    del flush
+    return statistics.median(times)
+
+
 def launch_note(args):
     if args.launch == "graph":
         return "the %d timed steps captured as one CUDA graph, replayed once" % args.steps
@@ -206,14 +263,21 @@ def barrier(world):
         dist.barrier()
 
 
+def host_cores():
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def cpu_oracle_rate(w, budget_s, threads=0):
     """Run the oracle over the whole workload until `budget_s` has passed, on
     `threads` host cores (0: all); returns (GB/s over algorithmic bytes,
     sample, cores, sequences/s)."""
     import oracle
 
-    if threads > 0:
-        oracle.set_num_threads(threads)
+    oracle.set_num_threads(threads if threads > 0 else host_cores())
 
     q, k, v = gen.to_numpy_bits(w.q), gen.to_numpy_bits(w.k_pool), gen.to_numpy_bits(w.v_pool)
     elt, q_elt = accounting.ELT[w.dtype], accounting.Q_ELT[w.dtype]
@@ -245,8 +309,7 @@ def run_reference(args, world, rank):
     nbytes = accounting.algorithmic_bytes(w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt, q_elt)
     import oracle
 
-    if args.cpu_threads > 0:
-        oracle.set_num_threads(args.cpu_threads)
+    oracle.set_num_threads(args.cpu_threads if args.cpu_threads > 0 else host_cores())
     cores = oracle.num_threads()
     q, k, v = gen.to_numpy_bits(w.q), gen.to_numpy_bits(w.k_pool), gen.to_numpy_bits(w.v_pool)
     # One step = the oracle over a bounded sample: every sequence, a subset of
@@ -394,10 +457,15 @@ def run_ours(args, world, rank, local):
         barrier(world)
         torch.cuda.synchronize()
     t_ms = ev0.elapsed_time(ev1) / args.steps
-    t_ms = max_over_ranks(t_ms, world, dev)
+    rank_ms = gather_over_ranks(t_ms, world, dev)
+    t_ms = max(rank_ms)
     status = pgd.paged_gqa_get_error(pool, stream)
     if status != 0:
         raise RuntimeError("device error: %s" % pgd.strerror(status))
+    # L2-cold figure: single launches, each after a read of twice the L2 size
+    # on the same stream, events around the launch alone; median over 50
+    cold_ms = cold_median_ms(step, stream, dev, reps=args.cold_reps)
+    cold_ms = max_over_ranks(cold_ms, world, dev) if cold_ms is not None else None
 
     if args.op != "decode":
         if rank == 0:
@@ -412,6 +480,10 @@ def run_ours(args, world, rank, local):
                            "launch": launch_note(args), "algorithmic_bytes_per_step": nbytes},
                 "pct_of_peak": round(100 * gbs / world / peak, 2),
                 "peak_source": "%s (%.0f GB/s)" % (peak_src, peak),
+                "per_rank_ms_per_step": [round(x, 5) for x in rank_ms],
+                "cold_ms": round(cold_ms, 5) if cold_ms is not None else None,
+                "cold_pct_of_peak": (round(100 * nbytes / (cold_ms * 1e-3) / 1e9 / peak, 2)
+                                     if cold_ms is not None else None),
                 "clocks": clk.summary()}), flush=True)
         return
 
@@ -492,6 +564,7 @@ def run_ours(args, world, rank, local):
                      "frac": round(per_gpu / peak, 4), "traffic": ncu_traffic(args.config),
                      "note": "bf16 and 8-bit steps are one kernel launch (split-KV merge "
                              "fused), so achieved = algorithmic bytes / event-timed step"},
+        "per_rank_ms_per_step": [round(x, 5) for x in rank_ms],
         "e2e": {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
@@ -503,7 +576,15 @@ def run_ours(args, world, rank, local):
         "gpu_launches": args.steps * (2 if w.dtype == "f32" else 1),
         "clocks": clk.summary(),
     }
-    if not args.no_cpu_baseline:
+    if cold_ms is not None:
+        cold = nbytes / (cold_ms * 1e-3) / 1e9
+        line["roofline"].update({
+            "cold_ms": round(cold_ms, 5), "cold_achieved": round(cold, 2),
+            "cold_frac": round(cold / peak, 4),
+            "cold_note": "median of %d single launches, each after a read of a buffer "
+                         "twice the L2 size on the same stream; events around the launch alone"
+                         % args.cold_reps})
+    if not args.no_cpu_baseline and world == 1:
         rate, sample, cores, _ = cpu_oracle_rate(w, args.cpu_seconds, args.cpu_threads)
         line["cpu_baseline"] = {"value": round(rate, 4), "unit": "GB/s", "cores": cores,
                                 "kind": "oracle", "sample": sample}
@@ -530,12 +611,23 @@ def main():
     ap.add_argument("--launch", default="graph", choices=["graph", "stream"],
                     help="timed steps replayed as one CUDA graph (default) or launched one "
                          "by one from Python")
+    ap.add_argument("--cold-reps", type=int, default=50,
+                    help="single launches after an L2 flush for the cold figure (0: skip)")
     ap.add_argument("--profile", action="store_true",
                     help="only W + K step launches (for ncu); prints no bench line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # no launcher: start one rank per GPU of this node under torch.distributed.run
+        sys.exit(subprocess.call(relaunch_cmd(sys.argv[1:], args.gpus, free_port())))
     world, rank, local = dist_setup()
+    if world != args.gpus:
+        print("bench.py: --gpus %d but the launcher started %d rank(s)" % (args.gpus, world),
+              file=sys.stderr)
+        sys.exit(2)
     if args.impl == "reference":
         run_reference(args, world, rank)
     else:

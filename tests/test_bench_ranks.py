@@ -48,6 +48,55 @@ def test_two_gloo_ranks(tmp_path):
     assert rows[0][2] != rows[1][2]                       # hence distinct workloads
 
 
+@pytest.mark.timeout(300)
+def test_gpus_flag_starts_that_many_ranks():
+    """`bench.py --gpus 2` outside a launcher starts two ranks under
+    torch.distributed.run (gloo on CPU); the reference arm's rank 0 prints the
+    one JSON line, with n_gpus 2, and the other rank exits without work."""
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    res = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2",
+                          "--impl", "reference", "--config", "tiny", "--steps", "3",
+                          "--warmup", "3", "--cpu-threads", "1"],
+                         capture_output=True, text=True, cwd=root, env=env, timeout=280)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [json.loads(x) for x in res.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1, res.stdout
+    assert lines[0]["impl"] == "reference" and lines[0]["n_gpus"] == 2
+
+
+def test_gpus_flag_must_match_the_launcher():
+    """Under a launcher that started one rank, `--gpus 2` is refused instead of
+    printing a one-GPU line as if it were two."""
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    res = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2",
+                          "--impl", "reference", "--config", "tiny", "--steps", "3",
+                          "--warmup", "3"], capture_output=True, text=True, cwd=root, env=env,
+                         timeout=120)
+    assert res.returncode == 2 and "--gpus 2" in res.stderr
+    assert not res.stdout.strip()
+
+
+def test_relaunch_command():
+    import bench
+
+    cmd = bench.relaunch_cmd(["--gpus", "4", "--steps", "9"], 4, 29555)
+    i = cmd.index("torch.distributed.run")
+    assert cmd[i - 1] == "-m" and cmd[cmd.index("--nproc-per-node") + 1] == "4"
+    assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1"
+    assert cmd[cmd.index("--master-port") + 1] == "29555"
+    assert cmd[-4:] == ["--gpus", "4", "--steps", "9"] and cmd[-5].endswith("bench.py")
+
+
 def test_whole_job_value():
     import bench
 

@@ -45,7 +45,8 @@ def test_noalloc_matches_oracle_and_workspace_entry_point_on_two_calls(page):
     lib = _lib.load()
     spec = dict(CASES[page])
     w = gen.make(spec.pop("name"), device="cuda", poison=True, **spec)
-    want = run_oracle(w)
+    want, rc = run_oracle(w)
+    assert rc == 0
     tmax, tmean = tol(w.dtype)
     stream = torch.cuda.current_stream()
     pool = pgd.PagedKVPool(w.k_pool, w.v_pool, w.k_scale, w.v_scale)
