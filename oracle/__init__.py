@@ -17,6 +17,8 @@ from . import build as _build
 
 F32 = 0
 BF16 = 1
+FP8_E4M3 = 2
+INT8 = 3
 STATUS = {0: "ok", 1: "bad arguments", 2: "block id out of range", 3: "sequence length out of range"}
 
 
@@ -67,6 +69,13 @@ class Oracle:
                                               [ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_double, ctypes.c_void_p])
         lib.oracle_decode_kv8_f64.restype = ctypes.c_int
+        lib.oracle_decode_q8_f64.argtypes = ([ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                              ctypes.c_void_p] + [ctypes.c_int] * 6 +
+                                             [ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_double, ctypes.c_void_p])
+        lib.oracle_decode_q8_f64.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
@@ -168,6 +177,53 @@ class Oracle:
             raise ValueError("oracle rejected the arguments")
         return (out[:, 0] if squeeze else out), int(rc)
 
+    def decode_q8_f64(self, q, k8, v8, code, k_scale, v_scale, block_table, seq_lens, scale,
+                      window=0):
+        """8-bit K/V pages of `code` "e4m3" or "int8" (signed).  k_scale /
+        v_scale float32 [Hkv] (one scale per KV head) or [num_blocks, Hkv] (one
+        per physical block and KV head).  q is [B, q_len, Hq, D] (or [B, Hq,
+        D]) float32 or bfloat16 bits.  Returns (out with q's shape, float64;
+        status)."""
+        q = np.ascontiguousarray(q)
+        squeeze = q.ndim == 3
+        if squeeze:
+            q = q[:, None]
+        if q.dtype == np.float32:
+            q_dtype = F32
+        elif q.dtype == np.uint16:
+            q_dtype = BF16
+        else:
+            raise TypeError("q must be float32 or bfloat16 bits")
+        codes = {"e4m3": FP8_E4M3, "int8": INT8}
+        if code not in codes:
+            raise ValueError("code must be 'e4m3' or 'int8'")
+        k8 = np.ascontiguousarray(k8).view(np.uint8)
+        v8 = np.ascontiguousarray(v8).view(np.uint8)
+        ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+        vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        B, q_len, Hq, D = q.shape
+        nb, bs, Hkv, D2 = k8.shape
+        if ks.shape == (Hkv,) and vs.shape == (Hkv,):
+            per_block = 0
+        elif ks.shape == (nb, Hkv) and vs.shape == (nb, Hkv):
+            per_block = 1
+        else:
+            raise ValueError("scales must be [Hkv] or [num_blocks, Hkv]")
+        if D2 != D or v8.shape != k8.shape:
+            raise ValueError("shape mismatch")
+        out = np.empty((B, q_len, Hq, D), dtype=np.float64)
+        rc = self.lib.oracle_decode_q8_f64(q.ctypes.data, q_dtype, k8.ctypes.data,
+                                           v8.ctypes.data, codes[code], ks.ctypes.data,
+                                           vs.ctypes.data, per_block, bt.ctypes.data,
+                                           sl.ctypes.data, B, q_len, Hq, Hkv, D, bs, nb,
+                                           bt.shape[1], int(window), float(scale),
+                                           out.ctypes.data)
+        if rc == 1:
+            raise ValueError("oracle rejected the arguments")
+        return (out[:, 0] if squeeze else out), int(rc)
+
 
 _default = None
 
@@ -199,6 +255,11 @@ def decode_ex_f64(q, k_pool, v_pool, block_table, seq_lens, scale, window=0):
 def decode_kv8_f64(q, k8, v8, k_scale, v_scale, block_table, seq_lens, scale, window=0):
     return default().decode_kv8_f64(q, k8, v8, k_scale, v_scale, block_table, seq_lens, scale,
                                     window)
+
+
+def decode_q8_f64(q, k8, v8, code, k_scale, v_scale, block_table, seq_lens, scale, window=0):
+    return default().decode_q8_f64(q, k8, v8, code, k_scale, v_scale, block_table, seq_lens,
+                                   scale, window)
 
 
 def decode_rows_f64(q, k_pool, v_pool, block_table, seq_lens, scale, rows):

@@ -103,3 +103,27 @@ def brute_decode_kv8(q, k8, v8, k_scale, v_scale, block_table, seq_lens, scale, 
     if q.ndim == 3:
         return brute_decode_ex(q[:, None], k, v, block_table, seq_lens, scale, window)[:, 0]
     return brute_decode_ex(q, k, v, block_table, seq_lens, scale, window)
+
+
+def int8_to_f64(bits):
+    """uint8 bytes read as two's-complement int8 codes -> float64."""
+    return np.ascontiguousarray(bits, dtype=np.uint8).view(np.int8).astype(np.float64)
+
+
+def brute_decode_q8(q, k8, v8, code, k_scale, v_scale, block_table, seq_lens, scale,
+                    window=0):
+    """Dequantise 8-bit pages (value = scale x code value; the scale per KV
+    head [Hkv] or per physical block and KV head [num_blocks, Hkv]) into
+    dense float64 pools and run the dense masked formulation."""
+    dec = e4m3_to_f64 if code == "e4m3" else int8_to_f64
+    ks = np.asarray(k_scale, dtype=np.float64)
+    vs = np.asarray(v_scale, dtype=np.float64)
+    # broadcast the scales over [num_blocks, bs, Hkv, D]
+    ks = ks[None, None, :, None] if ks.ndim == 1 else ks[:, None, :, None]
+    vs = vs[None, None, :, None] if vs.ndim == 1 else vs[:, None, :, None]
+    k = dec(k8) * ks
+    v = dec(v8) * vs
+    q = np.asarray(q)
+    if q.ndim == 3:
+        return brute_decode_ex(q[:, None], k, v, block_table, seq_lens, scale, window)[:, 0]
+    return brute_decode_ex(q, k, v, block_table, seq_lens, scale, window)

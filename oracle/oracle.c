@@ -39,6 +39,14 @@
  * Inference ...", section 7.1); local attention restricts each token to the
  * most recent K tokens (same notes, section 4.4 "Local Attention").
  *
+ * Extension (oracle_decode_q8_f64): quantized K/V pages holding 8-bit codes,
+ * e4m3 floats or signed int8 integers, each standing for a scale times its
+ * value; one scale per KV head, or one per physical block and KV head (the
+ * scale of a token is the one of the block it is stored in).  Passages: int8
+ * and fp8 quantization ("Modern LLM Inference ...", section 6) and KV cache
+ * compression ("The Ultimate Guide ... Part 2", section "KV Cache
+ * Compression").
+ *
  * Readings where the pages are silent:
  *   - seq_lens[b] counts the cached tokens; the single decode query attends to
  *     all of them (no causal mask for one query token).
@@ -64,7 +72,7 @@
 #include <omp.h>
 #endif
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_FP8_E4M3 = 2 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_FP8_E4M3 = 2, ORACLE_INT8 = 3 };
 enum { ORACLE_OK = 0, ORACLE_ERR_ARG = 1, ORACLE_ERR_BLOCK_ID = 2, ORACLE_ERR_SEQ_LEN = 3 };
 
 /*
@@ -85,7 +93,8 @@ static double e4m3_value(uint8_t v)
     return sign ? -x : x;
 }
 
-/* Exact widening of element `idx` of a float32, bfloat16 or e4m3 array. */
+/* Exact widening of element `idx` of a float32, bfloat16, e4m3 or int8 array
+ * (an int8 code is a two's-complement integer in [-128, 127]). */
 static double load_elem(const void *base, int64_t idx, int dtype)
 {
     if (dtype == ORACLE_F32) {
@@ -93,6 +102,9 @@ static double load_elem(const void *base, int64_t idx, int dtype)
     }
     if (dtype == ORACLE_FP8_E4M3) {
         return e4m3_value(((const uint8_t *)base)[idx]);
+    }
+    if (dtype == ORACLE_INT8) {
+        return (double)((const int8_t *)base)[idx];
     }
     uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
     float f;
@@ -107,9 +119,15 @@ static double load_elem(const void *base, int64_t idx, int dtype)
  * [lo, p], lo = max(0, p - window + 1) when window > 0, else 0 (causal, and
  * local attention keeps only the most recent `window` tokens).  An empty range
  * gives zeros.  Returns a status.
+ *
+ * Quantized pages: a stored K (V) element stands for a scale times its code
+ * value.  Without scale arrays the scale is 1; with scale_per_block == 0 it
+ * is k_scale[kv] (one per KV head); with scale_per_block == 1 it is
+ * k_scale[phys * Hkv + kv], one per physical block and KV head, so tokens of
+ * one sequence in different blocks may carry different scales.
  */
 static int decode_row(const void *q, const void *k_pool, const void *v_pool,
-                      const float *k_scale, const float *v_scale,
+                      const float *k_scale, const float *v_scale, int scale_per_block,
                       const int32_t *block_table, const int32_t *seq_lens, int dtype,
                       int kv_dtype,
                       int q_len, int Hq, int Hkv, int D, int block_size, int64_t num_blocks,
@@ -118,9 +136,6 @@ static int decode_row(const void *q, const void *k_pool, const void *v_pool,
     const int G = Hq / Hkv;
     const int kv = h / G;
     const int64_t L = seq_lens[b];
-    /* a stored K/V element stands for scale[kv] times its value (1 without scales) */
-    const double ks = k_scale ? (double)k_scale[kv] : 1.0;
-    const double vs = v_scale ? (double)v_scale[kv] : 1.0;
     int d;
 
     if (L < 0 || L > (int64_t)max_blocks * block_size) {
@@ -134,12 +149,17 @@ static int decode_row(const void *q, const void *k_pool, const void *v_pool,
     const int64_t n = p - lo + 1;
     if (n <= 0) return ORACLE_OK;
 
-    /* Gather: physical (block, slot) of every attended token, checked first. */
+    /* Gather: physical (block, slot) of every attended token, checked first,
+     * and the K / V scales of that token's block. */
     int64_t *row_base = (int64_t *)malloc((size_t)n * sizeof(int64_t));
     double *s = (double *)malloc((size_t)n * sizeof(double));
-    if (!row_base || !s) {
+    double *ks = (double *)malloc((size_t)n * sizeof(double));
+    double *vs = (double *)malloc((size_t)n * sizeof(double));
+    if (!row_base || !s || !ks || !vs) {
         free(row_base);
         free(s);
+        free(ks);
+        free(vs);
         for (d = 0; d < D; ++d) out[d] = NAN;
         return ORACLE_ERR_ARG;
     }
@@ -150,11 +170,16 @@ static int decode_row(const void *q, const void *k_pool, const void *v_pool,
         if (phys < 0 || phys >= num_blocks) {
             free(row_base);
             free(s);
+            free(ks);
+            free(vs);
             for (d = 0; d < D; ++d) out[d] = NAN;
             return ORACLE_ERR_BLOCK_ID;
         }
         /* pool layout [num_blocks, block_size, Hkv, D] */
         row_base[t] = ((phys * block_size + slot) * Hkv + kv) * (int64_t)D;
+        const int64_t sc_idx = scale_per_block ? phys * Hkv + kv : kv;
+        ks[t] = k_scale ? (double)k_scale[sc_idx] : 1.0;
+        vs[t] = v_scale ? (double)v_scale[sc_idx] : 1.0;
     }
 
     /* Scores s_t = scale * <q, k_t>; q layout [B, q_len, Hq, D]. */
@@ -163,7 +188,7 @@ static int decode_row(const void *q, const void *k_pool, const void *v_pool,
         double dot = 0.0;
         for (d = 0; d < D; ++d) {
             dot += load_elem(q, q_base + d, dtype) *
-                   (ks * load_elem(k_pool, row_base[t] + d, kv_dtype));
+                   (ks[t] * load_elem(k_pool, row_base[t] + d, kv_dtype));
         }
         s[t] = scale * dot;
     }
@@ -180,13 +205,15 @@ static int decode_row(const void *q, const void *k_pool, const void *v_pool,
     }
     for (int64_t t = 0; t < n; ++t) {
         for (d = 0; d < D; ++d) {
-            out[d] += s[t] * (vs * load_elem(v_pool, row_base[t] + d, kv_dtype));
+            out[d] += s[t] * (vs[t] * load_elem(v_pool, row_base[t] + d, kv_dtype));
         }
     }
     for (d = 0; d < D; ++d) out[d] /= z;
 
     free(row_base);
     free(s);
+    free(ks);
+    free(vs);
     return ORACLE_OK;
 }
 
@@ -219,7 +246,7 @@ int oracle_decode_rows_f64(const void *q, const void *k_pool, const void *v_pool
     int status = ORACLE_OK;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t i = 0; i < n_rows; ++i) {
-        int r = decode_row(q, k_pool, v_pool, NULL, NULL, block_table, seq_lens, dtype, dtype,
+        int r = decode_row(q, k_pool, v_pool, NULL, NULL, 0, block_table, seq_lens, dtype, dtype,
                            1, Hq, Hkv, D,
                            block_size, num_blocks, max_blocks, 0, scale, rows[2 * i], 0,
                            rows[2 * i + 1], out + i * (int64_t)D);
@@ -245,7 +272,7 @@ int oracle_decode_f64(const void *q, const void *k_pool, const void *v_pool,
     const int64_t n_rows = (int64_t)B * Hq;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t i = 0; i < n_rows; ++i) {
-        int r = decode_row(q, k_pool, v_pool, NULL, NULL, block_table, seq_lens, dtype, dtype,
+        int r = decode_row(q, k_pool, v_pool, NULL, NULL, 0, block_table, seq_lens, dtype, dtype,
                            1, Hq, Hkv, D,
                            block_size, num_blocks, max_blocks, 0, scale, (int)(i / Hq), 0,
                            (int)(i % Hq), out + i * (int64_t)D);
@@ -266,7 +293,8 @@ int oracle_decode_f64(const void *q, const void *k_pool, const void *v_pool,
  * no window.  With q_len = 1 and window = 0 this is oracle_decode_f64.
  */
 static int decode_ex(const void *q, const void *k_pool, const void *v_pool, const float *k_scale,
-                     const float *v_scale, const int32_t *block_table, const int32_t *seq_lens,
+                     const float *v_scale, int scale_per_block, const int32_t *block_table,
+                     const int32_t *seq_lens,
                      int dtype, int kv_dtype, int B, int q_len, int Hq, int Hkv, int D,
                      int block_size, int64_t num_blocks, int max_blocks, int window,
                      double scale, double *out)
@@ -281,7 +309,8 @@ static int decode_ex(const void *q, const void *k_pool, const void *v_pool, cons
         const int h = (int)(r % Hq);
         const int i = (int)((r / Hq) % q_len);
         const int b = (int)(r / ((int64_t)Hq * q_len));
-        int st = decode_row(q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, dtype,
+        int st = decode_row(q, k_pool, v_pool, k_scale, v_scale, scale_per_block, block_table,
+                            seq_lens, dtype,
                             kv_dtype, q_len, Hq, Hkv, D,
                             block_size, num_blocks, max_blocks, window, scale, b, i, h,
                             out + r * (int64_t)D);
@@ -300,26 +329,46 @@ int oracle_decode_ex_f64(const void *q, const void *k_pool, const void *v_pool,
                          int q_len, int Hq, int Hkv, int D, int block_size, int64_t num_blocks,
                          int max_blocks, int window, double scale, double *out)
 {
-    return decode_ex(q, k_pool, v_pool, NULL, NULL, block_table, seq_lens, dtype, dtype, B, q_len,
+    return decode_ex(q, k_pool, v_pool, NULL, NULL, 0, block_table, seq_lens, dtype, dtype, B, q_len,
                      Hq, Hkv, D, block_size, num_blocks, max_blocks, window, scale, out);
 }
 
 /*
- * 8-bit K/V pages: k_pool / v_pool hold e4m3 bytes; element (block, slot,
- * head kv, d) stands for k_scale[kv] * e4m3(byte) (v_scale for V), one scale
- * per KV head.  q and out as in oracle_decode_ex_f64, q in `q_dtype`
- * (float32 or bfloat16).
+ * 8-bit K/V pages: k_pool / v_pool hold 8-bit codes, `code` ORACLE_FP8_E4M3
+ * (e4m3 bytes) or ORACLE_INT8 (signed integers); element (block, slot, head
+ * kv, d) stands for a scale times the code's value.  scale_per_block == 0:
+ * k_scale / v_scale hold one scale per KV head [Hkv]; 1: one per physical
+ * block and KV head [num_blocks, Hkv].  q and out as in
+ * oracle_decode_ex_f64, q in `q_dtype` (float32 or bfloat16).  Quantized KV
+ * pages: "Modern LLM Inference ...", section 6 (int8 / fp8 quantization);
+ * "The Ultimate Guide ... Part 2", "KV Cache Compression".
  */
+int oracle_decode_q8_f64(const void *q, int q_dtype, const void *k_pool, const void *v_pool,
+                         int code, const float *k_scale, const float *v_scale,
+                         int scale_per_block, const int32_t *block_table,
+                         const int32_t *seq_lens, int B, int q_len, int Hq, int Hkv, int D,
+                         int block_size, int64_t num_blocks, int max_blocks, int window,
+                         double scale, double *out)
+{
+    if (q_dtype != ORACLE_F32 && q_dtype != ORACLE_BF16) return ORACLE_ERR_ARG;
+    if (code != ORACLE_FP8_E4M3 && code != ORACLE_INT8) return ORACLE_ERR_ARG;
+    if (!k_scale || !v_scale || (scale_per_block != 0 && scale_per_block != 1))
+        return ORACLE_ERR_ARG;
+    return decode_ex(q, k_pool, v_pool, k_scale, v_scale, scale_per_block, block_table,
+                     seq_lens, q_dtype, code, B, q_len, Hq, Hkv, D, block_size, num_blocks,
+                     max_blocks, window, scale, out);
+}
+
+/* e4m3 pages with one scale per KV head (oracle_decode_q8_f64's first form). */
 int oracle_decode_kv8_f64(const void *q, int q_dtype, const void *k_pool, const void *v_pool,
                           const float *k_scale, const float *v_scale,
                           const int32_t *block_table, const int32_t *seq_lens, int B, int q_len,
                           int Hq, int Hkv, int D, int block_size, int64_t num_blocks,
                           int max_blocks, int window, double scale, double *out)
 {
-    if (q_dtype == ORACLE_FP8_E4M3 || !k_scale || !v_scale) return ORACLE_ERR_ARG;
-    return decode_ex(q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, q_dtype,
-                     ORACLE_FP8_E4M3, B, q_len, Hq, Hkv, D, block_size, num_blocks, max_blocks,
-                     window, scale, out);
+    return oracle_decode_q8_f64(q, q_dtype, k_pool, v_pool, ORACLE_FP8_E4M3, k_scale, v_scale,
+                                0, block_table, seq_lens, B, q_len, Hq, Hkv, D, block_size,
+                                num_blocks, max_blocks, window, scale, out);
 }
 
 /* Threads OpenMP will use (1 without OpenMP). */

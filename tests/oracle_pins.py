@@ -496,6 +496,122 @@ def pin_kv8_scales(orc):
     assert np.abs(k2 - s2).max() <= 1e-12 * np.abs(s2).max()
 
 
+# ------------------------------------------- int8 codes and per-block scales
+# The same quantized pages with signed 8-bit integer codes, and with a scale
+# per physical block and KV head instead of one per KV head: a block's scale is
+# fixed when the block is written, so a cache filled token by token can give
+# each block its own range ("Modern LLM Inference ...", section 6, int8 / fp8
+# quantization; "The Ultimate Guide ... Part 2", "KV Cache Compression").
+INT8_CASES = [(0x80, -128.0), (0xFF, -1.0), (0x00, 0.0), (0x01, 1.0), (0x7F, 127.0),
+              (0x9C, -100.0), (0x64, 100.0), (0xC0, -64.0), (0x2A, 42.0)]
+
+
+def _q8_case(rng, code, B, Hq, Hkv, D, bs, lens, per_block):
+    q, k, v, t, L = paged_case(rng, B, Hq, Hkv, D, bs, lens, "f32")
+    k8 = rng.integers(0, 256, size=k.shape).astype(np.uint8)
+    v8 = rng.integers(0, 256, size=v.shape).astype(np.uint8)
+    if code == "e4m3":
+        k8[(k8 & 0x7F) == 0x7F] = 0x38          # no NaN codes
+        v8[(v8 & 0x7F) == 0x7F] = 0x30
+    shape = (k.shape[0], Hkv) if per_block else (Hkv,)
+    lo, hi = (0.01, 0.1) if code == "e4m3" else (0.0005, 0.005)   # moderate logits
+    ks = rng.uniform(lo, hi, size=shape).astype(np.float32)
+    vs = rng.uniform(0.5, 2.0, size=shape).astype(np.float32)
+    return q, k8, v8, ks, vs, t, L
+
+
+def pin_q8_int8_values(orc):
+    """One cached token: the output is the V scale times the signed integer
+    code, with the scale taken from the row of the block the token sits in."""
+    D = len(INT8_CASES)
+    q = np.zeros((1, 1, D), dtype=np.float32)
+    k8 = np.zeros((3, 1, 1, D), dtype=np.uint8)
+    v8 = np.zeros((3, 1, 1, D), dtype=np.uint8)
+    v8[2, 0, 0] = [c for c, _ in INT8_CASES]
+    want = np.array([x for _, x in INT8_CASES])
+    table = np.array([[2]], np.int32)
+    one = np.ones(1, np.int32)
+    out, rc = orc.decode_q8_f64(q, k8, v8, "int8", np.ones(1, np.float32),
+                                np.full(1, 0.75, np.float32), table, one, 1.0)
+    assert rc == 0 and np.array_equal(out[0, 0], 0.75 * want)
+    vs = np.array([[9.0], [5.0], [0.25]], np.float32)           # block 2 -> 0.25
+    out, rc = orc.decode_q8_f64(q, k8, v8, "int8", np.ones((3, 1), np.float32), vs, table, one,
+                                1.0)
+    assert rc == 0 and np.array_equal(out[0, 0], 0.25 * want)
+
+
+def pin_q8_block_scale_closed_form(orc):
+    """Four tokens in two 2-token blocks stored at physical blocks 3 and 1.
+    Every K code is 1 and q = 1, so token t has logit ks[block(t)]; V codes
+    are 1, 2, 3, 4.  With K scales (2.0 at block 3, 0.5 at block 1) and V
+    scales (0.25 at block 3, 3.0 at block 1):
+        out = (e^2 * 0.25 * (1 + 2) + e^0.5 * 3.0 * (3 + 4)) / (2 e^2 + 2 e^0.5)."""
+    for code, one_code, v_codes in (("int8", 1, [1, 2, 3, 4]),
+                                    ("e4m3", 0x38, [0x38, 0x40, 0x44, 0x48])):  # 1, 2, 3, 4
+        k8 = np.zeros((4, 2, 1, 1), dtype=np.uint8)
+        v8 = np.zeros((4, 2, 1, 1), dtype=np.uint8)
+        k8[3, :, 0, 0] = one_code
+        k8[1, :, 0, 0] = one_code
+        v8[3, :, 0, 0] = v_codes[:2]
+        v8[1, :, 0, 0] = v_codes[2:]
+        ks = np.array([[5.0], [0.5], [7.0], [2.0]], np.float32)
+        vs = np.array([[9.0], [3.0], [11.0], [0.25]], np.float32)
+        q = np.ones((1, 1, 1), dtype=np.float32)
+        out, rc = orc.decode_q8_f64(q, k8, v8, code, ks, vs, np.array([[3, 1]], np.int32),
+                                    np.array([4], np.int32), 1.0)
+        e2, e05 = math.exp(2.0), math.exp(0.5)
+        want = (e2 * 0.25 * (1 + 2) + e05 * 3.0 * (3 + 4)) / (2 * e2 + 2 * e05)
+        assert rc == 0 and abs(out[0, 0, 0] - want) <= 1e-12 * want, (code, out[0, 0, 0], want)
+
+
+def pin_q8_brute_force(orc):
+    """Against the dense formulation on pages dequantised outside the oracle
+    (torch's e4m3 decoding, numpy's int8 view), both scale forms, several
+    query tokens and windows."""
+    from oracle.brute import brute_decode_q8
+    rng = np.random.default_rng(83)
+    for code in ("e4m3", "int8"):
+        for per_block in (False, True):
+            for lens, q_len, window in (([9, 17, 3], 1, 0), ([12, 5, 30], 3, 0),
+                                        ([20, 8, 14], 2, 6)):
+                q, k8, v8, ks, vs, t, L = _q8_case(rng, code, 3, 4 * q_len, 2, 8, 4, lens,
+                                                   per_block)
+                q = q.reshape(3, q_len, 4, 8)
+                out, rc = orc.decode_q8_f64(q, k8, v8, code, ks, vs, t, L, 0.3, window)
+                ref = brute_decode_q8(q, k8, v8, code, ks, vs, t, L, 0.3, window)
+                assert rc == 0
+                assert np.abs(out - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max()), (
+                    code, per_block, q_len, window)
+
+
+def pin_q8_uniform_block_scales(orc):
+    """A per-block table whose every row holds the per-head scales gives
+    exactly the per-head result."""
+    rng = np.random.default_rng(89)
+    for code in ("e4m3", "int8"):
+        q, k8, v8, ks, vs, t, L = _q8_case(rng, code, 2, 8, 2, 8, 4, [13, 7], False)
+        a, _ = orc.decode_q8_f64(q, k8, v8, code, ks, vs, t, L, 0.5)
+        nb = k8.shape[0]
+        b, _ = orc.decode_q8_f64(q, k8, v8, code, np.tile(ks, (nb, 1)), np.tile(vs, (nb, 1)), t,
+                                 L, 0.5)
+        assert np.array_equal(a, b)
+
+
+def pin_q8_block_permutation(orc):
+    """Moving physical blocks together with their scale rows (and renumbering
+    the table) leaves the output unchanged, bit for bit."""
+    rng = np.random.default_rng(97)
+    for code in ("e4m3", "int8"):
+        q, k8, v8, ks, vs, t, L = _q8_case(rng, code, 3, 4, 2, 8, 4, [10, 3, 15], True)
+        a, _ = orc.decode_q8_f64(q, k8, v8, code, ks, vs, t, L, 0.5)
+        nb = k8.shape[0]
+        perm = rng.permutation(nb)                     # new block i holds old block perm[i]
+        inv = np.argsort(perm)
+        t2 = np.where(t >= 0, inv[np.maximum(t, 0)], -1).astype(np.int32)
+        b, _ = orc.decode_q8_f64(q, k8[perm], v8[perm], code, ks[perm], vs[perm], t2, L, 0.5)
+        assert np.array_equal(a, b)
+
+
 PINS = [
     pin_brute_force,
     pin_paged_equals_contiguous,
@@ -520,4 +636,9 @@ PINS = [
     pin_kv8_brute_force,
     pin_kv8_equals_wide_pages,
     pin_kv8_scales,
+    pin_q8_int8_values,
+    pin_q8_block_scale_closed_form,
+    pin_q8_brute_force,
+    pin_q8_uniform_block_scales,
+    pin_q8_block_permutation,
 ]

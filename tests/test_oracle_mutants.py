@@ -23,15 +23,24 @@ MUTANTS = {
     "not_normalised": ("out[d] /= z;", "out[d] /= 1.0;"),
     "exp_sign": ("s[t] = exp(s[t] - m);", "s[t] = exp(m - s[t]);"),
     "exp_base_two": ("s[t] = exp(s[t] - m);", "s[t] = exp2(s[t] - m);"),
-    "values_from_k": ("out[d] += s[t] * (vs * load_elem(v_pool,",
-                      "out[d] += s[t] * (vs * load_elem(k_pool,"),
+    "values_from_k": ("out[d] += s[t] * (vs[t] * load_elem(v_pool,",
+                      "out[d] += s[t] * (vs[t] * load_elem(k_pool,"),
     "e4m3_bias": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
     "e4m3_subnormal": ("ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
     "e4m3_sign_lost": ("return sign ? -x : x;", "return x;"),
-    "k_scale_ignored": ("const double ks = k_scale ? (double)k_scale[kv] : 1.0;",
-                        "const double ks = 1.0;"),
-    "v_scale_ignored": ("const double vs = v_scale ? (double)v_scale[kv] : 1.0;",
-                        "const double vs = 1.0;"),
+    "k_scale_ignored": ("ks[t] = k_scale ? (double)k_scale[sc_idx] : 1.0;", "ks[t] = 1.0;"),
+    "v_scale_ignored": ("vs[t] = v_scale ? (double)v_scale[sc_idx] : 1.0;", "vs[t] = 1.0;"),
+    "v_scale_from_k_table": ("vs[t] = v_scale ? (double)v_scale[sc_idx] : 1.0;",
+                             "vs[t] = v_scale ? (double)k_scale[sc_idx] : 1.0;"),
+    "block_scale_by_logical_block": (
+        "const int64_t sc_idx = scale_per_block ? phys * Hkv + kv : kv;",
+        "const int64_t sc_idx = scale_per_block ? (tok / block_size) * Hkv + kv : kv;"),
+    "block_scale_head_dropped": ("const int64_t sc_idx = scale_per_block ? phys * Hkv + kv : kv;",
+                                 "const int64_t sc_idx = scale_per_block ? phys * Hkv : kv;"),
+    "block_scale_ignored": ("const int64_t sc_idx = scale_per_block ? phys * Hkv + kv : kv;",
+                            "const int64_t sc_idx = kv;"),
+    "int8_read_unsigned": ("return (double)((const int8_t *)base)[idx];",
+                           "return (double)((const uint8_t *)base)[idx];"),
     "query_head_index": ("* Hq + h) * (int64_t)D", "* Hq + kv) * (int64_t)D"),
     "query_token_index": ("((int64_t)b * q_len + i) * Hq", "((int64_t)b * q_len) * Hq"),
     "causal_shifted": ("const int64_t p = L - q_len + i;", "const int64_t p = L - q_len + i - 1;"),
