@@ -56,6 +56,25 @@ def describe(w):
                                          else "fixed", w.num_blocks, w.seed))
 
 
+def workload_bytes(w, q_len=1, window=0):
+    """Algorithmic bytes of one step over workload w (8-bit pages with a scale
+    per block and KV head also read those scales)."""
+    elt, q_elt = accounting.ELT[w.dtype], accounting.Q_ELT[w.dtype]
+    pb = w.k_scale is not None and w.k_scale.dim() == 2
+    if q_len == 1 and window == 0:
+        return accounting.algorithmic_bytes(w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt, q_elt,
+                                            block_scales=pb)
+    return accounting.algorithmic_bytes_ex(w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt, q_len,
+                                           window, q_elt, block_scales=pb)
+
+
+def oracle_q8(oracle, w, q, k, v, table, lens):
+    """The oracle on 8-bit pages of w (e4m3 or int8 codes, either scale form)."""
+    return oracle.decode_q8_f64(q, k, v, "e4m3" if w.dtype == "fp8" else "int8",
+                                w.k_scale.cpu().numpy(), w.v_scale.cpu().numpy(), table, lens,
+                                w.scale)
+
+
 def peak_hbm():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -281,10 +300,9 @@ def cpu_oracle_rate(w, budget_s, threads=0):
 
     q, k, v = gen.to_numpy_bits(w.q), gen.to_numpy_bits(w.k_pool), gen.to_numpy_bits(w.v_pool)
     elt, q_elt = accounting.ELT[w.dtype], accounting.Q_ELT[w.dtype]
-    nbytes = accounting.algorithmic_bytes(w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt, q_elt)
-    if w.dtype == "fp8":
-        ks, vs = w.k_scale.cpu().numpy(), w.v_scale.cpu().numpy()
-        run = lambda: oracle.decode_kv8_f64(q, k, v, ks, vs, w.table_np, w.lens_np, w.scale)
+    nbytes = workload_bytes(w)
+    if w.dtype in gen.Q8:
+        run = lambda: oracle_q8(oracle, w, q, k, v, w.table_np, w.lens_np)
     else:
         run = lambda: oracle.decode_f64(q, k, v, w.table_np, w.lens_np, w.scale)
     reps = 0
@@ -306,7 +324,7 @@ def run_reference(args, world, rank):
         return
     w = gen.make(args.config, device="cpu")
     elt, q_elt = accounting.ELT[w.dtype], accounting.Q_ELT[w.dtype]
-    nbytes = accounting.algorithmic_bytes(w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt, q_elt)
+    nbytes = workload_bytes(w)
     import oracle
 
     oracle.set_num_threads(args.cpu_threads if args.cpu_threads > 0 else host_cores())
@@ -314,14 +332,13 @@ def run_reference(args, world, rank):
     q, k, v = gen.to_numpy_bits(w.q), gen.to_numpy_bits(w.k_pool), gen.to_numpy_bits(w.v_pool)
     # One step = the oracle over a bounded sample: every sequence, a subset of
     # query heads (whole KV groups) so that K+W steps fit in a few minutes.
-    if w.dtype == "fp8":
+    if w.dtype in gen.Q8:
         # 8-bit pages: every query head of the first B/8 sequences per step
         nb = max(1, w.B // 8)
-        ks, vs = w.k_scale.numpy(), w.v_scale.numpy()
-        step = lambda: oracle.decode_kv8_f64(q[:nb], k, v, ks, vs, w.table_np[:nb],
-                                             w.lens_np[:nb], w.scale)
+        step = lambda: oracle_q8(oracle, w, q[:nb], k, v, w.table_np[:nb], w.lens_np[:nb])
         frac = accounting.algorithmic_bytes(w.lens_np[:nb], w.Hq, w.Hkv, w.D, w.block_size, elt,
-                                            q_elt) / nbytes
+                                            q_elt) / accounting.algorithmic_bytes(
+            w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt, q_elt)
         sample = ("each step: sequences 0..%d of %d, every query head, float64, %d host "
                   "core(s)" % (nb - 1, w.B, cores))
     else:
@@ -359,7 +376,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(dev)
     w = gen.make(args.config, device=dev, seed=replica_seed(args.config, rank))
     elt, q_elt = accounting.ELT[w.dtype], accounting.Q_ELT[w.dtype]
-    nbytes = accounting.algorithmic_bytes(w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt, q_elt)
+    nbytes = workload_bytes(w)
     pool = pgd.PagedKVPool(w.k_pool, w.v_pool, w.k_scale, w.v_scale)
     out = torch.empty_like(w.q)
     ws = pgd.alloc_workspace(pool, w.B, w.Hq, 0)
@@ -376,8 +393,7 @@ def run_ours(args, world, rank, local):
         g.manual_seed(w.seed + 7)
         q_ex = torch.randn((w.B, args.q_len, w.Hq, w.D), generator=g, device=dev).to(w.q.dtype)
         out = torch.empty_like(q_ex)
-        nbytes = accounting.algorithmic_bytes_ex(w.lens_np, w.Hq, w.Hkv, w.D, w.block_size, elt,
-                                                 args.q_len, args.window, q_elt)
+        nbytes = workload_bytes(w, args.q_len, args.window)
         ws = torch.zeros(max(256, pgd.paged_gqa_workspace_size_ex(pool, w.B, args.q_len, w.Hq)),
                          dtype=torch.uint8, device=dev)
 

@@ -58,13 +58,27 @@ for _bs in (8, 16, 32, 64, 128):
                                        Hkv=8, D=128, block_size=_bs, dtype="bf16", max_len=8192,
                                        seed=1005)
 
-TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.float8_e4m3fn}
+TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.float8_e4m3fn,
+                "i8": torch.int8}
+Q8 = ("fp8", "i8")   # 8-bit pages
+CODE_MAX = {"fp8": 448.0, "i8": 127.0}
 
 # 8-bit (e4m3) pages: the Llama-3-8B and 70B layer shapes with K/V stored as
 # e4m3 codes of N(0, 1) draws and one scale per KV head drawn from U[0.5, 1.5];
 # q stays bfloat16.
 CONFIGS["llama3_8b_fp8"] = dict(CONFIGS["llama3_8b"], dtype="fp8")
 CONFIGS["long_70b_fp8"] = dict(CONFIGS["long_70b"], dtype="fp8")
+# int8 pages with one scale per KV head: N(0, 1) draws divided by a per-head
+# scale U[0.5, 1.5] * 4 / 127, rounded, clipped to [-127, 127].
+CONFIGS["llama3_8b_i8"] = dict(CONFIGS["llama3_8b"], dtype="i8")
+CONFIGS["long_70b_i8"] = dict(CONFIGS["long_70b"], dtype="i8")
+# 8-bit pages with a scale per physical block and KV head, quantized the way a
+# writer quantizes a filled block: scale = max |x| over the block's slots and
+# head dimension / the code's largest value (448 for e4m3, 127 for int8),
+# code = x / scale rounded to the code (nearest even for e4m3, nearest for int8).
+for _base in ("llama3_8b", "long_70b"):
+    for _code in Q8:
+        CONFIGS["%s_%s_pb" % (_base, _code)] = dict(CONFIGS[_base], dtype=_code, scales="block")
 
 
 def config_names():
@@ -130,6 +144,34 @@ def _randn(shape, gen, device, dtype, chunk_elems=1 << 27):
     return out
 
 
+def _quantized(shape, gen, device, code, scales, chunk_elems=1 << 27):
+    """8-bit pages of N(0, 1) draws: (codes [num_blocks, bs, Hkv, D], scales
+    [Hkv] or [num_blocks, Hkv] float32), made in slices of blocks."""
+    nb, bs, hkv, d = shape
+    codes = torch.empty(shape, dtype=TORCH_DTYPES[code], device=device)
+    if scales == "block":
+        sc = torch.empty((nb, hkv), dtype=torch.float32, device=device)
+    else:  # per head: fixed before the data, values beyond 4 * U scale saturate
+        sc = ((0.5 + torch.rand((hkv,), generator=gen, device=device)) * 4.0 / CODE_MAX[code]
+              ).to(torch.float32)
+    rows = max(1, chunk_elems // (bs * hkv * d))
+    for r0 in range(0, nb, rows):
+        r1 = min(nb, r0 + rows)
+        x = torch.randn((r1 - r0, bs, hkv, d), generator=gen, device=device, dtype=torch.float32)
+        if scales == "block":
+            amax = x.abs().amax(dim=(1, 3))                       # [blocks, Hkv]
+            s = (amax / CODE_MAX[code]).clamp_min(1e-30)
+            sc[r0:r1] = s
+        else:
+            s = sc[None, :].expand(r1 - r0, hkv)
+        y = x / s[:, None, :, None]
+        if code == "i8":
+            codes[r0:r1] = torch.round(y).clamp_(-127, 127).to(torch.int8)
+        else:
+            codes[r0:r1] = y.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn)
+    return codes, sc
+
+
 def make(name="tiny", device="cpu", poison=False, seed=None, **over):
     """Build a workload from the recipe `name`, with optional field overrides.
 
@@ -159,29 +201,41 @@ def make(name="tiny", device="cpu", poison=False, seed=None, **over):
         pos += nb[b]
 
     tdt = TORCH_DTYPES[spec["dtype"]]
-    fp8 = spec["dtype"] == "fp8"
+    q8 = spec["dtype"] in Q8
+    scales = spec.get("scales", "head")
     gen = torch.Generator(device=device)
     gen.manual_seed(int(spec["seed"]))
-    q = _randn((B, Hq, D), gen, device, torch.bfloat16 if fp8 else tdt)
-    k_pool = _randn((num_blocks, bs, Hkv, D), gen, device, tdt)
-    v_pool = _randn((num_blocks, bs, Hkv, D), gen, device, tdt)
+    q = _randn((B, Hq, D), gen, device, torch.bfloat16 if q8 else tdt)
     k_scale = v_scale = None
-    if fp8:
-        k_scale = (0.5 + torch.rand((Hkv,), generator=gen, device=device)).to(torch.float32)
-        v_scale = (0.5 + torch.rand((Hkv,), generator=gen, device=device)).to(torch.float32)
+    if q8 and (spec["dtype"] == "i8" or scales == "block"):
+        k_pool, k_scale = _quantized((num_blocks, bs, Hkv, D), gen, device, spec["dtype"], scales)
+        v_pool, v_scale = _quantized((num_blocks, bs, Hkv, D), gen, device, spec["dtype"], scales)
+    else:
+        k_pool = _randn((num_blocks, bs, Hkv, D), gen, device, tdt)
+        v_pool = _randn((num_blocks, bs, Hkv, D), gen, device, tdt)
+        if q8:
+            k_scale = (0.5 + torch.rand((Hkv,), generator=gen, device=device)).to(torch.float32)
+            v_scale = (0.5 + torch.rand((Hkv,), generator=gen, device=device)).to(torch.float32)
     if poison:
+        # NaN where the type has one; int8 pages get the code -128, which no
+        # writer above produces, and (per-block scales) NaN scale rows for
+        # the unused blocks
+        bad = -128 if spec["dtype"] == "i8" else float("nan")
         used_mask = np.zeros(num_blocks, dtype=bool)
         used_mask[perm[:used]] = True
         unused = torch.from_numpy(np.nonzero(~used_mask)[0]).to(device)
         if unused.numel():
-            k_pool[unused] = float("nan")
-            v_pool[unused] = float("nan")
+            k_pool[unused] = bad
+            v_pool[unused] = bad
+            if k_scale is not None and k_scale.dim() == 2:
+                k_scale[unused] = float("nan")
+                v_scale[unused] = float("nan")
         for b in range(B):
             L = int(lens[b])
             if L % bs:
                 last = int(table[b, nb[b] - 1])
-                k_pool[last, L % bs:] = float("nan")
-                v_pool[last, L % bs:] = float("nan")
+                k_pool[last, L % bs:] = bad
+                v_pool[last, L % bs:] = bad
     return Workload(name=name, q=q, k_pool=k_pool, v_pool=v_pool,
                     block_table=torch.from_numpy(table).to(device),
                     seq_lens=torch.from_numpy(lens.astype(np.int32)).to(device),
@@ -193,12 +247,12 @@ def make(name="tiny", device="cpu", poison=False, seed=None, **over):
 
 def to_numpy_bits(t):
     """A float32 or bfloat16 tensor as a host numpy array the oracle accepts
-    (float32 as is, bfloat16 as its uint16 bit patterns, 8-bit e4m3 as uint8
-    codes)."""
+    (float32 as is, bfloat16 as its uint16 bit patterns, 8-bit e4m3 and int8
+    codes as their uint8 bytes)."""
     t = t.detach().to("cpu").contiguous()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
-    if t.dtype in (torch.float8_e4m3fn, torch.uint8):
+    if t.dtype in (torch.float8_e4m3fn, torch.uint8, torch.int8):
         return t.view(torch.uint8).numpy()
     if t.dtype == torch.float32:
         return t.numpy()

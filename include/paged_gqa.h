@@ -31,9 +31,10 @@
  *     block_table  [B, max_blocks]                     int32
  *     seq_lens     [B]                                 int32
  *     out          [B, Hq, D]                          dtype
- * dtype is float32 or bfloat16 (PGD_F32 / PGD_BF16), or 8-bit e4m3 pages with
- * bfloat16 q and out (PGD_FP8_E4M3, paged_kv_pool_create_fp8); accumulation
- * is float32.
+ * dtype is float32 or bfloat16 (PGD_F32 / PGD_BF16), or 8-bit pages (e4m3
+ * floats or int8 integers, scaled per KV head or per block and KV head) with
+ * bfloat16 q and out (PGD_FP8_E4M3 / PGD_INT8, paged_kv_pool_create_fp8 and
+ * paged_kv_pool_create_q8); accumulation is float32.
  * D (head_dim) is 64 or 128; G = Hq / Hkv is 1..64; block_size is 1..256
  * (bfloat16 pools need a power of two in 8..256).
  *
@@ -65,7 +66,13 @@ extern "C" {
 
 typedef struct pgd_pool_s *pgd_pool_t;
 
-enum pgd_dtype { PGD_F32 = 0, PGD_BF16 = 1, PGD_FP8_E4M3 = 2 };
+enum pgd_dtype { PGD_F32 = 0, PGD_BF16 = 1, PGD_FP8_E4M3 = 2, PGD_INT8 = 3 };
+
+/* Granularity of the scales of 8-bit pages. */
+enum pgd_scale_granularity {
+    PGD_SCALE_PER_HEAD = 0,  /* k_scale / v_scale [Hkv] */
+    PGD_SCALE_PER_BLOCK = 1  /* k_scale / v_scale [num_blocks, Hkv] */
+};
 
 enum pgd_status {
     PGD_OK = 0,
@@ -113,6 +120,31 @@ int paged_kv_pool_create(pgd_pool_t *out, const void *k_pool, const void *v_pool
 int paged_kv_pool_create_fp8(pgd_pool_t *out, const void *k_pool, const void *v_pool,
                              const float *k_scale, const float *v_scale, int64_t num_blocks,
                              int block_size, int num_kv_heads, int head_dim);
+
+/*
+ * Describe a pool pair of 8-bit K/V pages of either code, with scales of
+ * either granularity.
+ *   code         PGD_FP8_E4M3 (e4m3 bytes, as for paged_kv_pool_create_fp8) or
+ *                PGD_INT8 (two's-complement integers in [-128, 127])
+ *   granularity  PGD_SCALE_PER_HEAD: k_scale / v_scale are [num_kv_heads];
+ *                element (block, slot, h, d) stands for k_scale[h] * code.
+ *                PGD_SCALE_PER_BLOCK: k_scale / v_scale are [num_blocks,
+ *                num_kv_heads] (row-major); element (block, slot, h, d)
+ *                stands for k_scale[block * num_kv_heads + h] * code, so each
+ *                physical block carries its own range (a cache written token
+ *                by token fixes a block's scale when it writes the block).
+ * The other arguments and rules are those of paged_kv_pool_create_fp8
+ * (head_dim 128, block_size a power of two in 8..256, bfloat16 q and out).
+ * The scale arrays are read by the decode kernels at every call, so a caller
+ * may rewrite a block's row between calls (stream-ordered).  Quantized KV
+ * pages: int8 / fp8 quantization, "Modern LLM Inference ...", section 6;
+ * "The Ultimate Guide ... Part 2", "KV Cache Compression".
+ * PGD_ERR_DTYPE for another code, PGD_ERR_ARG for another granularity or a
+ * null scale array.
+ */
+int paged_kv_pool_create_q8(pgd_pool_t *out, const void *k_pool, const void *v_pool, int code,
+                            const float *k_scale, const float *v_scale, int granularity,
+                            int64_t num_blocks, int block_size, int num_kv_heads, int head_dim);
 
 /* Release a handle (not the pools).  NULL is accepted. */
 int paged_kv_pool_destroy(pgd_pool_t pool);

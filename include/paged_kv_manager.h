@@ -94,15 +94,19 @@ int pgd_kvm_ref_count(pgd_kvm_t m, int64_t block, int *count);
 /*
  * Device: copy whole blocks, K and V, from src[i] to dst[i] for i < n (device
  * int32 arrays).  Destinations must be distinct and differ from every source.
+ * For 8-bit pages with a scale per block and KV head (paged_kv_pool_create_q8
+ * with PGD_SCALE_PER_BLOCK) the destination blocks' K and V scale rows are
+ * copied from the sources' too (the handle's scale arrays are written).
  */
 int paged_kv_copy_blocks(pgd_pool_t pool, const int32_t *src, const int32_t *dst, int n,
                          void *stream);
 
 /*
  * Device: store n new tokens.  k_new and v_new are [n, Hkv, D] in the pool's
- * dtype; slot_mapping is a device int32 array of n physical slots (distinct,
- * in [0, num_blocks * block_size)).  A slot out of range is skipped and
- * latches PGD_ERR_BLOCK_ID (read it with paged_gqa_get_error).
+ * dtype (8-bit pages: codes, already quantized with the scales of the blocks
+ * they go to); slot_mapping is a device int32 array of n physical slots
+ * (distinct, in [0, num_blocks * block_size)).  A slot out of range is skipped
+ * and latches PGD_ERR_BLOCK_ID (read it with paged_gqa_get_error).
  */
 int paged_kv_append(pgd_pool_t pool, const void *k_new, const void *v_new,
                     const int32_t *slot_mapping, int n, void *stream);

@@ -25,6 +25,14 @@ __all__ = [
 
 _DTYPES = {torch.float32: _lib.PGD_F32, torch.bfloat16: _lib.PGD_BF16}
 _FP8 = (torch.float8_e4m3fn, torch.uint8)  # 8-bit e4m3 pages (uint8 = raw codes)
+_Q8 = _FP8 + (torch.int8,)                  # 8-bit pages of either code
+
+
+def _code_of(dtype):
+    """Library dtype of a pool's torch dtype (int8 pages: int8 codes)."""
+    if dtype == torch.int8:
+        return _lib.PGD_INT8
+    return _lib.PGD_FP8_E4M3 if dtype in _FP8 else _DTYPES[dtype]
 
 
 def _check(rc, what=""):
@@ -47,14 +55,16 @@ class PagedKVPool:
     """
 
     def __init__(self, k_pool, v_pool, k_scale=None, v_scale=None):
-        """float32 / bfloat16 pools, or 8-bit e4m3 pages (torch.float8_e4m3fn or
-        uint8 codes) with per-KV-head float32 scales k_scale / v_scale [Hkv]."""
+        """float32 / bfloat16 pools, or 8-bit pages -- e4m3 (torch.float8_e4m3fn
+        or uint8 codes) or int8 (torch.int8 codes) -- with float32 scales
+        k_scale / v_scale of shape [Hkv] (one per KV head) or [num_blocks, Hkv]
+        (one per physical block and KV head)."""
         lib = _lib.load()
         if not (isinstance(k_pool, torch.Tensor) and isinstance(v_pool, torch.Tensor)):
             raise TypeError("k_pool and v_pool must be torch tensors")
         if k_pool.shape != v_pool.shape or k_pool.dim() != 4:
             raise ValueError("pools must both be [num_blocks, block_size, Hkv, D]")
-        fp8 = k_pool.dtype in _FP8
+        fp8 = k_pool.dtype in _Q8
         if k_pool.dtype != v_pool.dtype or not (fp8 or k_pool.dtype in _DTYPES):
             raise TypeError("pools must be float32, bfloat16 or 8-bit, the same for K and V")
         if not (k_pool.is_cuda and v_pool.is_cuda):
@@ -66,17 +76,25 @@ class PagedKVPool:
         self.dtype = k_pool.dtype
         self.q_dtype = torch.bfloat16 if fp8 else k_pool.dtype
         self.k_scale, self.v_scale = k_scale, v_scale
+        self.scale_per_block = False
         h = ctypes.c_void_p()
         with torch.cuda.device(k_pool.device):
             if fp8:
+                per_head, per_block = (self.num_kv_heads,), (self.num_blocks, self.num_kv_heads)
                 for sc in (k_scale, v_scale):
                     if (not isinstance(sc, torch.Tensor) or sc.dtype != torch.float32 or
-                            not sc.is_cuda or sc.shape != (self.num_kv_heads,)):
-                        raise ValueError("8-bit pools need float32 CUDA scales [Hkv]")
-                _check(lib.paged_kv_pool_create_fp8(
-                    ctypes.byref(h), k_pool.data_ptr(), v_pool.data_ptr(), k_scale.data_ptr(),
-                    v_scale.data_ptr(), self.num_blocks, self.block_size, self.num_kv_heads,
-                    self.head_dim), "paged_kv_pool_create_fp8")
+                            not sc.is_cuda or not sc.is_contiguous() or
+                            tuple(sc.shape) not in (per_head, per_block) or
+                            sc.shape != k_scale.shape):
+                        raise ValueError("8-bit pools need float32 contiguous CUDA scales "
+                                         "[Hkv] or [num_blocks, Hkv], the same for K and V")
+                self.scale_per_block = tuple(k_scale.shape) == per_block
+                _check(lib.paged_kv_pool_create_q8(
+                    ctypes.byref(h), k_pool.data_ptr(), v_pool.data_ptr(),
+                    _code_of(k_pool.dtype), k_scale.data_ptr(), v_scale.data_ptr(),
+                    _lib.PGD_SCALE_PER_BLOCK if self.scale_per_block else _lib.PGD_SCALE_PER_HEAD,
+                    self.num_blocks, self.block_size, self.num_kv_heads, self.head_dim),
+                    "paged_kv_pool_create_q8")
             else:
                 _check(lib.paged_kv_pool_create(ctypes.byref(h), k_pool.data_ptr(),
                                                 v_pool.data_ptr(), self.num_blocks,
@@ -295,7 +313,7 @@ def paged_gqa_plan(dtype, num_kv_heads, head_dim, B, Hq, q_len=1, num_splits=0, 
     if num_sms is None:
         num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     if isinstance(dtype, torch.dtype):
-        dtype = _lib.PGD_FP8_E4M3 if dtype in _FP8 else _DTYPES[dtype]
+        dtype = _code_of(dtype)
     plan = (ctypes.c_int * 5)()
     _check(_lib.load().paged_gqa_plan(int(dtype), int(num_kv_heads), int(head_dim), int(num_sms),
                                       int(B), int(q_len), int(Hq), int(num_splits), int(window),

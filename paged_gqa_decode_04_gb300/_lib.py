@@ -16,6 +16,9 @@ HEADERS = [HEADER, os.path.join(os.path.dirname(HERE), "include", "paged_kv_mana
 PGD_F32 = 0
 PGD_BF16 = 1
 PGD_FP8_E4M3 = 2
+PGD_INT8 = 3
+PGD_SCALE_PER_HEAD = 0
+PGD_SCALE_PER_BLOCK = 1
 
 STATUS_NAMES = {
     0: "PGD_OK", 1: "PGD_ERR_ARG", 2: "PGD_ERR_SHAPE", 3: "PGD_ERR_DTYPE", 4: "PGD_ERR_ALIGN",
@@ -51,6 +54,9 @@ def load(path=LIB_PATH):
     lib.paged_kv_pool_create_fp8.argtypes = [ctypes.POINTER(vp), vp, vp, vp, vp, i64, i32, i32,
                                              i32]
     lib.paged_kv_pool_create_fp8.restype = i32
+    lib.paged_kv_pool_create_q8.argtypes = [ctypes.POINTER(vp), vp, vp, i32, vp, vp, i32, i64,
+                                            i32, i32, i32]
+    lib.paged_kv_pool_create_q8.restype = i32
     lib.paged_kv_pool_destroy.argtypes = [vp]
     lib.paged_kv_pool_destroy.restype = i32
     lib.paged_gqa_workspace_size.argtypes = [vp, i32, i32, i32, ctypes.POINTER(sz)]

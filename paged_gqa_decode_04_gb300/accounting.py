@@ -15,8 +15,8 @@ the split-KV workspace are not counted.
 """
 import numpy as np
 
-ELT = {"f32": 4, "bf16": 2, "fp8": 1}      # K/V element bytes
-Q_ELT = {"f32": 4, "bf16": 2, "fp8": 2}    # q / out element bytes (bf16 with 8-bit pages)
+ELT = {"f32": 4, "bf16": 2, "fp8": 1, "i8": 1}      # K/V element bytes
+Q_ELT = {"f32": 4, "bf16": 2, "fp8": 2, "i8": 2}    # q / out element bytes (bf16 with 8-bit pages)
 
 
 def kv_bytes_per_token(hkv, d, elt):
@@ -29,14 +29,16 @@ def gqa_reduction_factor(hq, hkv):
     return kv_bytes_per_token(hq, 1, 1) / kv_bytes_per_token(hkv, 1, 1)
 
 
-def algorithmic_bytes(lens, hq, hkv, d, block_size, elt, q_elt=None):
-    """elt: K/V element bytes; q_elt: q / out element bytes (default elt)."""
+def algorithmic_bytes(lens, hq, hkv, d, block_size, elt, q_elt=None, block_scales=False):
+    """elt: K/V element bytes; q_elt: q / out element bytes (default elt);
+    block_scales: 8-bit pages with a K and a V float32 scale per block and KV
+    head, read once for every block used (8 * Hkv bytes per block)."""
     q_elt = elt if q_elt is None else q_elt
     lens = np.asarray(lens, dtype=np.int64)
     pages = int(np.sum((lens + block_size - 1) // block_size))
     B = int(lens.size)
     return (int(lens.sum()) * kv_bytes_per_token(hkv, d, elt) + 2 * B * hq * d * q_elt
-            + 4 * (B + pages))
+            + 4 * (B + pages) + (8 * hkv * pages if block_scales else 0))
 
 
 def flops(lens, hq, d):
@@ -53,10 +55,11 @@ def tokens_read(L, q_len=1, window=0):
     return max(0, L - lo)
 
 
-def algorithmic_bytes_ex(lens, hq, hkv, d, block_size, elt, q_len=1, window=0, q_elt=None):
+def algorithmic_bytes_ex(lens, hq, hkv, d, block_size, elt, q_len=1, window=0, q_elt=None,
+                         block_scales=False):
     """Algorithmic bytes of a multi-token / windowed call: K/V of the tokens
     read, q and out for q_len tokens per sequence, the table words of the
-    blocks read and seq_lens."""
+    blocks read and seq_lens (and the per-block scales of the blocks read)."""
     q_elt = elt if q_elt is None else q_elt
     lens = np.asarray(lens, dtype=np.int64)
     kv = 0
@@ -68,4 +71,5 @@ def algorithmic_bytes_ex(lens, hq, hkv, d, block_size, elt, q_len=1, window=0, q
             lo = L - n
             words += (L - 1) // block_size - lo // block_size + 1
     B = int(lens.size)
-    return kv + 2 * B * q_len * hq * d * q_elt + 4 * (B + words)
+    return (kv + 2 * B * q_len * hq * d * q_elt + 4 * (B + words)
+            + (8 * hkv * words if block_scales else 0))

@@ -20,6 +20,9 @@ namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// 8-bit pages (either code)
+bool is_q8(int dtype) { return dtype == PGD_FP8_E4M3 || dtype == PGD_INT8; }
+
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Make `dev` current for the scope of a call; restore the caller's device.
@@ -110,9 +113,9 @@ static int make_plan(int dtype, int hkv, int d, int num_sms, int B, int q_len, i
     if (hkv < 1 || Hq < 1 || B < 0 || q_len < 1 || num_sms < 1 || num_splits < 0 ||
         num_splits > (1 << 20) || window < 0)
         return PGD_ERR_ARG;
-    if (dtype != PGD_F32 && dtype != PGD_BF16 && dtype != PGD_FP8_E4M3) return PGD_ERR_DTYPE;
+    if (dtype != PGD_F32 && dtype != PGD_BF16 && !is_q8(dtype)) return PGD_ERR_DTYPE;
     if (d != 64 && d != 128) return PGD_ERR_SHAPE;
-    if (dtype == PGD_FP8_E4M3 && d != 128) return PGD_ERR_SHAPE;
+    if (is_q8(dtype) && d != 128) return PGD_ERR_SHAPE;
     if (Hq % hkv != 0) return PGD_ERR_SHAPE;
     const int rows = q_len * (Hq / hkv);
     if (rows > kMaxGroup) return PGD_ERR_SHAPE;
@@ -120,7 +123,7 @@ static int make_plan(int dtype, int hkv, int d, int num_sms, int B, int q_len, i
     Plan pl;
     pl.hg = choose_hg_for(dtype, hkv, rows);
     pl.m_tiles = (rows + 15) / 16;
-    pl.tile_tokens = dtype == PGD_F32 ? kSimpleTileTokens : (dtype == PGD_FP8_E4M3 ? 256 : 128) / pl.hg;
+    pl.tile_tokens = dtype == PGD_F32 ? kSimpleTileTokens : (is_q8(dtype) ? 256 : 128) / pl.hg;
     pl.parts = num_splits > 0 ? num_splits : num_sms;
     // Merge variant from the expected size of a split run's merge: about
     // parts / runs + 1 pieces per run, times the row passes of one warp.
@@ -191,20 +194,21 @@ using namespace pgd;
 extern "C" {
 
 static int pool_create(pgd_pool_t* out, const void* k_pool, const void* v_pool,
-                       const float* k_scale, const float* v_scale, int64_t num_blocks,
-                       int block_size, int num_kv_heads, int head_dim, int dtype) {
+                       const float* k_scale, const float* v_scale, int scale_per_block,
+                       int64_t num_blocks, int block_size, int num_kv_heads, int head_dim,
+                       int dtype) {
     if (!out) return PGD_ERR_ARG;
     *out = nullptr;
     if (!k_pool || !v_pool) return PGD_ERR_ARG;
     if (num_blocks < 1 || num_blocks > INT32_MAX || block_size < 1 || num_kv_heads < 1)
         return PGD_ERR_ARG;
-    if (dtype != PGD_F32 && dtype != PGD_BF16 && dtype != PGD_FP8_E4M3) return PGD_ERR_DTYPE;
+    if (dtype != PGD_F32 && dtype != PGD_BF16 && !is_q8(dtype)) return PGD_ERR_DTYPE;
     if (head_dim != 64 && head_dim != 128) return PGD_ERR_SHAPE;
     if (block_size > 1024) return PGD_ERR_SHAPE;
     if (dtype != PGD_F32 &&
         (block_size < 8 || block_size > 256 || (block_size & (block_size - 1)) != 0))
         return PGD_ERR_SHAPE;
-    if (dtype == PGD_FP8_E4M3) {
+    if (is_q8(dtype)) {
         if (head_dim != 128) return PGD_ERR_SHAPE;
         if (!k_scale || !v_scale) return PGD_ERR_ARG;
         if (!aligned(k_scale, 4) || !aligned(v_scale, 4)) return PGD_ERR_ALIGN;
@@ -224,6 +228,7 @@ static int pool_create(pgd_pool_t* out, const void* k_pool, const void* v_pool,
     p.dtype = dtype;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
+    p.scale_per_block = scale_per_block;
     if (cudaGetDevice(&p.device) != cudaSuccess || p.device >= kMaxDevices ||
         cudaDeviceGetAttribute(&p.num_sms, cudaDevAttrMultiProcessorCount, p.device) !=
             cudaSuccess ||
@@ -237,7 +242,7 @@ static int pool_create(pgd_pool_t* out, const void* k_pool, const void* v_pool,
         return PGD_ERR_CUDA;
     }
     if (dtype != PGD_F32) {
-        const bool fp8 = dtype == PGD_FP8_E4M3;
+        const bool fp8 = is_q8(dtype);  // 8-bit pages of either code: uint8 tensor maps
         for (int i = 0; i < 4; ++i) {
             const int hg = 1 << i;
             if (num_kv_heads % hg != 0) continue;
@@ -259,16 +264,28 @@ static int pool_create(pgd_pool_t* out, const void* k_pool, const void* v_pool,
 int paged_kv_pool_create(pgd_pool_t* out, const void* k_pool, const void* v_pool,
                          int64_t num_blocks, int block_size, int num_kv_heads, int head_dim,
                          int dtype) {
-    if (dtype == PGD_FP8_E4M3) return PGD_ERR_ARG;  // needs scales: paged_kv_pool_create_fp8
-    return pool_create(out, k_pool, v_pool, nullptr, nullptr, num_blocks, block_size,
+    if (is_q8(dtype)) return PGD_ERR_ARG;  // needs scales: paged_kv_pool_create_q8
+    return pool_create(out, k_pool, v_pool, nullptr, nullptr, 0, num_blocks, block_size,
                        num_kv_heads, head_dim, dtype);
 }
 
 int paged_kv_pool_create_fp8(pgd_pool_t* out, const void* k_pool, const void* v_pool,
                              const float* k_scale, const float* v_scale, int64_t num_blocks,
                              int block_size, int num_kv_heads, int head_dim) {
-    return pool_create(out, k_pool, v_pool, k_scale, v_scale, num_blocks, block_size,
+    return pool_create(out, k_pool, v_pool, k_scale, v_scale, 0, num_blocks, block_size,
                        num_kv_heads, head_dim, PGD_FP8_E4M3);
+}
+
+int paged_kv_pool_create_q8(pgd_pool_t* out, const void* k_pool, const void* v_pool, int code,
+                            const float* k_scale, const float* v_scale, int granularity,
+                            int64_t num_blocks, int block_size, int num_kv_heads, int head_dim) {
+    if (out) *out = nullptr;
+    if (!is_q8(code)) return PGD_ERR_DTYPE;
+    if (granularity != PGD_SCALE_PER_HEAD && granularity != PGD_SCALE_PER_BLOCK)
+        return PGD_ERR_ARG;
+    return pool_create(out, k_pool, v_pool, k_scale, v_scale,
+                       granularity == PGD_SCALE_PER_BLOCK ? 1 : 0, num_blocks, block_size,
+                       num_kv_heads, head_dim, code);
 }
 
 int paged_kv_pool_destroy(pgd_pool_t pool) {
@@ -349,6 +366,7 @@ int paged_gqa_decode_ex(pgd_pool_t pool, const void* q, int B, int q_len, int Hq
     a.scale_log2 = scale * 1.4426950408889634f;
     a.k_scale = p.k_scale;
     a.v_scale = p.v_scale;
+    a.scale_per_block = p.scale_per_block;
     a.num_parts = parts;
     a.auto_parts = num_splits == 0;
     a.hg = hg;

@@ -132,6 +132,13 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
     return v;
 }
 
+// Relaxed (morally strong, unordered) read: a later fence makes it an acquire.
+__device__ __forceinline__ int ld_relaxed(const int* p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void st_release(int* p, int v) {
     asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -247,6 +254,26 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
     return r;
 }
 
+// Two int8 codes (low byte -> low half) to two f16, exactly.  Each byte b,
+// with its sign bit flipped, is placed as the low byte under an 0x64 high
+// byte: the f16 with those bits is 1024 + (b + 128) (exponent 10, the byte as
+// the low mantissa bits), and subtracting 1152 leaves b.  Every value is an
+// integer below 2048, so each step is exact in f16.
+__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint16_t v) {
+    const uint32_t x = __byte_perm((uint32_t)v ^ 0x8080u, 0x64646464u, 0x5140);
+    const __half2 bias = __halves2half2(__ushort_as_half((unsigned short)0x6480),
+                                        __ushort_as_half((unsigned short)0x6480));
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&x), bias);
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// Two 8-bit codes of the page type to two f16.
+template <bool INT8>
+__device__ __forceinline__ uint32_t widen_x2(uint16_t v) {
+    if constexpr (INT8) return i8x2_to_f16x2(v);
+    else return e4m3x2_to_f16x2(v);
+}
+
 // Two bf16 (one 32-bit word) to two f16.
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
     __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&w);
@@ -255,14 +282,17 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
 }
 
 // ----------------------------------------------------------------- configuration
-template <int D_, int HG_, int MT_, int TG_, bool ROWS16_, bool FP8_ = false, int MV_ = 0>
+template <int D_, int HG_, int MT_, int TG_, bool ROWS16_, bool FP8_ = false, int MV_ = 0,
+          bool INT8_ = false, bool PB_ = false>
 struct Cfg {
     static constexpr int D = D_;
     static constexpr int HG = HG_;            // KV heads per unit of work
     static constexpr int MT = MT_;            // m16 row tiles of one head's query group
     static constexpr int TG = TG_;            // token groups per tile
     static constexpr bool ROWS16 = ROWS16_;   // rows 8..15 of an m-tile in use
-    static constexpr bool FP8 = FP8_;         // 8-bit (e4m3) K/V pages, f16 products
+    static constexpr bool FP8 = FP8_;         // 8-bit K/V pages, f16 products
+    static constexpr bool INT8 = INT8_;       // 8-bit pages hold int8 codes (else e4m3)
+    static constexpr bool PB = PB_;           // 8-bit pages with a scale per block and KV head
     // merge variant of split runs: 0 the last arriver merges with register
     // loads; 1 (SHARE, cooperative launch) all pieces' warps merge a share of
     // the rows; 2 (STAGE) the last arriver stages the pieces through the idle
@@ -285,6 +315,8 @@ struct Cfg {
     static constexpr int TENSOR_BYTES = HH * T * 128;   // K (or V) bytes of a stage
     static constexpr int STAGE_BYTES = 2 * TENSOR_BYTES;
     static constexpr int ROWS = ROWS16 ? 16 : 8;
+    // per-block scales of 8-bit pages: pages of a tile (block_size >= 8)
+    static constexpr int MAXP = FP8 ? (T / 8 < 32 ? T / 8 : 32) : 1;
     static constexpr int COMB_FLOATS = (TG - 1) * HG * MT * ROWS * (D + 2);
     static constexpr int COMB_BYTES = COMB_FLOATS * 4;
     static constexpr int STATIC_RESERVE = 4096;  // static smem + alignment slack
@@ -297,10 +329,12 @@ struct Cfg {
     static constexpr uint32_t MERGE_SLICE =
         (uint32_t)((STAGES * STAGE_BYTES + COMB_BYTES) / (HG * MT)) & ~15u;
     static_assert(!FP8 || D == 128, "8-bit pages: head_dim 128");
+    static_assert(!INT8 || FP8, "int8 codes are 8-bit pages");
+    static_assert(!PB || FP8, "per-block scales are for 8-bit pages");
     static_assert(STAGES >= 2, "pipeline needs at least two stages");
     static_assert(TW % 16 == 0, "a warp's token slice must be whole k16 steps");
     static_assert(TW % CH == 0 && CH % 16 == 0, "chunks must split the slice in k16 steps");
-    static_assert(THREADS <= 288, "at most 8 consumer warps");
+    static_assert(NC <= 8, "at most 8 consumer warps");
 };
 
 // A run whose pieces this warp brought to completion: merged after the tile loop.
@@ -350,15 +384,17 @@ __device__ __forceinline__ void lse_fold(float& M, float& W, float4& acc, float 
     // (M, W, acc) holds acc = sum_k 2^(lse_k - M) o_k and W = sum_k 2^(lse_k - M);
     // add a term that is (e, w, v) in the same form: a piece is (lse, 1, o),
     // another slot is (M', W', acc')
+    // explicit roundings: every merge (after the loop, inside it, staged)
+    // rounds the same way, whatever the compiler would contract
     const float nm = fmaxf(M, e);
     const float base = nm == -INFINITY ? 0.f : nm;
     const float sa = fast_exp2(M - base), sb = fast_exp2(e - base);
     M = nm;
-    W = W * sa + w * sb;
-    acc.x = acc.x * sa + v.x * sb;
-    acc.y = acc.y * sa + v.y * sb;
-    acc.z = acc.z * sa + v.z * sb;
-    acc.w = acc.w * sa + v.w * sb;
+    W = __fmaf_rn(W, sa, __fmul_rn(w, sb));
+    acc.x = __fmaf_rn(acc.x, sa, __fmul_rn(v.x, sb));
+    acc.y = __fmaf_rn(acc.y, sa, __fmul_rn(v.y, sb));
+    acc.z = __fmaf_rn(acc.z, sa, __fmul_rn(v.z, sb));
+    acc.w = __fmaf_rn(acc.w, sa, __fmul_rn(v.w, sb));
 }
 
 template <class C, bool PHASED>
@@ -524,6 +560,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     __shared__ StageDesc desc[S];
     __shared__ MergeJob jobs[C::NC][2];  // per consumer warp and partial slot
     __shared__ __align__(8) uint64_t merge_bar[C::STAGE ? C::NC : 1];  // STAGE: staging barriers
+    // 8-bit pages with per-block scales: K (0) and V (1) scale of every head
+    // of the unit for each page of the tile in a stage
+    __shared__ float qsc[C::PB ? S : 1][2][C::HG][C::PB ? C::MAXP : 1];
     __shared__ volatile int aborted;
 
     uint8_t* stage_base = reinterpret_cast<uint8_t*>(
@@ -537,9 +576,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int R = bs < T ? bs : T;
     const int log_r = __ffs(R) - 1;
 
+    // 8-bit pages with per-block scales: the producer publishes each stage's
+    // scales after issuing its copies, with a second arrival on the stage
+    constexpr bool pbs = C::PB;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&full_bar[s]), pbs ? 2 : 1);
             mbar_init(smem_u32(&empty_bar[s]), C::NC * 32);
         }
         mbar_init(smem_u32(&comb_bar), C::NC * 32);
@@ -617,6 +659,19 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const bool ok = want && phys >= 0 && phys < a.num_blocks;
             const bool bad = __any_sync(0xffffffffu, want && !ok);
             const int nok = __popc(__ballot_sync(0xffffffffu, ok));
+            // per-block scales of page `lane` for the unit's heads, loaded
+            // before the wait and published after the copies are issued;
+            // pages not fetched get 0 (their tokens are masked, their V rows
+            // zeroed, so the factor only has to be finite)
+            float ksv[C::HG], vsv[C::HG];
+            if constexpr (pbs) {
+                const int64_t sb = ok ? (int64_t)phys * a.hkv + (int64_t)cur.unit * C::HG : -1;
+#pragma unroll
+                for (int h = 0; h < C::HG; ++h) {
+                    ksv[h] = sb >= 0 ? __ldg(a.k_scale + sb + h) : 0.f;
+                    vsv[h] = sb >= 0 ? __ldg(a.v_scale + sb + h) : 0.f;
+                }
+            }
             const int flags =
                 segment_flags(x, cur.run_start, cur.n_b, r0, r1) | (bad ? kTileBad : 0);
 
@@ -644,6 +699,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 tma_load_4d(dst, &tmap_k, fb, 0, slot0, hh0, (int)phys, policy);
                 tma_load_4d(dst + C::TENSOR_BYTES, &tmap_v, fb, 0, slot0, hh0, (int)phys, policy);
             }
+            if constexpr (pbs) {
+                if (lane < C::MAXP) {
+#pragma unroll
+                    for (int h = 0; h < C::HG; ++h) {
+                        qsc[s][0][h][lane] = ksv[h];
+                        qsc[s][1][h][lane] = vsv[h];
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(fb);  // second arrival: the scales are in place
+            }
             cursor_next(cur, a.seq_lens, a.B, a.units, T, a.q_len, a.window, a.max_blocks, bs);
         }
         // Do not leave while copies this CTA issued may still land.
@@ -656,14 +722,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         return;
     }
 
+    const int rows = a.q_len * a.group;  // query rows per KV head
+    constexpr int RPP = 32 / (D / 4);    // rows per merge pass
+
     // ================================================================ consumers
     const int tg = warp % C::TG;
     const int mt = (warp / C::TG) % C::MT;
     const int hgi = warp / (C::TG * C::MT);
     const int gid = lane >> 2, tig = lane & 3;
     const int tw0 = tg * C::TW;
-    const int G = a.group;
-    const int rows = a.q_len * G;        // query rows per KV head: (token i, head g) = (r / G, r % G)
+    const int G = a.group;               // query row r is (token r / G, head r % G)
     const int row0 = mt * 16 + gid;      // row of accumulator rows c0,c1
     const int row1 = row0 + 8;           // row of c2,c3
     const bool row0_ok = row0 < rows;
@@ -713,8 +781,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 qa[ks][2] = row0_ok ? bf16x2_to_f16x2(__ldg(q0 + c + 1)) : 0u;
                 qa[ks][3] = row1_ok ? bf16x2_to_f16x2(__ldg(q1 + c + 1)) : 0u;
             }
-            s_mul = a.scale_log2 * __ldg(a.k_scale + q_kvh);
-            v_mul = __ldg(a.v_scale + q_kvh);
+            if constexpr (pbs) {  // scales per page, applied per n-tile
+                s_mul = a.scale_log2;
+                v_mul = 1.f;
+            } else {
+                s_mul = a.scale_log2 * __ldg(a.k_scale + q_kvh);
+                v_mul = __ldg(a.v_scale + q_kvh);
+            }
         } else {
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
@@ -749,6 +822,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (__any_sync(0xffffffffu, aborted)) break;
         const StageDesc dsc = desc[s];
         uint8_t* st = stage_base + s * C::STAGE_BYTES;
+        // the CTA's final piece of a split run reads its run's counter now
+        // (relaxed; the merge after the loop fences first), so that if every
+        // other piece is in already it skips its fence and arrival
+        int pre_cnt = 0;
+        if (!C::SHARE && it == n_tiles - 1 && tg == 0 && (dsc.flags & kSegEnd) &&
+            (dsc.flags & kSegPartial))
+            pre_cnt = ld_relaxed(a.counters +
+                                 ((int64_t)dsc.b * a.hkv + dsc.unit * C::HG + hgi) * C::MT + mt);
         const uint32_t k_u = smem_u32(st);
         const uint32_t v_u = k_u + C::TENSOR_BYTES;
         const int kvh = dsc.unit * C::HG + hgi;
@@ -815,8 +896,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
                             for (int q = 0; q < 4; ++q) {
                                 mma_f16(sc[jp + (q & 1)], qa[ks + (q >> 1)],
-                                        e4m3x2_to_f16x2((uint16_t)(w[q] & 0xffffu)),
-                                        e4m3x2_to_f16x2((uint16_t)(w[q] >> 16)));
+                                        widen_x2<C::INT8>((uint16_t)(w[q] & 0xffffu)),
+                                        widen_x2<C::INT8>((uint16_t)(w[q] >> 16)));
                             }
                         }
                     }
@@ -841,6 +922,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const int lo0 = a.window > 0 ? hi0 - a.window : INT_MIN;
                 const int lo1 = a.window > 0 ? hi1 - a.window : INT_MIN;
                 float mx0 = -INFINITY, mx1 = -INFINITY;
+                // logit multiplier of each n-tile (8 tokens, one page): with
+                // per-block scales, times the K scale of the tile's page
+                float smj[C::CH / 8];
+#pragma unroll
+                for (int j = 0; j < C::CH / 8; ++j) smj[j] = s_mul;
+                if constexpr (pbs) {
+#pragma unroll
+                    for (int j = 0; j < C::CH / 8; ++j)
+                        smj[j] = s_mul * qsc[s][0][hgi][(c0 + 8 * j) >> log_r];
+                }
                 // every row sees all of this warp's tokens (the usual case): no mask
                 const bool full = c0 + C::CH <= dsc.L - a.q_len + 1 - dsc.tok0 &&
                                   (a.window == 0 || c0 >= dsc.L - a.window - dsc.tok0);
@@ -849,8 +940,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     for (int j = 0; j < C::CH / 8; ++j) {
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
-                            sc[j][e] *= s_mul;
-                            sc[j][2 + e] *= s_mul;
+                            sc[j][e] *= smj[j];
+                            sc[j][2 + e] *= smj[j];
                             mx0 = fmaxf(mx0, sc[j][e]);
                             mx1 = fmaxf(mx1, sc[j][2 + e]);
                         }
@@ -863,8 +954,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             const int tok = c0 + j * 8 + tig * 2 + e;
                             const bool v0 = tok < hi0 && tok >= lo0;
                             const bool v1 = tok < hi1 && tok >= lo1;
-                            sc[j][e] = v0 ? sc[j][e] * s_mul : -INFINITY;
-                            sc[j][2 + e] = v1 ? sc[j][2 + e] * s_mul : -INFINITY;
+                            sc[j][e] = v0 ? sc[j][e] * smj[j] : -INFINITY;
+                            sc[j][2 + e] = v1 ? sc[j][2 + e] * smj[j] : -INFINITY;
                             mx0 = fmaxf(mx0, sc[j][e]);
                             mx1 = fmaxf(mx1, sc[j][2 + e]);
                         }
@@ -922,10 +1013,21 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         // 2 c + par then holds d = 16 c + 2 j + par for B column j, so
                         // the output columns come out permuted (undone where O is stored).
                         uint32_t pa[4];
-                        pa[0] = pack_f16(sc[2 * kk][0], sc[2 * kk][1]);
-                        pa[1] = pack_f16(sc[2 * kk][2], sc[2 * kk][3]);
-                        pa[2] = pack_f16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-                        pa[3] = pack_f16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+                        if constexpr (pbs) {
+                            // per-block V scales folded into P (the row sums
+                            // above use P itself)
+                            const float v0 = qsc[s][1][hgi][(c0 + 16 * kk) >> log_r];
+                            const float v1 = qsc[s][1][hgi][(c0 + 16 * kk + 8) >> log_r];
+                            pa[0] = pack_f16(sc[2 * kk][0] * v0, sc[2 * kk][1] * v0);
+                            pa[1] = pack_f16(sc[2 * kk][2] * v0, sc[2 * kk][3] * v0);
+                            pa[2] = pack_f16(sc[2 * kk + 1][0] * v1, sc[2 * kk + 1][1] * v1);
+                            pa[3] = pack_f16(sc[2 * kk + 1][2] * v1, sc[2 * kk + 1][3] * v1);
+                        } else {
+                            pa[0] = pack_f16(sc[2 * kk][0], sc[2 * kk][1]);
+                            pa[1] = pack_f16(sc[2 * kk][2], sc[2 * kk][3]);
+                            pa[2] = pack_f16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+                            pa[3] = pack_f16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+                        }
                         const int tok = c0 + kk * 16 + (lm_mi & 1) * 8 + lm_i;
 #pragma unroll
                         for (int c2 = 0; c2 < D / 32; ++c2) {
@@ -938,10 +1040,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
                             for (int h = 0; h < 2; ++h) {  // chunk 2 c2 + h: r[2h] tokens 0-7, r[2h+1] 8-15
                                 const int n = 4 * c2 + 2 * h;
-                                mma_f16(o[n], pa, e4m3x2_to_f16x2((uint16_t)(r[2 * h] & 0xffffu)),
-                                        e4m3x2_to_f16x2((uint16_t)(r[2 * h + 1] & 0xffffu)));
-                                mma_f16(o[n + 1], pa, e4m3x2_to_f16x2((uint16_t)(r[2 * h] >> 16)),
-                                        e4m3x2_to_f16x2((uint16_t)(r[2 * h + 1] >> 16)));
+                                mma_f16(o[n], pa, widen_x2<C::INT8>((uint16_t)(r[2 * h] & 0xffffu)),
+                                        widen_x2<C::INT8>((uint16_t)(r[2 * h + 1] & 0xffffu)));
+                                mma_f16(o[n + 1], pa, widen_x2<C::INT8>((uint16_t)(r[2 * h] >> 16)),
+                                        widen_x2<C::INT8>((uint16_t)(r[2 * h + 1] >> 16)));
                             }
                         }
                         continue;
@@ -1091,8 +1193,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
             continue;
         }
-        const int64_t slot = (int64_t)blockIdx.x * 2 + ((dsc.flags & kSegSlot1) ? 1 : 0);
+        // The pieces of run [t0, t0 + n_b): with P <= N every span holds at
+        // least one tile, so they are CTAs c0..c1; with P > N every span holds
+        // at most one tile, so piece k is the owner of tile t0 + k.
+        const int64_t t0 = dsc.run_start;
+        const int64_t N = ss.n_total, P = ss.parts;
+        const int64_t c0 = span_owner(t0, N, P);
+        const int npieces = P > N ? dsc.n_b : (int)(span_owner(t0 + dsc.n_b - 1, N, P) - c0 + 1);
+        const bool first_is_tail = P <= N && span_begin(c0, N, P) < t0;
         const int prow0 = hgi * rows + row0, prow1 = hgi * rows + row1;  // rows of the piece
+        const int64_t slot = (int64_t)blockIdx.x * 2 + ((dsc.flags & kSegSlot1) ? 1 : 0);
         {
             float* po = a.part_o + slot * piece_rows * D;
             if constexpr (C::FP8) {
@@ -1134,22 +1244,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // loop, waits for the flip and merges a share of the rows.  Otherwise
         // the last warp merges all rows.  No second kernel, no atomics at the
         // end.
-        __threadfence();
+        const int pre = __shfl_sync(0xffffffffu, pre_cnt, 0);
+        // final piece, every other piece counted: no fence, no arrival (this
+        // warp merges after its loop, reading its own rows after __syncwarp)
+        const bool known_last = !C::SHARE && it == n_tiles - 1 &&
+                                (pre & kRunCountMask) == npieces - 1;
+        if (!known_last) __threadfence();
         __syncwarp();
-        const int64_t t0 = dsc.run_start;
-        const int64_t N = ss.n_total, P = ss.parts;
-        // The pieces of run [t0, t0 + n_b): with P <= N every span holds at
-        // least one tile, so they are CTAs c0..c1; with P > N every span holds
-        // at most one tile, so piece k is the owner of tile t0 + k.
-        const int64_t c0 = span_owner(t0, N, P);
-        const int npieces = P > N ? dsc.n_b : (int)(span_owner(t0 + dsc.n_b - 1, N, P) - c0 + 1);
-        const bool first_is_tail = P <= N && span_begin(c0, N, P) < t0;
         if (lane == 0) {
             int* word = a.counters + ((int64_t)dsc.b * a.hkv + kvh) * C::MT + mt;
             const int js = (dsc.flags & kSegSlot1) ? 1 : 0;  // one piece per partial slot and CTA
-            const int old = atomicAdd(word, 1);
+            const int old = known_last ? pre : atomicAdd(word, 1);
             const int flag = (old >> kRunFlagShift) & 1;  // cannot flip before I arrive
             const bool last = (old & kRunCountMask) == npieces - 1;
+
             if constexpr (C::SHARE) {
                 const int nr = min(rows - mt * 16, C::ROWS);
                 constexpr int RPP = 32 / (D / 4);          // rows per merge pass
@@ -1180,7 +1288,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     // ---- merge the split runs recorded above
     if (__any_sync(0xffffffffu, aborted)) return;
-    constexpr int RPP = 32 / (D / 4);  // rows per merge pass
     const int r_mine = mt * 16, r_end = min(rows, r_mine + C::ROWS);
     uint32_t mphase = 0;
     if constexpr (C::STAGE) {
@@ -1307,40 +1414,41 @@ constexpr int token_groups(int t, int hg, int mt) {
     return by_tokens < by_warps ? by_tokens : by_warps;
 }
 
-template <int D, int HG, int MT, bool R16, bool FP8, int MV>
+template <int D, int HG, int MT, bool R16, bool FP8, int MV, bool INT8, bool PB>
 cudaError_t launch_hg(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
     constexpr int TG = token_groups((FP8 ? 256 : 128) / HG, HG, MT);
     const int idx = HG == 1 ? 0 : HG == 2 ? 1 : HG == 4 ? 2 : 3;
-    return launch_cfg<Cfg<D, HG, MT, TG, R16, FP8, MV>>(a, p.tmap_k[idx], p.tmap_v[idx],
-                                                          p.num_sms, p.device, s);
+    return launch_cfg<Cfg<D, HG, MT, TG, R16, FP8, MV, INT8, PB>>(
+        a, p.tmap_k[idx], p.tmap_v[idx], p.num_sms, p.device, s);
 }
 
-template <int D, int MT, bool R16, bool FP8, int MV>
+template <int D, int MT, bool R16, bool FP8, int MV, bool INT8, bool PB>
 cudaError_t launch_mt(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
     switch (a.hg) {
-        case 1: return launch_hg<D, 1, MT, R16, FP8, MV>(a, p, s);
-        case 2: return launch_hg<D, 2, MT, R16, FP8, MV>(a, p, s);
+        case 1: return launch_hg<D, 1, MT, R16, FP8, MV, INT8, PB>(a, p, s);
+        case 2: return launch_hg<D, 2, MT, R16, FP8, MV, INT8, PB>(a, p, s);
         case 4:
-            if constexpr (MT <= 2) return launch_hg<D, 4, MT, R16, FP8, MV>(a, p, s);
+            if constexpr (MT <= 2) return launch_hg<D, 4, MT, R16, FP8, MV, INT8, PB>(a, p, s);
             break;
         case 8:
-            if constexpr (MT == 1) return launch_hg<D, 8, MT, R16, FP8, MV>(a, p, s);
+            if constexpr (MT == 1) return launch_hg<D, 8, MT, R16, FP8, MV, INT8, PB>(a, p, s);
             break;
     }
     return cudaErrorInvalidValue;
 }
 
-// FP8: 8-bit (e4m3) K/V pages (head_dim 128 only).
+// FP8: 8-bit K/V pages (head_dim 128 only), INT8: of int8 codes (else e4m3),
+// PB: with a scale per block and KV head (else per KV head).
 // MV: merge variant (see Cfg).  The shared variant (1) returns
 // cudaErrorCooperativeLaunchTooLarge when the grid cannot be resident at once.
-template <int D, bool FP8, int MV>
+template <int D, bool FP8, int MV, bool INT8 = false, bool PB = false>
 cudaError_t launch_tma_d(const DecodeArgs& a, const Pool& p, cudaStream_t s) {
     const int rows = a.q_len * a.group;  // query rows per KV head
-    if (rows <= 8) return launch_mt<D, 1, false, FP8, MV>(a, p, s);
-    if (rows <= 16) return launch_mt<D, 1, true, FP8, MV>(a, p, s);
-    if (rows <= 32) return launch_mt<D, 2, true, FP8, MV>(a, p, s);
-    if (rows <= 48) return launch_mt<D, 3, true, FP8, MV>(a, p, s);
-    return launch_mt<D, 4, true, FP8, MV>(a, p, s);
+    if (rows <= 8) return launch_mt<D, 1, false, FP8, MV, INT8, PB>(a, p, s);
+    if (rows <= 16) return launch_mt<D, 1, true, FP8, MV, INT8, PB>(a, p, s);
+    if (rows <= 32) return launch_mt<D, 2, true, FP8, MV, INT8, PB>(a, p, s);
+    if (rows <= 48) return launch_mt<D, 3, true, FP8, MV, INT8, PB>(a, p, s);
+    return launch_mt<D, 4, true, FP8, MV, INT8, PB>(a, p, s);
 }
 
 }  // namespace tma

@@ -1,0 +1,10 @@
+// The TMA decode kernel for 8-bit K/V pages of e4m3 codes with a scale per
+// block and KV head, head_dim 128, staged-merge variant.
+#include "decode_tma.cuh"
+
+namespace pgd {
+namespace tma {
+template cudaError_t launch_tma_d<128, true, 2, false, true>(const DecodeArgs&, const Pool&,
+                                                           cudaStream_t);
+}  // namespace tma
+}  // namespace pgd

@@ -37,16 +37,26 @@ __global__ void __launch_bounds__(kWriteThreads)
     }
 }
 
-// Block y of the grid copies chunk blockIdx.x of block pair y (K and V).
+// Block y of the grid copies chunk blockIdx.x of block pair y (K and V), and,
+// for 8-bit pages with a scale per block and KV head (k_scale / v_scale
+// non-null, [num_blocks][hkv]), chunk 0 also copies the pair's scale rows: a
+// copied block keeps the range its codes were written with.
 __global__ void __launch_bounds__(kWriteThreads)
     copy_blocks_kernel(const int32_t* __restrict__ src, const int32_t* __restrict__ dst,
                        int64_t num_blocks, int64_t block_vec, uint4* __restrict__ k_pool,
-                       uint4* __restrict__ v_pool, int* err) {
+                       uint4* __restrict__ v_pool, float* __restrict__ k_scale,
+                       float* __restrict__ v_scale, int hkv, int* err) {
     const int pair = blockIdx.y;
     const int64_t s = src[pair], d = dst[pair];
     if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
         if (blockIdx.x == 0 && threadIdx.x == 0) atomicCAS(err, 0, PGD_ERR_BLOCK_ID);
         return;
+    }
+    if (k_scale && blockIdx.x == 0) {
+        for (int h = threadIdx.x; h < hkv; h += kWriteThreads) {
+            k_scale[d * hkv + h] = k_scale[s * hkv + h];
+            v_scale[d * hkv + h] = v_scale[s * hkv + h];
+        }
     }
     const int64_t per = (block_vec + gridDim.x - 1) / gridDim.x;
     const int64_t lo = blockIdx.x * per;
@@ -103,7 +113,9 @@ extern "C" int paged_kv_copy_blocks(pgd_pool_t pool, const int32_t* src, const i
     if (prev != p.device && cudaSetDevice(p.device) != cudaSuccess) return PGD_ERR_CUDA;
     copy_blocks_kernel<<<dim3(chunks, n), kWriteThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         src, dst, p.num_blocks, block_vec, static_cast<uint4*>(const_cast<void*>(p.k)),
-        static_cast<uint4*>(const_cast<void*>(p.v)), p.err);
+        static_cast<uint4*>(const_cast<void*>(p.v)),
+        p.scale_per_block ? const_cast<float*>(p.k_scale) : nullptr,
+        p.scale_per_block ? const_cast<float*>(p.v_scale) : nullptr, p.hkv, p.err);
     const cudaError_t e = cudaGetLastError();
     if (prev != p.device) cudaSetDevice(prev);
     return e == cudaSuccess ? PGD_OK : PGD_ERR_CUDA;

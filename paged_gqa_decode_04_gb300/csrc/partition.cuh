@@ -150,20 +150,28 @@ struct TileCursor {
     int64_t run_start;       // flat index of tile 0 of (b, unit)
 };
 
+// Cursor at flat tile x, which sequence b (first tile b_base) holds.
+__device__ inline TileCursor cursor_at_tile(int64_t x, int b, int64_t b_base,
+                                            const int32_t* seq_lens, int T, int q_len,
+                                            int window, int max_blocks, int block_size) {
+    TileCursor c;
+    c.b = b;
+    const int L = seq_lens[b];
+    c.n_b = tiles_of(L, max_blocks, block_size, T, q_len, window);
+    c.first = first_tile_of(L, T, q_len, window);
+    int64_t off = x - b_base;
+    c.unit = (int)(off / c.n_b);
+    c.i = (int)(off % c.n_b);
+    c.run_start = b_base + (int64_t)c.unit * c.n_b;
+    return c;
+}
+
 __device__ inline TileCursor cursor_at(const SpanStart& s, const int32_t* seq_lens, int units,
                                        int T, int q_len, int window, int max_blocks,
                                        int block_size) {
-    TileCursor c;
-    c.b = s.b;
-    const int L = seq_lens[s.b];
-    c.n_b = tiles_of(L, max_blocks, block_size, T, q_len, window);
-    c.first = first_tile_of(L, T, q_len, window);
-    int64_t off = s.r0 - s.b_base;
-    c.unit = (int)(off / c.n_b);
-    c.i = (int)(off % c.n_b);
-    c.run_start = s.b_base + (int64_t)c.unit * c.n_b;
     (void)units;
-    return c;
+    return cursor_at_tile(s.r0, s.b, s.b_base, seq_lens, T, q_len, window, max_blocks,
+                          block_size);
 }
 
 __device__ inline void cursor_next(TileCursor& c, const int32_t* seq_lens, int B, int units,

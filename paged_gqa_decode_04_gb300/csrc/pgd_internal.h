@@ -38,8 +38,9 @@ struct Pool {
     int device;
     int num_sms;
     int* err;              // device error word (latched pgd_status)
-    const float* k_scale;  // 8-bit pages: per-KV-head scales [Hkv] (device), else null
+    const float* k_scale;  // 8-bit pages: scales [Hkv] or [num_blocks][Hkv] (device), else null
     const float* v_scale;
+    int scale_per_block;   // 8-bit pages: 1 when the scales are per block and KV head
     // bfloat16 TMA descriptors, one per head-group size HG = 1, 2, 4, 8 (index
     // log2 HG), valid where HG divides Hkv: 4-D view (d_lo 64, slot, head-half,
     // block) of the pool, box (64, min(bs, 128 / HG), HG * D / 64, 1).
@@ -67,8 +68,9 @@ struct DecodeArgs {
     int max_blocks;
     int64_t num_blocks;
     float scale_log2;      // scale * log2(e): logits kept in base-2 units
-    const float* k_scale;  // 8-bit pages: K / V scale per KV head (device)
-    const float* v_scale;
+    const float* k_scale;  // 8-bit pages: K / V scales per KV head [Hkv], or per physical
+    const float* v_scale;  // block and KV head [num_blocks][Hkv] (device)
+    int scale_per_block;   // which of the two
     int num_parts;         // CTAs of the decode grid (spans of the tile sequence)
     int auto_parts;        // num_parts came from num_splits == 0 (kernel may use fewer)
     int hg;                // KV heads per unit of work

@@ -39,10 +39,12 @@ def run_oracle(w, table=None, lens=None, q=None, window=None):
     table = w.table_np if table is None else table
     lens = w.lens_np if lens is None else lens
     qq = w.q if q is None else q
-    if w.dtype == "fp8":
-        return oracle.decode_kv8_f64(host(qq), host(w.k_pool), host(w.v_pool),
-                                     w.k_scale.cpu().numpy(), w.v_scale.cpu().numpy(), table,
-                                     lens, w.scale, window or 0)
+    if w.dtype in ("fp8", "i8"):
+        # 8-bit pages: e4m3 or int8 codes, scales per KV head or per block and KV head
+        return oracle.decode_q8_f64(host(qq), host(w.k_pool), host(w.v_pool),
+                                    "e4m3" if w.dtype == "fp8" else "int8",
+                                    w.k_scale.cpu().numpy(), w.v_scale.cpu().numpy(), table,
+                                    lens, w.scale, window or 0)
     if q is not None or window:
         return oracle.decode_ex_f64(host(qq), host(w.k_pool), host(w.v_pool), table, lens,
                                     w.scale, window or 0)
@@ -55,7 +57,7 @@ def errors(got, want):
     return g, float(e.max()), float(e.mean())
 
 
-# 8-bit pages: an output is (per-head float32 scale) x (e4m3 code) arithmetic,
+# 8-bit pages: an output is (float32 scale) x (e4m3 or int8 code) arithmetic,
 # not a bfloat16 value, so rounding it to the bfloat16 output adds up to half
 # an ulp, 2^-8 |out| (a one-token sequence returns a scaled V row of up to ~7);
 # bfloat16 pages return their bfloat16 rows exactly there.
@@ -66,7 +68,7 @@ def assert_close(got, want, dtype, what=""):
     g, emax, emean = errors(got, want)
     tmax, tmean = tol(dtype)
     assert np.isfinite(g).all(), "%s: non-finite output" % what
-    if dtype in ("fp8", torch.float8_e4m3fn):
+    if dtype in ("fp8", "i8", torch.float8_e4m3fn, torch.int8):
         excess = float((np.abs(g - want) - (tmax + FP8_REL * np.abs(want))).max())
         assert excess <= 0 and emean <= tmean, "%s: max %.3g (over the bound by %.3g) mean %.3g" % (
             what, emax, excess, emean)

@@ -90,6 +90,34 @@ def test_fp8_pool_create_rejects(lib):
     assert h.value is None
 
 
+def test_q8_pool_create_rejects(lib):
+    """The 8-bit pool entry of either code and scale granularity refuses bad
+    arguments before any CUDA call."""
+    h = ctypes.c_void_p()
+    f = lib.paged_kv_pool_create_q8
+    # unknown code, and a wide dtype passed as a code
+    assert f(ctypes.byref(h), 256, 256, 7, 256, 256, 0, 10, 16, 8, 128) == _lib.PGD_ERR_DTYPE
+    assert f(ctypes.byref(h), 256, 256, _lib.PGD_BF16, 256, 256, 0, 10, 16, 8,
+             128) == _lib.PGD_ERR_DTYPE
+    # unknown scale granularity
+    for code in (_lib.PGD_FP8_E4M3, _lib.PGD_INT8):
+        assert f(ctypes.byref(h), 256, 256, code, 256, 256, 2, 10, 16, 8, 128) == _lib.PGD_ERR_ARG
+        # missing scales, head_dim 64, misaligned scales, non-power-of-two block
+        for gran in (_lib.PGD_SCALE_PER_HEAD, _lib.PGD_SCALE_PER_BLOCK):
+            assert f(ctypes.byref(h), 256, 256, code, None, 256, gran, 10, 16, 8,
+                     128) == _lib.PGD_ERR_ARG
+            assert f(ctypes.byref(h), 256, 256, code, 256, 256, gran, 10, 16, 8,
+                     64) == _lib.PGD_ERR_SHAPE
+            assert f(ctypes.byref(h), 256, 256, code, 258, 256, gran, 10, 16, 8,
+                     128) == _lib.PGD_ERR_ALIGN
+            assert f(ctypes.byref(h), 256, 256, code, 256, 256, gran, 10, 24, 8,
+                     128) == _lib.PGD_ERR_SHAPE
+    # int8 pages need scales too: the plain create refuses the dtype
+    assert lib.paged_kv_pool_create(ctypes.byref(h), 256, 256, 10, 16, 8, 128,
+                                    _lib.PGD_INT8) == _lib.PGD_ERR_ARG
+    assert h.value is None
+
+
 def test_binding_checks_decode_arguments_before_the_library():
     """The Python face rejects malformed tensors before any call into the
     library: wrong ranks, dtypes, shapes, then anything not a contiguous CUDA

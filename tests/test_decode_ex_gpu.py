@@ -59,6 +59,13 @@ CASES = [
                            max_len=1024), 3, 40),                                # 8-token blocks
     ("mqa_13b_b8", dict(B=2, block_size=128, lens=[900, 300], max_len=1024), 1, 100),
     ("mha_13b_b8", dict(B=3, lens=[1000, 5, 260], max_len=1024), 2, 0),
+    # int8 pages and per-block scales: causal and window bounds inside tiles
+    # whose blocks carry different scales
+    ("llama3_8b_i8", dict(B=6, lens=("uniform", 50, 900), max_len=1024), 4, 0),
+    ("llama3_8b_i8_pb", dict(B=6, lens=("uniform", 50, 900), max_len=1024), 3, 40),
+    ("llama3_8b_fp8_pb", dict(B=6, block_size=8, lens=("lognormal", 200.0, 1.0, 1, 900),
+                              max_len=1024), 2, 100),
+    ("long_70b_i8_pb", dict(B=2, lens=[3000, 1000], max_len=4096), 8, 100),
 ]
 
 

@@ -23,8 +23,11 @@ def test_full_size_every_row(name):
     del w, out
 
 
-# 8-bit pages at full size.
-@pytest.mark.parametrize("name", ["llama3_8b_fp8", "long_70b_fp8"])
+# 8-bit pages at full size: e4m3 and int8 codes, scales per KV head and per
+# block and KV head.
+@pytest.mark.parametrize("name", ["llama3_8b_fp8", "long_70b_fp8", "llama3_8b_i8", "long_70b_i8",
+                                  "llama3_8b_fp8_pb", "long_70b_fp8_pb", "llama3_8b_i8_pb",
+                                  "long_70b_i8_pb"])
 def test_full_size_8bit_every_row(name):
     w = gen.make(name, device="cuda", poison=True)
     out, _ = run_cuda(w)
@@ -37,7 +40,8 @@ def test_full_size_8bit_every_row(name):
 # Several query tokens and windows at full size, as `bench.py --op decode_ex`
 # runs them (its query draw: a device generator seeded with seed + 7).
 EX_FULL = [("llama3_8b", 4, 0), ("llama3_8b", 4, 512), ("llama3_8b", 1, 1024),
-           ("long_70b", 1, 4096), ("llama3_8b_fp8", 4, 0)]
+           ("long_70b", 1, 4096), ("llama3_8b_fp8", 4, 0), ("llama3_8b_i8_pb", 4, 0),
+           ("llama3_8b_fp8_pb", 2, 512)]
 
 
 @pytest.mark.parametrize("name,q_len,window", EX_FULL)

@@ -41,12 +41,30 @@ def draw(case):
                 lens=lens, window=window, splits=splits, max_len=max_len)
 
 
-@pytest.mark.parametrize("case", range(N_CASES))
-def test_random_configuration_matches_oracle(case):
-    c = draw(case)
+# A second sweep over the 8-bit page types: e4m3 and int8 codes with scales
+# per KV head or per block and KV head (its own seeds, so the sweep above
+# keeps its draws).
+N_Q8_CASES = 32
+
+
+def draw_q8(case):
+    c = draw(7100 - 7000 + case)
+    rng = np.random.default_rng(7100 + case)
+    c["dtype"] = str(rng.choice(["fp8", "i8"]))
+    c["scales"] = str(rng.choice(["head", "block"]))
+    c["D"] = 128
+    if c["q_len"] == 1 and c["dtype"] != "f32":
+        c["q_len"] = int(rng.choice([1, 1, 2, 4]))
+    c["Hq"] = c["Hkv"] * max(1, min(c["Hq"] // c["Hkv"], 64 // c["q_len"]))
+    if c["block_size"] not in (8, 16, 32, 64, 128):
+        c["block_size"] = 16
+    return c
+
+
+def _run_case(c, case):
     w = gen.make("llama3_8b", device="cuda", poison=True, seed=7000 + case, B=c["B"],
                  lens=c["lens"], Hq=c["Hq"], Hkv=c["Hkv"], D=c["D"], block_size=c["block_size"],
-                 dtype=c["dtype"], max_len=c["max_len"])
+                 dtype=c["dtype"], max_len=c["max_len"], scales=c.get("scales", "head"))
     pool = pgd.PagedKVPool(w.k_pool, w.v_pool, w.k_scale, w.v_scale)
     try:
         if c["q_len"] == 1 and c["window"] == 0:
@@ -65,3 +83,13 @@ def test_random_configuration_matches_oracle(case):
         assert_close(out.view(want.shape), want, w.dtype, str(c))
     finally:
         pool.close()
+
+
+@pytest.mark.parametrize("case", range(N_CASES))
+def test_random_configuration_matches_oracle(case):
+    _run_case(draw(case), case)
+
+
+@pytest.mark.parametrize("case", range(N_Q8_CASES))
+def test_random_8bit_configuration_matches_oracle(case):
+    _run_case(draw_q8(case), 100 + case)

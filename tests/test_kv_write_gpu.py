@@ -25,36 +25,64 @@ def rand_rows(n, hkv, d, dtype, g):
 
 
 FP8 = torch.float8_e4m3fn
+I8 = torch.int8
 
 
-def make_pool(k, v):
-    if k.dtype == FP8:   # 8-bit pages: unit scales (the rows are codes already)
-        ones = torch.ones(k.shape[2], dtype=torch.float32, device=DEV)
-        return pgd.PagedKVPool(k, v, ones, ones.clone())
+def make_pool(k, v, per_block=False, unit=False):
+    """8-bit pages (the rows are codes already) get random scales per KV head
+    or per block and KV head, or unit per-head scales."""
+    if k.dtype in (FP8, I8):
+        shape = (k.shape[0], k.shape[2]) if per_block else (k.shape[2],)
+        if unit:
+            ones = torch.ones(shape, dtype=torch.float32, device=DEV)
+            return pgd.PagedKVPool(k, v, ones, ones.clone())
+        g = torch.Generator(device=DEV)
+        g.manual_seed(11)
+        ks = 0.5 + torch.rand(shape, generator=g, device=DEV, dtype=torch.float32)
+        vs = 0.5 + torch.rand(shape, generator=g, device=DEV, dtype=torch.float32)
+        return pgd.PagedKVPool(k, v, ks, vs)
     return pgd.PagedKVPool(k, v)
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32, FP8])
-def test_append_and_copy_match_reference(dtype):
+def rand_pages(shape, dtype, g):
+    if dtype == I8:
+        return torch.randint(-127, 128, shape, generator=g, device=DEV, dtype=torch.int32).to(I8)
+    return torch.randn(shape, generator=g, device=DEV).to(dtype)
+
+
+@pytest.mark.parametrize("dtype,per_block", [(torch.bfloat16, False), (torch.float32, False),
+                                             (FP8, False), (I8, False), (FP8, True), (I8, True)])
+def test_append_and_copy_match_reference(dtype, per_block):
     g = torch.Generator(device=DEV)
     g.manual_seed(3)
     nb, bs, hkv, d = 20, 16, 8, 128
-    k = torch.randn((nb, bs, hkv, d), generator=g, device=DEV).to(dtype)
-    v = torch.randn((nb, bs, hkv, d), generator=g, device=DEV).to(dtype)
-    pool = make_pool(k, v)
+    k = rand_pages((nb, bs, hkv, d), dtype, g)
+    v = rand_pages((nb, bs, hkv, d), dtype, g)
+    pool = make_pool(k, v, per_block)
     try:
         slots = torch.tensor([5, 16 * 3 + 7, 319, 0, 200], dtype=torch.int32, device=DEV)
-        kn, vn = rand_rows(5, hkv, d, dtype, g), rand_rows(5, hkv, d, dtype, g)
+        kn, vn = rand_pages((5, hkv, d), dtype, g), rand_pages((5, hkv, d), dtype, g)
         want_k, want_v = kv_write.append(bits(k), bits(v), bits(kn), bits(vn), slots.cpu().numpy())
         pgd.paged_kv_append(pool, kn, vn, slots)
         assert pgd.paged_gqa_get_error(pool) == 0
         assert np.array_equal(bits(k), want_k) and np.array_equal(bits(v), want_v)
         src = torch.tensor([3, 0, 7], dtype=torch.int32, device=DEV)
         dst = torch.tensor([11, 12, 19], dtype=torch.int32, device=DEV)
-        want_k, want_v = kv_write.copy_blocks(bits(k), bits(v), src.cpu().numpy(), dst.cpu().numpy())
+        if per_block:
+            want_k, want_v, want_ks, want_vs = kv_write.copy_blocks(
+                bits(k), bits(v), src.cpu().numpy(), dst.cpu().numpy(),
+                pool.k_scale.cpu().numpy(), pool.v_scale.cpu().numpy())
+        else:
+            want_k, want_v = kv_write.copy_blocks(bits(k), bits(v), src.cpu().numpy(),
+                                                  dst.cpu().numpy())
+            if pool.k_scale is not None:   # per-head scales: untouched
+                want_ks, want_vs = pool.k_scale.cpu().numpy(), pool.v_scale.cpu().numpy()
         pgd.paged_kv_copy_blocks(pool, src, dst)
         assert pgd.paged_gqa_get_error(pool) == 0
         assert np.array_equal(bits(k), want_k) and np.array_equal(bits(v), want_v)
+        if pool.k_scale is not None:
+            assert np.array_equal(pool.k_scale.cpu().numpy(), want_ks)
+            assert np.array_equal(pool.v_scale.cpu().numpy(), want_vs)
         # out-of-range slot: skipped and reported
         before = bits(k)
         bad = torch.tensor([nb * bs], dtype=torch.int32, device=DEV)
@@ -76,7 +104,7 @@ def test_cache_lifecycle_decode_matches_oracle(hkv, hq, d, dtype):
     nb, bs = 96, 16
     k = torch.full((nb, bs, hkv, d), float("nan"), device=DEV, dtype=dtype)
     v = torch.full_like(k, float("nan"))
-    pool = make_pool(k, v)
+    pool = make_pool(k, v, unit=True)
     m = pgd.KVBlockManager(nb, bs, max_seqs=8, max_blocks_per_seq=16)
     rows = {}                                     # seq -> list of (k_row, v_row) host bits
 

@@ -92,6 +92,19 @@ def pin_copy_blocks(mod):
     assert np.array_equal(k0, k_keep) and np.array_equal(v0, v_keep), "inputs modified"
 
 
+def pin_copy_blocks_scale_rows(mod):
+    # 8-bit pages with a scale per block and KV head: the copies 3 -> 0 and
+    # 1 -> 2 carry the scale rows, blocks 1 and 3 keep theirs
+    k0, v0 = _pool(4, 0), _pool(4, 1000)
+    ks = np.array([[0.5, 1.5], [2.5, 3.5], [4.5, 5.5], [6.5, 7.5]], dtype=np.float32)
+    vs = ks + 10
+    k, v, ks2, vs2 = mod.copy_blocks(k0, v0, np.array(COPY_SRC), np.array(COPY_DST), ks, vs)
+    assert np.array_equal(k, COPY_K_WANT) and np.array_equal(v, COPY_V_WANT)
+    assert ks2.tolist() == [[6.5, 7.5], [2.5, 3.5], [2.5, 3.5], [6.5, 7.5]]
+    assert vs2.tolist() == [[16.5, 17.5], [12.5, 13.5], [12.5, 13.5], [16.5, 17.5]]
+    assert ks.tolist()[0] == [0.5, 1.5], "input scales modified"
+
+
 def pin_empty_calls(mod):
     k0, v0 = _pool(2, 0), _pool(2, 1000)
     k, v = mod.append(k0, v0, np.zeros((0, 2, 1), np.int64), np.zeros((0, 2, 1), np.int64),
@@ -101,7 +114,8 @@ def pin_empty_calls(mod):
     assert np.array_equal(k, k0) and np.array_equal(v, v0)
 
 
-PINS = [pin_append, pin_append_bf16_bits, pin_copy_blocks, pin_empty_calls]
+PINS = [pin_append, pin_append_bf16_bits, pin_copy_blocks, pin_copy_blocks_scale_rows,
+        pin_empty_calls]
 
 
 def _load(src, name="kv_write_under_test"):
@@ -128,6 +142,10 @@ MUTANTS = {
     "copy_skips_v": ("v[d] = v[s]", "pass"),
     "copy_v_from_k": ("v[d] = v[s]", "v[d] = k[s]"),
     "in_place_update": ("k, v = k_pool.copy(), v_pool.copy()", "k, v = k_pool, v_pool"),
+    "scale_rows_not_copied": ("            ks[d] = ks[s]\n", "            pass\n"),
+    "v_scale_row_from_k": ("vs[d] = vs[s]", "vs[d] = ks[s]"),
+    "scale_copied_in_place": ("ks = None if k_scale is None else np.array(k_scale, copy=True)",
+                              "ks = k_scale"),
 }
 
 

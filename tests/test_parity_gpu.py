@@ -63,6 +63,35 @@ SMALL = {
     "tile_edges": ("llama3_8b", dict(B=8, lens=[15, 16, 17, 31, 32, 33, 127, 128], max_len=160)),
     "fp8_tile_edges": ("llama3_8b_fp8", dict(B=8, lens=[31, 32, 33, 63, 64, 65, 255, 256],
                                              max_len=288)),
+    # int8 pages (per-head scales) and 8-bit pages with a scale per block and
+    # KV head (e4m3 and int8): tiles of 32 tokens span 2-4 blocks of 8-16
+    # tokens, each with its own scale
+    "i8_llama3_small": ("llama3_8b_i8", dict(B=8, lens=("uniform", 1, 700), max_len=1024)),
+    "i8_long_small": ("long_70b_i8", dict(B=2, lens=("uniform", 2000, 4100), max_len=4224)),
+    "i8_mqa": ("llama3_8b_i8", dict(B=2, Hq=40, Hkv=1, lens=[517, 1], max_len=1024)),
+    "i8_hkv6": ("llama3_8b_i8", dict(B=3, Hq=24, Hkv=6, lens=[90, 300, 17], max_len=320)),
+    "fp8pb_llama3_small": ("llama3_8b_fp8_pb", dict(B=8, lens=("uniform", 1, 700),
+                                                    max_len=1024)),
+    "fp8pb_long_small": ("long_70b_fp8_pb", dict(B=2, lens=("uniform", 2000, 4100),
+                                                 max_len=4224)),
+    "fp8pb_bs8": ("llama3_8b_fp8_pb", dict(B=12, block_size=8,
+                                           lens=("lognormal", 200.0, 1.0, 1, 900), max_len=1024)),
+    "fp8pb_bs256": ("llama3_8b_fp8_pb", dict(B=3, block_size=256, lens=[700, 256, 3],
+                                             max_len=768)),
+    "fp8pb_mha": ("llama3_8b_fp8_pb", dict(B=2, Hq=40, Hkv=40, lens=[333, 64], max_len=512)),
+    "fp8pb_mqa": ("llama3_8b_fp8_pb", dict(B=2, Hq=40, Hkv=1, lens=[517, 1], max_len=1024)),
+    "fp8pb_hkv2_g16": ("llama3_8b_fp8_pb", dict(B=3, Hq=32, Hkv=2, lens=[90, 200, 17],
+                                                max_len=256)),
+    "i8pb_llama3_small": ("llama3_8b_i8_pb", dict(B=8, lens=("uniform", 1, 700), max_len=1024)),
+    "i8pb_long_small": ("long_70b_i8_pb", dict(B=2, lens=("uniform", 2000, 4100),
+                                               max_len=4224)),
+    "i8pb_bs8": ("llama3_8b_i8_pb", dict(B=12, block_size=8,
+                                         lens=("lognormal", 200.0, 1.0, 1, 900), max_len=1024)),
+    "i8pb_hkv4": ("llama3_8b_i8_pb", dict(B=5, Hq=16, Hkv=4, lens=[1, 65, 130, 64, 300],
+                                          max_len=320)),
+    "i8pb_mqa": ("llama3_8b_i8_pb", dict(B=2, Hq=40, Hkv=1, lens=[517, 1], max_len=1024)),
+    "i8pb_tile_edges": ("llama3_8b_i8_pb", dict(B=8, lens=[31, 32, 33, 63, 64, 65, 255, 256],
+                                                max_len=288)),
 }
 
 
@@ -233,9 +262,10 @@ def test_golden_fixture_on_gpu():
 
 
 @pytest.mark.parametrize("splits", [1, 7, 1000])
-def test_fp8_split_invariance_and_poison(splits):
-    w = gen.make("llama3_8b_fp8", device=DEV, B=6, lens=("uniform", 1, 2000), max_len=2048,
-                 poison=True)
+@pytest.mark.parametrize("recipe", ["llama3_8b_fp8", "llama3_8b_i8", "llama3_8b_fp8_pb",
+                                    "llama3_8b_i8_pb"])
+def test_8bit_split_invariance_and_poison(recipe, splits):
+    w = gen.make(recipe, device=DEV, B=6, lens=("uniform", 1, 2000), max_len=2048, poison=True)
     want, _ = run_oracle(w)
     out, _ = run_cuda(w, num_splits=splits)
-    assert_close(out, want, "fp8", "fp8 splits=%d" % splits)
+    assert_close(out, want, w.dtype, "%s splits=%d" % (recipe, splits))

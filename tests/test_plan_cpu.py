@@ -8,7 +8,7 @@ import torch
 import paged_gqa_decode_04_gb300 as pgd
 from paged_gqa_decode_04_gb300 import _lib
 
-BF16, FP8, F32 = torch.bfloat16, torch.float8_e4m3fn, torch.float32
+BF16, FP8, F32, I8 = torch.bfloat16, torch.float8_e4m3fn, torch.float32, torch.int8
 
 
 def plan(dtype, hkv, d, B, Hq, **kw):
@@ -35,6 +35,9 @@ CASES = [
     ("32 rows, B 8", (BF16, 8, 128, 8, 64), dict(q_len=4), (4, 2, 32, 152, "shared (cooperative)")),
     ("8-bit llama3", (FP8, 8, 128, 64, 32), {}, (8, 1, 32, 152, "last arriver")),
     ("8-bit long_70b", (FP8, 8, 128, 8, 64), {}, (8, 1, 32, 152, "shared (cooperative)")),
+    ("int8 llama3", (I8, 8, 128, 64, 32), {}, (8, 1, 32, 152, "last arriver")),
+    ("int8 long_70b", (I8, 8, 128, 8, 64), {}, (8, 1, 32, 152, "shared (cooperative)")),
+    ("int8 4 query tokens", (I8, 8, 128, 64, 32), dict(q_len=4), (8, 1, 32, 152, "staged")),
     ("head_dim 64", (BF16, 2, 64, 4, 8), {}, (2, 1, 64, 152, "last arriver")),
     ("Hkv 6", (BF16, 6, 128, 4, 24), {}, (2, 1, 64, 152, "last arriver")),
     ("float32 tiny", (F32, 2, 64, 4, 8), {}, (1, 1, 64, 152, "merge kernel")),
@@ -58,7 +61,7 @@ def test_plan_of_each_shape(name, args, kw, want):
 
 
 def test_plan_invariants():
-    for dtype in (BF16, FP8):
+    for dtype in (BF16, FP8, I8):
         for hkv in (1, 2, 3, 4, 5, 6, 8, 40):
             for G in (1, 2, 4, 8, 16, 40, 64):
                 for q_len in (1, 2, 4):
@@ -69,7 +72,7 @@ def test_plan_invariants():
                     assert hkv % hg == 0 and hg in (1, 2, 4, 8)
                     assert mt == (q_len * G + 15) // 16
                     assert hg * mt <= 8                       # at most 8 consumer warps
-                    assert T * hg == (256 if dtype == FP8 else 128)  # 64 KB stages
+                    assert T * hg == (128 if dtype == BF16 else 256)  # 64 KB stages
 
 
 @pytest.mark.parametrize("args,kw,status", [
@@ -78,6 +81,7 @@ def test_plan_invariants():
     ((BF16, 8, 128, 4, 32), dict(q_len=17), _lib.PGD_ERR_SHAPE),  # 68 rows per head
     ((BF16, 8, 96, 4, 32), {}, _lib.PGD_ERR_SHAPE),              # head_dim 96
     ((FP8, 8, 64, 4, 32), {}, _lib.PGD_ERR_SHAPE),               # 8-bit pages: head_dim 128
+    ((I8, 8, 64, 4, 32), {}, _lib.PGD_ERR_SHAPE),
     ((F32, 2, 64, 4, 8), dict(q_len=2), _lib.PGD_ERR_UNSUPPORTED),
     ((F32, 2, 64, 4, 8), dict(window=16), _lib.PGD_ERR_UNSUPPORTED),
     ((BF16, 8, 128, -1, 32), {}, _lib.PGD_ERR_ARG),
