@@ -372,6 +372,7 @@ int paged_gqa_decode_ex(pgd_pool_t pool, const void* q, int B, int q_len, int Hq
     a.hg = hg;
     a.units = p.hkv / hg;
     a.tile_tokens = plan.tile_tokens;
+    a.run_cost = p.dtype == PGD_F32 ? 0 : kRunCostTiles;  // the float32 path's merge kernel: 0
     a.err = p.err;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     a.counters = reinterpret_cast<int*>(ws + wl.counters_off);

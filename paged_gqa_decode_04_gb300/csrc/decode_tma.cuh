@@ -254,24 +254,31 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
     return r;
 }
 
-// Two int8 codes (low byte -> low half) to two f16, exactly.  Each byte b,
-// with its sign bit flipped, is placed as the low byte under an 0x64 high
-// byte: the f16 with those bits is 1024 + (b + 128) (exponent 10, the byte as
-// the low mantissa bits), and subtracting 1152 leaves b.  Every value is an
-// integer below 2048, so each step is exact in f16.
-__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint16_t v) {
-    const uint32_t x = __byte_perm((uint32_t)v ^ 0x8080u, 0x64646464u, 0x5140);
-    const __half2 bias = __halves2half2(__ushort_as_half((unsigned short)0x6480),
-                                        __ushort_as_half((unsigned short)0x6480));
-    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&x), bias);
-    return *reinterpret_cast<const uint32_t*>(&r);
-}
-
-// Two 8-bit codes of the page type to two f16.
+// The low (bytes 0, 1) and high (bytes 2, 3) pair of a word of 8-bit codes
+// as f16x2.  e4m3: the exact values.  int8: the word must hold the codes with
+// their sign bits flipped (w ^ 0x80808080); each byte is then placed as the
+// low byte under an 0x64 high byte, and that f16 is 1024 + (code + 128) =
+// code + kI8Bias (exponent 10, the byte as the low mantissa bits), exact.  The
+// kernel takes the bias out of the sums it enters (see kI8Bias).
 template <bool INT8>
-__device__ __forceinline__ uint32_t widen_x2(uint16_t v) {
-    if constexpr (INT8) return i8x2_to_f16x2(v);
-    else return e4m3x2_to_f16x2(v);
+__device__ __forceinline__ uint32_t widen_lo(uint32_t w) {
+    if constexpr (INT8) return __byte_perm(w, 0x64646464u, 0x5140);
+    else return e4m3x2_to_f16x2((uint16_t)(w & 0xffffu));
+}
+template <bool INT8>
+__device__ __forceinline__ uint32_t widen_hi(uint32_t w) {
+    if constexpr (INT8) return __byte_perm(w, 0x64646464u, 0x5342);
+    else return e4m3x2_to_f16x2((uint16_t)(w >> 16));
+}
+// int8 pages: every widened code carries +1152.  In q . k that adds
+// 1152 * sum_d q[d] to every score of a query row (subtracted with the logit
+// multiplier); in P V it adds 1152 * sum_t P[t] to every output column of a
+// row (the f16 P values fed to the products are summed beside them and the
+// term subtracted at the piece's end).
+constexpr float kI8Bias = 1152.f;
+
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t w) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
 // Two bf16 (one 32-bit word) to two f16.
@@ -552,7 +559,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     constexpr int D = C::D;
     constexpr int T = C::T;
     extern __shared__ uint8_t dyn_smem[];
-    __shared__ int64_t scratch[C::THREADS];
+    __shared__ int64_t scratch[C::THREADS > 96 ? C::THREADS : 96];
     __shared__ SpanStart ss;
     __shared__ __align__(8) uint64_t full_bar[S];
     __shared__ __align__(8) uint64_t empty_bar[S];
@@ -593,7 +600,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     find_span_start(a.seq_lens, a.B, a.units, T, a.q_len, a.window, a.max_blocks, bs,
                     a.num_parts, a.auto_parts ? kMinTilesPerCta : 1, scratch, &ss,
-                    a.tile_base);  // ends with __syncthreads
+                    a.tile_base, a.run_cost);  // ends with __syncthreads
 
     // Sequences that own no tiles: length 0 gives zeros, an out-of-range length
     // gives NaN and latches PGD_ERR_SEQ_LEN.  CTA b % P writes sequence b.
@@ -605,14 +612,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out) + (int64_t)b * a.q_len * a.hq * D;
         for (int i = threadIdx.x; i < a.q_len * a.hq * D; i += blockDim.x) ob[i] = fill;
     }
-    if (ss.r0 >= ss.r1) return;
     const int64_t r0 = ss.r0, r1 = ss.r1;
-    const int n_tiles = (int)(r1 - r0);
+    const int W = ss.run_cost;
+    // real tiles of the span (virtual indices; a span may hold cost slots only)
+    const int n_tiles =
+        span_real_tiles(ss, a.seq_lens, a.B, a.units, T, a.q_len, a.window, a.max_blocks, bs, W);
+    if (n_tiles == 0) return;
 
     if (warp == C::NC) {
         // ============================================================ producer
         TileCursor cur = cursor_at(ss, a.seq_lens, a.units, T, a.q_len, a.window, a.max_blocks,
-                                   bs);
+                                   bs, W);
         const uint64_t policy = policy_evict_first();
         const uint32_t box_bytes = (uint32_t)(C::HH * R * 128);
         // Block-id window: lane l holds block_table[win_b][win_lb + l]; the next
@@ -629,7 +639,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         for (int it = 0; it < n_tiles; ++it) {
             const int s = it % S;
             const uint32_t ph = (uint32_t)(it / S) & 1u;
-            const int64_t x = r0 + it;
+            const int64_t x = cur.run_start + cur.i;  // virtual index of the tile
             if (cur.b != L_b) {
                 L = a.seq_lens[cur.b];
                 L_b = cur.b;
@@ -710,7 +720,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(fb);  // second arrival: the scales are in place
             }
-            cursor_next(cur, a.seq_lens, a.B, a.units, T, a.q_len, a.window, a.max_blocks, bs);
+            cursor_next(cur, a.seq_lens, a.B, a.units, T, a.q_len, a.window, a.max_blocks, bs,
+                        W);
         }
         // Do not leave while copies this CTA issued may still land.
         if (lane == 0) {
@@ -747,6 +758,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // logit multiplier (base-2 units; times the K scale of 8-bit pages) and the
     // V scale of 8-bit pages, set per piece
     float s_mul = a.scale_log2, v_mul = 1.f;
+    // int8 pages: the K bias term of each row's scores (1152 * sum_d q) and
+    // the running sums of the f16 P values (for the V bias term); 0 otherwise
+    float qc0 = 0.f, qc1 = 0.f, cp0 = 0.f, cp1 = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     bool seg_bad = false;
     uint32_t comb_phase = 0;
@@ -781,6 +795,24 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 qa[ks][2] = row0_ok ? bf16x2_to_f16x2(__ldg(q0 + c + 1)) : 0u;
                 qa[ks][3] = row1_ok ? bf16x2_to_f16x2(__ldg(q1 + c + 1)) : 0u;
             }
+            if constexpr (C::INT8) {
+                // the sum of this lane's f16 q values of each row, over the
+                // lanes of the row's quad: the whole row
+                float q0s = 0.f, q1s = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const float2 x0 = f16x2_to_float2(qa[ks][0]), x2 = f16x2_to_float2(qa[ks][2]);
+                    const float2 x1 = f16x2_to_float2(qa[ks][1]), x3 = f16x2_to_float2(qa[ks][3]);
+                    q0s += (x0.x + x0.y) + (x2.x + x2.y);
+                    q1s += (x1.x + x1.y) + (x3.x + x3.y);
+                }
+                q0s += __shfl_xor_sync(0xffffffffu, q0s, 1);
+                q0s += __shfl_xor_sync(0xffffffffu, q0s, 2);
+                q1s += __shfl_xor_sync(0xffffffffu, q1s, 1);
+                q1s += __shfl_xor_sync(0xffffffffu, q1s, 2);
+                qc0 = kI8Bias * q0s;
+                qc1 = kI8Bias * q1s;
+            }
             if constexpr (pbs) {  // scales per page, applied per n-tile
                 s_mul = a.scale_log2;
                 v_mul = 1.f;
@@ -803,7 +835,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     int pre_seq = -1, pre_kvh = -1;
     {
         const TileCursor c0 = cursor_at(ss, a.seq_lens, a.units, T, a.q_len, a.window,
-                                        a.max_blocks, bs);
+                                        a.max_blocks, bs, W);
         pre_seq = c0.b;
         pre_kvh = c0.unit * C::HG + hgi;
         load_q(pre_seq, pre_kvh);
@@ -842,6 +874,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
             m0 = m1 = -INFINITY;
             l0 = l1 = 0.f;
+            cp0 = cp1 = 0.f;
             seg_bad = false;
         }
         seg_bad |= (dsc.flags & kTileBad) != 0;
@@ -895,9 +928,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                     w[3]);
 #pragma unroll
                             for (int q = 0; q < 4; ++q) {
+                                if constexpr (C::INT8) w[q] ^= 0x80808080u;
                                 mma_f16(sc[jp + (q & 1)], qa[ks + (q >> 1)],
-                                        widen_x2<C::INT8>((uint16_t)(w[q] & 0xffffu)),
-                                        widen_x2<C::INT8>((uint16_t)(w[q] >> 16)));
+                                        widen_lo<C::INT8>(w[q]), widen_hi<C::INT8>(w[q]));
                             }
                         }
                     }
@@ -940,8 +973,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     for (int j = 0; j < C::CH / 8; ++j) {
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
-                            sc[j][e] *= smj[j];
-                            sc[j][2 + e] *= smj[j];
+                            if constexpr (C::INT8) {
+                                sc[j][e] = fmaf(sc[j][e], smj[j], -qc0 * smj[j]);
+                                sc[j][2 + e] = fmaf(sc[j][2 + e], smj[j], -qc1 * smj[j]);
+                            } else {
+                                sc[j][e] *= smj[j];
+                                sc[j][2 + e] *= smj[j];
+                            }
                             mx0 = fmaxf(mx0, sc[j][e]);
                             mx1 = fmaxf(mx1, sc[j][2 + e]);
                         }
@@ -954,8 +992,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             const int tok = c0 + j * 8 + tig * 2 + e;
                             const bool v0 = tok < hi0 && tok >= lo0;
                             const bool v1 = tok < hi1 && tok >= lo1;
-                            sc[j][e] = v0 ? sc[j][e] * smj[j] : -INFINITY;
-                            sc[j][2 + e] = v1 ? sc[j][2 + e] * smj[j] : -INFINITY;
+                            sc[j][e] = v0 ? fmaf(sc[j][e], smj[j], -qc0 * smj[j]) : -INFINITY;
+                            sc[j][2 + e] = v1 ? fmaf(sc[j][2 + e], smj[j], -qc1 * smj[j])
+                                              : -INFINITY;
                             mx0 = fmaxf(mx0, sc[j][e]);
                             mx1 = fmaxf(mx1, sc[j][2 + e]);
                         }
@@ -992,6 +1031,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
                 l0 = l0 * alpha0 + ps0;
                 if (C::ROWS16) l1 = l1 * alpha1 + ps1;
+                if constexpr (C::INT8) {
+                    cp0 *= alpha0;
+                    if (C::ROWS16) cp1 *= alpha1;
+                }
                 if (__any_sync(0xffffffffu, alpha0 != 1.f || alpha1 != 1.f)) {
 #pragma unroll
                     for (int n = 0; n < D / 8; ++n) {
@@ -1028,6 +1071,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             pa[2] = pack_f16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
                             pa[3] = pack_f16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
                         }
+                        if constexpr (C::INT8) {  // the f16 P values the products take
+                            const float2 a0 = f16x2_to_float2(pa[0]), a2 = f16x2_to_float2(pa[2]);
+                            cp0 += (a0.x + a0.y) + (a2.x + a2.y);
+                            if (C::ROWS16) {
+                                const float2 a1 = f16x2_to_float2(pa[1]);
+                                const float2 a3 = f16x2_to_float2(pa[3]);
+                                cp1 += (a1.x + a1.y) + (a3.x + a3.y);
+                            }
+                        }
                         const int tok = c0 + kk * 16 + (lm_mi & 1) * 8 + lm_i;
 #pragma unroll
                         for (int c2 = 0; c2 < D / 32; ++c2) {
@@ -1036,14 +1088,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             ldsm_x4_t(v_u + row_off(tok, 0) + ((vc ^ lm_i) << 4), r[0], r[1], r[2],
                                       r[3]);
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) r[q] = __byte_perm(r[q], 0u, 0x3120);
+                            for (int q = 0; q < 4; ++q) {
+                                r[q] = __byte_perm(r[q], 0u, 0x3120);
+                                if constexpr (C::INT8) r[q] ^= 0x80808080u;
+                            }
 #pragma unroll
                             for (int h = 0; h < 2; ++h) {  // chunk 2 c2 + h: r[2h] tokens 0-7, r[2h+1] 8-15
                                 const int n = 4 * c2 + 2 * h;
-                                mma_f16(o[n], pa, widen_x2<C::INT8>((uint16_t)(r[2 * h] & 0xffffu)),
-                                        widen_x2<C::INT8>((uint16_t)(r[2 * h + 1] & 0xffffu)));
-                                mma_f16(o[n + 1], pa, widen_x2<C::INT8>((uint16_t)(r[2 * h] >> 16)),
-                                        widen_x2<C::INT8>((uint16_t)(r[2 * h + 1] >> 16)));
+                                mma_f16(o[n], pa, widen_lo<C::INT8>(r[2 * h]),
+                                        widen_lo<C::INT8>(r[2 * h + 1]));
+                                mma_f16(o[n + 1], pa, widen_hi<C::INT8>(r[2 * h]),
+                                        widen_hi<C::INT8>(r[2 * h + 1]));
                             }
                         }
                         continue;
@@ -1075,6 +1130,22 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (!(dsc.flags & kSegEnd)) continue;
 
         // ================================================ end of a piece: combine
+        if constexpr (C::INT8) {
+            // every output column of a row got 1152 * (the row's f16 P sum)
+            float ct0 = cp0 + __shfl_xor_sync(0xffffffffu, cp0, 1);
+            ct0 += __shfl_xor_sync(0xffffffffu, ct0, 2);
+            float ct1 = cp1 + __shfl_xor_sync(0xffffffffu, cp1, 1);
+            ct1 += __shfl_xor_sync(0xffffffffu, ct1, 2);
+            ct0 *= kI8Bias;
+            ct1 *= kI8Bias;
+#pragma unroll
+            for (int n = 0; n < D / 8; ++n) {
+                o[n][0] -= ct0;
+                o[n][1] -= ct0;
+                o[n][2] -= ct1;
+                o[n][3] -= ct1;
+            }
+        }
         float lt0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
         lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
         float lt1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);

@@ -11,7 +11,20 @@
 // Hkv / HG units.
 // CTA c of P takes the span [floor(c N / P), floor((c+1) N / P)) of the N
 // tiles, so every CTA gets the same amount of KV bytes (to one tile) whatever
-// the length mix.  A (b, u) run that lies inside one span is finished by that
+// the length mix.
+//
+// Run cost.  Starting a run inside a span costs that CTA time the tiles do
+// not show (its query rows, the piece's epilogue, the arrival and usually the
+// merge that follows): with run_cost = W > 0 each run is preceded by W
+// virtual tiles that hold no work, and the spans are cut over this virtual
+// sequence, so a span holding a run start gets W fewer real tiles.  A tile is
+// then named by its virtual index:
+//
+//     vbase(b) = sum over b' < b of units * (n_b' + W)   (0 for n_b' = 0)
+//     tile i of run (b, u) = vbase(b) + u * (n_b + W) + W + i
+//
+// and everything below (spans, piece owners, segment flags) works on virtual
+// indices; W = 0 gives the plain tile sequence.  A (b, u) run that lies inside one span is finished by that
 // CTA; a run cut by span boundaries leaves one partial result per piece, in
 // slot 0 of a CTA (the piece that starts the CTA's span) or slot 1 (the piece
 // that ends it), and a log-sum-exp merge combines them (inside the TMA kernel,
@@ -62,35 +75,71 @@ __device__ __forceinline__ void latch_error(int* err, int code) {
     atomicCAS(err, 0, code);
 }
 
+// Virtual tiles of a sequence with n tiles per unit (see "Run cost" above).
+__device__ __forceinline__ int64_t virtual_tiles(int n, int units, int run_cost) {
+    return n > 0 ? (int64_t)units * (n + run_cost) : 0;
+}
+
 // Start of this CTA's span, found with a block-wide scan over the sequences.
 struct SpanStart {
-    int64_t n_total;   // N
+    int64_t n_total;   // N: virtual tiles of the call (the real ones when run_cost = 0)
     int64_t parts;     // spans in use (<= gridDim.x)
-    int64_t r0, r1;    // this CTA's span
+    int64_t r0, r1;    // this CTA's span (virtual indices)
     int b;             // sequence holding r0 (valid when r0 < r1)
-    int64_t b_base;    // tile_base[b]
+    int64_t b_base;    // vbase(b): virtual index of the sequence's first slot
+    int run_cost;      // W in use (0 when the call has few tiles per span)
 };
+
+// A call charges run starts only when it has at least this many real tiles
+// per span in use.
+constexpr int kRunCostMinTiles = 8;
 
 // Every thread of the block must call this; blockDim.x is a multiple of 32 and
 // at most 1024.  `scratch` is >= 64 int64 of shared memory, `out` a shared
 // SpanStart.  With min_tiles > 1 the spans in use are min(parts,
 // ceil(N / min_tiles)) (at least 1) and CTAs beyond them get an empty span;
-// with min_tiles == 1 all `parts` spans are used.  CTA 0 also writes
-// tile_base[0..B] to global memory for the merge kernel.
+// with min_tiles == 1 all `parts` spans are used (N counts real tiles there).
+// The run cost asked for is used only when the call has at least
+// kRunCostMinTiles real tiles per span in use (out->run_cost says which).
+// CTA 0 also writes vbase[0..B] to global memory for the merge kernel.
+// `scratch` holds >= 96 int64.
 __device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int B, int units,
                                        int T, int q_len, int window, int max_blocks,
                                        int block_size, int64_t parts, int min_tiles,
                                        int64_t* scratch, SpanStart* out,
-                                       int64_t* __restrict__ tile_base_out) {
+                                       int64_t* __restrict__ tile_base_out, int run_cost = 0) {
     const int nt = blockDim.x;  // a multiple of 32
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
     const int per = (B + nt - 1) / nt;
     const int b_lo = min(B, tid * per);
     const int b_hi = min(B, b_lo + per);
+    // real tiles of the call: per-thread sums, then warp sums added up by
+    // every warp (each sees the same total)
+    int64_t local_real = 0;
+    for (int b = b_lo; b < b_hi; ++b)
+        local_real += (int64_t)units * tiles_of(seq_lens[b], max_blocks, block_size, T, q_len,
+                                                window);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        local_real += __shfl_xor_sync(0xffffffffu, local_real, off);
+    if (lane == 0) scratch[64 + warp] = local_real;
+    __syncthreads();
+    int64_t real = 0;
+    for (int w = 0; w < nwarps; ++w) real += scratch[64 + w];
+    // spans in use, and the run cost: only where spans hold many tiles (with a
+    // few tiles per span, cost slots would leave spans with none)
+    int64_t p = parts;
+    if (min_tiles > 1) {  // fewer spans only when asked for
+        p = (real + min_tiles - 1) / min_tiles;
+        p = p < parts ? p : parts;
+        p = p > 0 ? p : 1;
+    }
+    if (real < kRunCostMinTiles * p) run_cost = 0;
     int64_t local = 0;
     for (int b = b_lo; b < b_hi; ++b)
-        local += (int64_t)units * tiles_of(seq_lens[b], max_blocks, block_size, T, q_len, window);
+        local += virtual_tiles(tiles_of(seq_lens[b], max_blocks, block_size, T, q_len, window),
+                               units, run_cost);
     // block-wide exclusive scan of the per-thread sums: warp shuffles, then the
     // warp totals scanned by warp 0 (scratch[32 + w] = inclusive prefix of warps)
     int64_t incl = local;
@@ -110,14 +159,9 @@ __device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int
         }
         if (lane < nwarps) scratch[32 + lane] = w;
         if (lane == nwarps - 1) {
-            const int64_t run = w;  // N
-            int64_t p = parts;
-            if (min_tiles > 1) {  // fewer spans only when asked for
-                p = (run + min_tiles - 1) / min_tiles;
-                p = p < parts ? p : parts;
-                p = p > 0 ? p : 1;
-            }
+            const int64_t run = w;  // N (virtual)
             out->n_total = run;
+            out->run_cost = run_cost;
             out->parts = p;
             out->r0 = blockIdx.x < p ? span_begin(blockIdx.x, run, p) : run;
             out->r1 = blockIdx.x < p ? span_begin(blockIdx.x + 1, run, p) : run;
@@ -129,8 +173,8 @@ __device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int
     const int64_t r0 = out->r0;
     int64_t run = (warp ? scratch[32 + warp - 1] : 0) + incl - local;  // exclusive prefix
     for (int b = b_lo; b < b_hi; ++b) {
-        int64_t n =
-            (int64_t)units * tiles_of(seq_lens[b], max_blocks, block_size, T, q_len, window);
+        const int64_t n = virtual_tiles(
+            tiles_of(seq_lens[b], max_blocks, block_size, T, q_len, window), units, run_cost);
         if (blockIdx.x == 0) tile_base_out[b] = run;
         if (r0 >= run && r0 < run + n) {
             out->b = b;
@@ -147,37 +191,46 @@ __device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int
 struct TileCursor {
     int b, unit, i, n_b;     // current position: tile i of n_b of (b, unit)
     int first;               // first tile of sequence b (windowed calls skip the start)
-    int64_t run_start;       // flat index of tile 0 of (b, unit)
+    int64_t run_start;       // virtual index of tile 0 of (b, unit); tile i is run_start + i
 };
 
-// Cursor at flat tile x, which sequence b (first tile b_base) holds.
+// Cursor at the first real tile at or after virtual index x, which sequence b
+// (first slot b_base) holds; when x falls among a run's cost slots that is
+// the run's tile 0.
 __device__ inline TileCursor cursor_at_tile(int64_t x, int b, int64_t b_base,
                                             const int32_t* seq_lens, int T, int q_len,
-                                            int window, int max_blocks, int block_size) {
+                                            int window, int max_blocks, int block_size,
+                                            int run_cost = 0) {
     TileCursor c;
     c.b = b;
     const int L = seq_lens[b];
     c.n_b = tiles_of(L, max_blocks, block_size, T, q_len, window);
     c.first = first_tile_of(L, T, q_len, window);
-    int64_t off = x - b_base;
-    c.unit = (int)(off / c.n_b);
-    c.i = (int)(off % c.n_b);
-    c.run_start = b_base + (int64_t)c.unit * c.n_b;
+    const int64_t per_run = (int64_t)c.n_b + run_cost;
+    const int64_t off = x - b_base;
+    c.unit = (int)(off / per_run);
+    const int i = (int)(off % per_run) - run_cost;
+    c.i = i > 0 ? i : 0;
+    c.run_start = b_base + (int64_t)c.unit * per_run + run_cost;
     return c;
 }
 
 __device__ inline TileCursor cursor_at(const SpanStart& s, const int32_t* seq_lens, int units,
                                        int T, int q_len, int window, int max_blocks,
-                                       int block_size) {
+                                       int block_size, int run_cost = 0) {
     (void)units;
     return cursor_at_tile(s.r0, s.b, s.b_base, seq_lens, T, q_len, window, max_blocks,
-                          block_size);
+                          block_size, run_cost);
 }
 
+// Next real tile: the next one of the run, else tile 0 of the next run (the
+// next unit, or the first unit of the next sequence with tiles), which
+// starts run_cost virtual slots after this run's end.
 __device__ inline void cursor_next(TileCursor& c, const int32_t* seq_lens, int B, int units,
-                                   int T, int q_len, int window, int max_blocks, int block_size) {
+                                   int T, int q_len, int window, int max_blocks, int block_size,
+                                   int run_cost = 0) {
     if (++c.i < c.n_b) return;
-    c.run_start += c.n_b;
+    c.run_start += c.n_b + run_cost;
     c.i = 0;
     if (++c.unit < units) return;
     c.unit = 0;
@@ -188,6 +241,27 @@ __device__ inline void cursor_next(TileCursor& c, const int32_t* seq_lens, int B
     }
     c.n_b = nb;
     if (c.b < B) c.first = first_tile_of(seq_lens[c.b], T, q_len, window);
+}
+
+// Real tiles in the span [s.r0, s.r1) (0 for an empty span, or one that
+// holds only cost slots).
+__device__ inline int span_real_tiles(const SpanStart& s, const int32_t* seq_lens, int B,
+                                      int units, int T, int q_len, int window, int max_blocks,
+                                      int block_size, int run_cost) {
+    if (s.r0 >= s.r1 || s.b < 0) return 0;
+    TileCursor c = cursor_at(s, seq_lens, units, T, q_len, window, max_blocks, block_size,
+                             run_cost);
+    int64_t n = 0;
+    while (c.b < B) {
+        const int64_t x = c.run_start + c.i;
+        if (x >= s.r1) break;
+        const int64_t e = c.run_start + c.n_b < s.r1 ? c.run_start + c.n_b : s.r1;
+        n += e - x;
+        if (e >= s.r1) break;
+        c.i = c.n_b - 1;  // to the next run
+        cursor_next(c, seq_lens, B, units, T, q_len, window, max_blocks, block_size, run_cost);
+    }
+    return (int)n;
 }
 
 // Segment flags for the piece of (b, unit) a CTA holds.

@@ -13,6 +13,13 @@ namespace pgd {
 // arrays of this size; pools on a device ordinal at or above it are refused).
 constexpr int kMaxDevices = 64;
 
+// Time a CTA spends on a run start that its tiles do not show (the piece's
+// query rows, epilogue, arrival and, usually, a merge), in tiles of the TMA
+// kernel (64 KB of K/V each): the work partition charges it to each run so
+// that spans holding run starts get fewer tiles.  Measured by CTA timelines:
+// a CTA with one more run start ended about three tiles later.
+constexpr int kRunCostTiles = 3;
+
 // Tokens per tile of the CUDA-core kernel (the TMA kernel uses 128 / HG).
 constexpr int kSimpleTileTokens = 64;
 
@@ -76,6 +83,7 @@ struct DecodeArgs {
     int hg;                // KV heads per unit of work
     int units;             // units per sequence, Hkv / hg
     int tile_tokens;       // tokens per tile
+    int run_cost;          // virtual tiles charged to each run start by the partition
     int* err;
     // workspace carve-up
     int* counters;         // [B][Hkv][m-tiles] per split run: pieces finished (zero between
