@@ -559,7 +559,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     constexpr int D = C::D;
     constexpr int T = C::T;
     extern __shared__ uint8_t dyn_smem[];
-    __shared__ int64_t scratch[C::THREADS > 96 ? C::THREADS : 96];
+    __shared__ int64_t scratch[C::THREADS > 98 ? C::THREADS : 98];
     __shared__ SpanStart ss;
     __shared__ __align__(8) uint64_t full_bar[S];
     __shared__ __align__(8) uint64_t empty_bar[S];
@@ -614,9 +614,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     const int64_t r0 = ss.r0, r1 = ss.r1;
     const int W = ss.run_cost;
-    // real tiles of the span (virtual indices; a span may hold cost slots only)
-    const int n_tiles =
-        span_real_tiles(ss, a.seq_lens, a.B, a.units, T, a.q_len, a.window, a.max_blocks, bs, W);
+    const int n_tiles = ss.n_tiles;  // real tiles (a span may hold cost slots only)
     if (n_tiles == 0) return;
 
     if (warp == C::NC) {

@@ -87,6 +87,8 @@ struct SpanStart {
     int64_t r0, r1;    // this CTA's span (virtual indices)
     int b;             // sequence holding r0 (valid when r0 < r1)
     int64_t b_base;    // vbase(b): virtual index of the sequence's first slot
+    int unit, i;       // run (b, unit) and its tile i: the first real tile at or after r0
+    int n_tiles;       // real tiles of the span
     int run_cost;      // W in use (0 when the call has few tiles per span)
 };
 
@@ -94,15 +96,24 @@ struct SpanStart {
 // per span in use.
 constexpr int kRunCostMinTiles = 8;
 
+// Real tiles before virtual slot x + 1 counted from the start of sequence b
+// (its runs are units of n tiles, each after W cost slots): tiles of the
+// whole runs before x's run, plus those of x's run up to and including x.
+__device__ __forceinline__ int real_upto(int64_t x, int64_t vbase, int n, int W) {
+    const int off = (int)(x - vbase);
+    const int per_run = n + W;
+    const int i = off % per_run - W;  // tile of x in its run; < 0: a cost slot
+    return (off / per_run) * n + (i < 0 ? 0 : i + 1);
+}
+
 // Every thread of the block must call this; blockDim.x is a multiple of 32 and
-// at most 1024.  `scratch` is >= 64 int64 of shared memory, `out` a shared
+// at most 1024.  `scratch` is >= 96 int64 of shared memory, `out` a shared
 // SpanStart.  With min_tiles > 1 the spans in use are min(parts,
 // ceil(N / min_tiles)) (at least 1) and CTAs beyond them get an empty span;
 // with min_tiles == 1 all `parts` spans are used (N counts real tiles there).
 // The run cost asked for is used only when the call has at least
 // kRunCostMinTiles real tiles per span in use (out->run_cost says which).
 // CTA 0 also writes vbase[0..B] to global memory for the merge kernel.
-// `scratch` holds >= 96 int64.
 __device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int B, int units,
                                        int T, int q_len, int window, int max_blocks,
                                        int block_size, int64_t parts, int min_tiles,
@@ -114,75 +125,109 @@ __device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int
     const int per = (B + nt - 1) / nt;
     const int b_lo = min(B, tid * per);
     const int b_hi = min(B, b_lo + per);
-    // real tiles of the call: per-thread sums, then warp sums added up by
-    // every warp (each sees the same total)
-    int64_t local_real = 0;
-    for (int b = b_lo; b < b_hi; ++b)
-        local_real += (int64_t)units * tiles_of(seq_lens[b], max_blocks, block_size, T, q_len,
-                                                window);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        local_real += __shfl_xor_sync(0xffffffffu, local_real, off);
-    if (lane == 0) scratch[64 + warp] = local_real;
-    __syncthreads();
-    int64_t real = 0;
-    for (int w = 0; w < nwarps; ++w) real += scratch[64 + w];
-    // spans in use, and the run cost: only where spans hold many tiles (with a
-    // few tiles per span, cost slots would leave spans with none)
-    int64_t p = parts;
-    if (min_tiles > 1) {  // fewer spans only when asked for
-        p = (real + min_tiles - 1) / min_tiles;
-        p = p < parts ? p : parts;
-        p = p > 0 ? p : 1;
+    // tiles per unit of this thread's sequences (the first one kept: one
+    // sequence per thread whenever B <= blockDim.x)
+    const int n_first =
+        b_lo < b_hi ? tiles_of(seq_lens[b_lo], max_blocks, block_size, T, q_len, window) : 0;
+    auto tiles_at = [&](int b) {
+        return b == b_lo ? n_first
+                         : tiles_of(seq_lens[b], max_blocks, block_size, T, q_len, window);
+    };
+    // both prefixes in one scan: real tiles, and virtual tiles with the cost
+    int64_t real_loc = 0, virt_loc = 0;
+    for (int b = b_lo; b < b_hi; ++b) {
+        const int n = tiles_at(b);
+        real_loc += (int64_t)units * n;
+        virt_loc += virtual_tiles(n, units, run_cost);
     }
-    if (real < kRunCostMinTiles * p) run_cost = 0;
-    int64_t local = 0;
-    for (int b = b_lo; b < b_hi; ++b)
-        local += virtual_tiles(tiles_of(seq_lens[b], max_blocks, block_size, T, q_len, window),
-                               units, run_cost);
-    // block-wide exclusive scan of the per-thread sums: warp shuffles, then the
-    // warp totals scanned by warp 0 (scratch[32 + w] = inclusive prefix of warps)
-    int64_t incl = local;
+    int64_t real_inc = real_loc, virt_inc = virt_loc;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-        const int64_t v = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += v;
+        const int64_t r = __shfl_up_sync(0xffffffffu, real_inc, off);
+        const int64_t v = __shfl_up_sync(0xffffffffu, virt_inc, off);
+        if (lane >= off) {
+            real_inc += r;
+            virt_inc += v;
+        }
     }
-    if (lane == 31) scratch[warp] = incl;
+    if (lane == 31) {
+        scratch[warp] = virt_inc;
+        scratch[64 + warp] = real_inc;
+    }
     __syncthreads();
     if (warp == 0) {
-        int64_t w = lane < nwarps ? scratch[lane] : 0;
+        int64_t v = lane < nwarps ? scratch[lane] : 0;
+        int64_t r = lane < nwarps ? scratch[64 + lane] : 0;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int64_t v = __shfl_up_sync(0xffffffffu, w, off);
-            if (lane >= off) w += v;
+            const int64_t v2 = __shfl_up_sync(0xffffffffu, v, off);
+            const int64_t r2 = __shfl_up_sync(0xffffffffu, r, off);
+            if (lane >= off) {
+                v += v2;
+                r += r2;
+            }
         }
-        if (lane < nwarps) scratch[32 + lane] = w;
+        if (lane < nwarps) {
+            scratch[32 + lane] = v;   // inclusive prefixes of the warps
+            scratch[64 + lane] = r;
+        }
         if (lane == nwarps - 1) {
-            const int64_t run = w;  // N (virtual)
-            out->n_total = run;
-            out->run_cost = run_cost;
+            const int64_t real = r;
+            // spans in use, and the run cost: only where spans hold many tiles
+            // (with a few tiles per span, cost slots would leave spans with none)
+            int64_t p = parts;
+            if (min_tiles > 1) {  // fewer spans only when asked for
+                p = (real + min_tiles - 1) / min_tiles;
+                p = p < parts ? p : parts;
+                p = p > 0 ? p : 1;
+            }
+            const int W = real >= (int64_t)kRunCostMinTiles * p ? run_cost : 0;
+            const int64_t n = W ? v : real;  // N
+            out->n_total = n;
+            out->run_cost = W;
             out->parts = p;
-            out->r0 = blockIdx.x < p ? span_begin(blockIdx.x, run, p) : run;
-            out->r1 = blockIdx.x < p ? span_begin(blockIdx.x + 1, run, p) : run;
+            out->r0 = blockIdx.x < p ? span_begin(blockIdx.x, n, p) : n;
+            out->r1 = blockIdx.x < p ? span_begin(blockIdx.x + 1, n, p) : n;
             out->b = -1;
             out->b_base = 0;
+            out->unit = out->i = 0;
+            out->n_tiles = 0;
         }
     }
     __syncthreads();
-    const int64_t r0 = out->r0;
-    int64_t run = (warp ? scratch[32 + warp - 1] : 0) + incl - local;  // exclusive prefix
+    const int W = out->run_cost;
+    const int64_t r0 = out->r0, r1 = out->r1;
+    // this thread's exclusive prefixes, virtual (or real, without the cost)
+    int64_t vrun = (warp ? (W ? scratch[32 + warp - 1] : scratch[64 + warp - 1]) : 0) +
+                   (W ? virt_inc - virt_loc : real_inc - real_loc);
+    int64_t rrun = (warp ? scratch[64 + warp - 1] : 0) + real_inc - real_loc;
+    // real tiles before r0 and before r1, found by the threads whose
+    // sequences hold those slots; their difference is the span's count
     for (int b = b_lo; b < b_hi; ++b) {
-        const int64_t n = virtual_tiles(
-            tiles_of(seq_lens[b], max_blocks, block_size, T, q_len, window), units, run_cost);
-        if (blockIdx.x == 0) tile_base_out[b] = run;
-        if (r0 >= run && r0 < run + n) {
+        const int nb = tiles_at(b);
+        const int64_t n = virtual_tiles(nb, units, W);
+        if (blockIdx.x == 0) tile_base_out[b] = vrun;
+        if (r0 >= vrun && r0 < vrun + n) {
+            const int off = (int)(r0 - vrun), per_run = nb + W;
+            const int i = off % per_run - W;
             out->b = b;
-            out->b_base = run;
+            out->b_base = vrun;
+            out->unit = off / per_run;
+            out->i = i > 0 ? i : 0;
+            scratch[96] = rrun + (off / per_run) * (int64_t)nb + (i > 0 ? i : 0);
         }
-        run += n;
+        if (r1 - 1 >= vrun && r1 - 1 < vrun + n && r0 < r1)
+            scratch[97] = rrun + real_upto(r1 - 1, vrun, nb, W);
+        vrun += n;
+        rrun += (int64_t)units * nb;
     }
     if (blockIdx.x == 0 && tid == nt - 1) tile_base_out[B] = out->n_total;
+    __syncthreads();
+    // (an empty span, r0 == r1, may still find a sequence holding r0: no count)
+    if (tid == 0 && out->b >= 0 && r0 < r1) {
+        const int64_t cnt = scratch[97] - scratch[96];
+        out->n_tiles = cnt > 0 ? (int)cnt : 0;
+    }
     __syncthreads();
 }
 
@@ -206,21 +251,29 @@ __device__ inline TileCursor cursor_at_tile(int64_t x, int b, int64_t b_base,
     const int L = seq_lens[b];
     c.n_b = tiles_of(L, max_blocks, block_size, T, q_len, window);
     c.first = first_tile_of(L, T, q_len, window);
-    const int64_t per_run = (int64_t)c.n_b + run_cost;
-    const int64_t off = x - b_base;
-    c.unit = (int)(off / per_run);
-    const int i = (int)(off % per_run) - run_cost;
+    const int per_run = c.n_b + run_cost;
+    const int off = (int)(x - b_base);  // within one sequence: fits 32 bits
+    c.unit = off / per_run;
+    const int i = off % per_run - run_cost;
     c.i = i > 0 ? i : 0;
     c.run_start = b_base + (int64_t)c.unit * per_run + run_cost;
     return c;
 }
 
+// Cursor at the span's first real tile (the position find_span_start found).
 __device__ inline TileCursor cursor_at(const SpanStart& s, const int32_t* seq_lens, int units,
                                        int T, int q_len, int window, int max_blocks,
                                        int block_size, int run_cost = 0) {
     (void)units;
-    return cursor_at_tile(s.r0, s.b, s.b_base, seq_lens, T, q_len, window, max_blocks,
-                          block_size, run_cost);
+    TileCursor c;
+    c.b = s.b;
+    const int L = seq_lens[s.b];
+    c.n_b = tiles_of(L, max_blocks, block_size, T, q_len, window);
+    c.first = first_tile_of(L, T, q_len, window);
+    c.unit = s.unit;
+    c.i = s.i;
+    c.run_start = s.b_base + (int64_t)s.unit * (c.n_b + run_cost) + run_cost;
+    return c;
 }
 
 // Next real tile: the next one of the run, else tile 0 of the next run (the
@@ -241,27 +294,6 @@ __device__ inline void cursor_next(TileCursor& c, const int32_t* seq_lens, int B
     }
     c.n_b = nb;
     if (c.b < B) c.first = first_tile_of(seq_lens[c.b], T, q_len, window);
-}
-
-// Real tiles in the span [s.r0, s.r1) (0 for an empty span, or one that
-// holds only cost slots).
-__device__ inline int span_real_tiles(const SpanStart& s, const int32_t* seq_lens, int B,
-                                      int units, int T, int q_len, int window, int max_blocks,
-                                      int block_size, int run_cost) {
-    if (s.r0 >= s.r1 || s.b < 0) return 0;
-    TileCursor c = cursor_at(s, seq_lens, units, T, q_len, window, max_blocks, block_size,
-                             run_cost);
-    int64_t n = 0;
-    while (c.b < B) {
-        const int64_t x = c.run_start + c.i;
-        if (x >= s.r1) break;
-        const int64_t e = c.run_start + c.n_b < s.r1 ? c.run_start + c.n_b : s.r1;
-        n += e - x;
-        if (e >= s.r1) break;
-        c.i = c.n_b - 1;  // to the next run
-        cursor_next(c, seq_lens, B, units, T, q_len, window, max_blocks, block_size, run_cost);
-    }
-    return (int)n;
 }
 
 // Segment flags for the piece of (b, unit) a CTA holds.
