@@ -329,16 +329,19 @@ struct Cfg {
     static constexpr int STATIC_RESERVE = 4096;  // static smem + alignment slack
     static constexpr int STAGES_FIT = (kSmemBudget - STATIC_RESERVE - COMB_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-    // dynamic smem: [1024 align slack][stages][comb]
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + COMB_BYTES;
+    // dynamic smem: [1024 align slack][stages][comb], and for STAGE the rest of
+    // the budget after them (a staging round then holds a warp's 16 rows of
+    // three pieces: one round instead of two at 4 query tokens)
+    static constexpr int SMEM_BYTES = STAGE ? ((kSmemBudget - STATIC_RESERVE) & ~1023)
+                                            : 1024 + STAGES * STAGE_BYTES + COMB_BYTES;
     // STAGE: after the tile loop the merging warps (token group 0 of each head
-    // and m-tile) each own a slice of the ring and the combine buffer
-    static constexpr uint32_t MERGE_SLICE =
-        (uint32_t)((STAGES * STAGE_BYTES + COMB_BYTES) / (HG * MT)) & ~15u;
+    // and m-tile) each own a slice of that region
+    static constexpr uint32_t MERGE_SLICE = (uint32_t)((SMEM_BYTES - 1024) / (HG * MT)) & ~15u;
     static_assert(!FP8 || D == 128, "8-bit pages: head_dim 128");
     static_assert(!INT8 || FP8, "int8 codes are 8-bit pages");
     static_assert(!PB || FP8, "per-block scales are for 8-bit pages");
     static_assert(STAGES >= 2, "pipeline needs at least two stages");
+    static_assert(SMEM_BYTES >= 1024 + STAGES * STAGE_BYTES + COMB_BYTES, "stages fit");
     static_assert(TW % 16 == 0, "a warp's token slice must be whole k16 steps");
     static_assert(TW % CH == 0 && CH % 16 == 0, "chunks must split the slice in k16 steps");
     static_assert(NC <= 8, "at most 8 consumer warps");
