@@ -416,6 +416,17 @@ def run_ours(args, world, rank, local):
 
         op_note = "append: one new token per sequence (read + write of K and V rows)"
 
+    # kernels one step launches: the decode, plus the run merge when the plan
+    # merges split runs in a second kernel (or the float32 path's merge kernel)
+    merge = "fused"
+    kernels_per_step = 1
+    if args.op != "append":
+        plan = pgd.paged_gqa_plan(w.k_pool.dtype, w.Hkv, w.D, w.B, w.Hq,
+                                  q_len=args.q_len if args.op == "decode_ex" else 1,
+                                  window=args.window if args.op == "decode_ex" else 0)
+        merge = plan["merge"]
+        kernels_per_step = 2 if merge in ("separate", "merge kernel") else 1
+
     step()
     status = pgd.paged_gqa_get_error(pool, stream)
     if status != 0:
@@ -493,7 +504,9 @@ def run_ours(args, world, rank, local):
                 "ms_per_step": round(t_ms, 5), "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
                 "config": {"workload": describe(w), "op": op_note,
-                           "launch": launch_note(args), "algorithmic_bytes_per_step": nbytes},
+                           "launch": launch_note(args), "algorithmic_bytes_per_step": nbytes,
+                           "merge": merge},
+                "gpu_launches": args.steps * kernels_per_step,
                 "pct_of_peak": round(100 * gbs / world / peak, 2),
                 "peak_source": "%s (%.0f GB/s)" % (peak_src, peak),
                 "per_rank_ms_per_step": [round(x, 5) for x in rank_ms],
@@ -571,25 +584,28 @@ def run_ours(args, world, rank, local):
                    "l2": "no flush: each step streams %.0f MB of K/V, above the 126 MB L2"
                          % (nbytes / 1e6),
                    "launch": launch_note(args),
-                   "algorithmic_bytes_per_step": nbytes},
+                   "algorithmic_bytes_per_step": nbytes, "merge": merge},
         "pct_of_peak": round(100 * per_gpu / peak, 2),
         "pct_of_nominal_8tbs": round(100 * per_gpu / NOMINAL_HBM_GBS, 2),
         "peak_source": "%s (%.0f GB/s)" % (peak_src, peak),
         "tokens_per_s_per_layer": round(world * w.B / (t_ms * 1e-3), 1),
         "roofline": {"bound": "hbm", "achieved": round(per_gpu, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(per_gpu / peak, 4), "traffic": ncu_traffic(args.config),
-                     "note": "bf16 and 8-bit steps are one kernel launch (split-KV merge "
-                             "fused), so achieved = algorithmic bytes / event-timed step"},
+                     "note": "achieved = algorithmic bytes / event-timed step: the decode "
+                             "kernel, plus the run-merge kernel when the plan merges split runs "
+                             "separately (config.merge = separate), so a lower bound on the "
+                             "decode kernel's own rate"},
         "per_rank_ms_per_step": [round(x, 5) for x in rank_ms],
         "e2e": {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "path": "paged_gqa_decode_host, page-locked host q / block table / lengths / "
-                        "out used in place by the kernel, one launch per step",
+                        "out used in place by the kernels, one decode launch per step (and the "
+                        "run merge when planned)",
                 "copy_path_ms_per_step": round(copy_ms, 5),
                 "copy_path": "cudaMemcpyAsync of the three inputs, paged_gqa_decode, "
                              "cudaMemcpyAsync of out"},
-        "gpu_launches": args.steps * (2 if w.dtype == "f32" else 1),
+        "gpu_launches": args.steps * kernels_per_step,
         "clocks": clk.summary(),
     }
     if cold_ms is not None:

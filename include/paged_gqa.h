@@ -300,9 +300,9 @@ int paged_gqa_decode_host(pgd_pool_t pool, const void *h_q, int B, int q_len, in
  *            among all the run's pieces under a cooperative launch (only
  *            when the grid, one CTA per SM, fits at once: plan[3] <= num_sms;
  *            should the device still refuse that launch, the library runs 0
- *            instead), 2 by
- *            the completing warp through bulk copies into shared memory, 3 a
- *            separate merge kernel (float32 pools)
+ *            instead), 2 none in the decode kernel: its pieces only write
+ *            partials and a second kernel merges every split run (runs over
+ *            2 to 5 spans), 3 the float32 path's merge kernel
  * Returns the status paged_gqa_decode_ex returns for these shapes before any
  * pointer is looked at (PGD_ERR_SHAPE, PGD_ERR_UNSUPPORTED, ...).  A
  * diagnostic of this library; the pages have no counterpart.

@@ -302,7 +302,7 @@ def paged_gqa_decode_host(pool, q, block_table, seq_lens, scale, window=0, out=N
     return out
 
 
-PLAN_MERGE = {0: "last arriver", 1: "shared (cooperative)", 2: "staged", 3: "merge kernel"}
+PLAN_MERGE = {0: "last arriver", 1: "shared (cooperative)", 2: "separate", 3: "merge kernel"}
 
 
 def paged_gqa_plan(dtype, num_kv_heads, head_dim, B, Hq, q_len=1, num_splits=0, window=0,

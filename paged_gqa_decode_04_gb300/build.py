@@ -18,11 +18,11 @@ LIB = os.path.join(HERE, "libpaged_gqa.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["api.cpp", "block_manager.cpp", "decode_simple.cu", "decode_tma_d64.cu",
-           "decode_tma_d128.cu", "decode_tma_d128_share.cu", "decode_tma_d128_stage.cu",
-           "decode_tma_fp8.cu", "decode_tma_fp8_share.cu", "decode_tma_fp8_stage.cu",
-           "decode_tma_i8.cu", "decode_tma_i8_share.cu", "decode_tma_i8_stage.cu",
-           "decode_tma_fp8pb.cu", "decode_tma_fp8pb_share.cu", "decode_tma_fp8pb_stage.cu",
-           "decode_tma_i8pb.cu", "decode_tma_i8pb_share.cu", "decode_tma_i8pb_stage.cu",
+           "decode_tma_d128.cu", "decode_tma_d128_share.cu", "decode_tma_d128_sep.cu",
+           "decode_tma_fp8.cu", "decode_tma_fp8_share.cu", "decode_tma_fp8_sep.cu",
+           "decode_tma_i8.cu", "decode_tma_i8_share.cu", "decode_tma_i8_sep.cu",
+           "decode_tma_fp8pb.cu", "decode_tma_fp8pb_share.cu", "decode_tma_fp8pb_sep.cu",
+           "decode_tma_i8pb.cu", "decode_tma_i8pb_share.cu", "decode_tma_i8pb_sep.cu",
            "kv_write.cu", "merge.cu", "noalloc.cu", "selftest.cu"]
 
 

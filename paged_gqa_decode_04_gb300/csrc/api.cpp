@@ -134,7 +134,9 @@ static int make_plan(int dtype, int hkv, int d, int num_sms, int B, int q_len, i
         const int passes = (nr * d + 127) / 128;       // 128 / D rows per merge pass
         const int64_t loads = (int64_t)passes * (pl.parts / runs + 1);
         if (nr >= 2 && loads > kShareMinLoads) pl.merge_variant = 1;
-        else if (nr >= 8 && loads > kStageMinLoads) pl.merge_variant = 2;
+        else if (nr >= kSepMinRows && 2 * runs <= pl.parts && pl.parts <= 5 * runs &&
+                 runs * pl.hg >= num_sms)
+            pl.merge_variant = 2;
         // the shared merge waits on other CTAs, so its grid must be resident
         // at once; the TMA kernel's shared memory (over half an SM's) allows
         // one CTA per SM, so a grid above the SM count takes the last arriver
@@ -150,7 +152,7 @@ WorkspaceLayout workspace_layout(int B, int hkv, int rows_per_head, int hg, int 
     const size_t rows = (size_t)hg * rows_per_head;  // rows of one partial result
     w.counters_off = 0;
     w.tile_base_off = round_up((size_t)B * hkv * mtiles * sizeof(int), 256);
-    w.part_lse_off = w.tile_base_off + round_up((size_t)(B + 1) * sizeof(int64_t), 256);
+    w.part_lse_off = w.tile_base_off + round_up((size_t)(B + 3) * sizeof(int64_t), 256);
     w.part_o_off = w.part_lse_off + round_up((size_t)parts * 2 * rows * sizeof(float), 256);
     w.total = w.part_o_off + round_up((size_t)parts * 2 * rows * d * sizeof(float), 256);
     return w;
@@ -383,8 +385,10 @@ int paged_gqa_decode_ex(pgd_pool_t pool, const void* q, int B, int q_len, int Hq
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p.dtype != PGD_F32) {
-        // one launch: the TMA kernel merges split runs itself
+        // the TMA kernel merges split runs itself, except in the separate-merge
+        // variant, whose partials a second kernel merges over all SMs
         if (launch_decode_tma(a, p, s) != cudaSuccess) return PGD_ERR_CUDA;
+        if (a.merge_variant == 2 && launch_merge_runs(a, s) != cudaSuccess) return PGD_ERR_CUDA;
     } else {
         if (launch_decode_simple(a, p.dtype, s) != cudaSuccess) return PGD_ERR_CUDA;
         if (launch_merge(a, p.dtype, s) != cudaSuccess) return PGD_ERR_CUDA;

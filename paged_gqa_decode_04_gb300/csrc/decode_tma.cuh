@@ -39,10 +39,10 @@
 //     then write the output rows (whole run) or a normalised partial and its
 //     log2-sum-exp (split run).  After the tile loop a split run is merged by
 //     the warp whose arrival completed it, with register loads of the pieces
-//     (merge variant 0) or, for many query rows and few pieces, through bulk
-//     copies of the pieces into its slice of the then idle stage ring
-//     (variant 2); in the shared-merge variant (1: cooperative launch, long
-//     runs) all its pieces' warps merge it, each taking a share of the rows.
+//     (merge variant 0); in the shared-merge variant (1: cooperative launch,
+//     long runs) all its pieces' warps merge it, each taking a share of the
+//     rows; in variant 2 (runs over 2 to 5 spans) pieces only write their
+//     partials and a second kernel merges every split run over all SMs.
 //   * 8-bit pages: K and V fragments come straight from the stage by
 //     ldmatrix and are widened to f16 in registers (cvt.rn.f16x2.e4m3x2);
 //     both products run on f16 mma.sync, the per-head scales fold into the
@@ -182,22 +182,6 @@ __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Orders this thread's generic global accesses with its async-proxy ones (the
-// split partials are stored by plain stores and read back by bulk copies).
-__device__ __forceinline__ void fence_proxy_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-// Untiled bulk copy global -> shared, completing on an mbarrier's transaction
-// count.  Both addresses 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -302,11 +286,11 @@ struct Cfg {
     static constexpr bool PB = PB_;           // 8-bit pages with a scale per block and KV head
     // merge variant of split runs: 0 the last arriver merges with register
     // loads; 1 (SHARE, cooperative launch) all pieces' warps merge a share of
-    // the rows; 2 (STAGE) the last arriver stages the pieces through the idle
-    // ring with bulk copies, a group of rows per round
+    // the rows; 2 (SEP) no merge here: pieces write partials, and a second
+    // kernel (merge_runs_kernel) merges them
     static constexpr int MV = MV_;
     static constexpr bool SHARE = MV_ == 1;
-    static constexpr bool STAGE = MV_ == 2;
+    static constexpr bool SEP = MV_ == 2;
     // 128-byte rows of a head in a page box: D/64 for bf16, 1 for 8-bit D = 128
     static constexpr int HALVES = FP8 ? D / 128 : D / 64;
     static constexpr int HH = HG * HALVES;    // 128-byte head rows per token in a tile
@@ -329,19 +313,12 @@ struct Cfg {
     static constexpr int STATIC_RESERVE = 4096;  // static smem + alignment slack
     static constexpr int STAGES_FIT = (kSmemBudget - STATIC_RESERVE - COMB_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-    // dynamic smem: [1024 align slack][stages][comb], and for STAGE the rest of
-    // the budget after them (a staging round then holds a warp's 16 rows of
-    // three pieces: one round instead of two at 4 query tokens)
-    static constexpr int SMEM_BYTES = STAGE ? ((kSmemBudget - STATIC_RESERVE) & ~1023)
-                                            : 1024 + STAGES * STAGE_BYTES + COMB_BYTES;
-    // STAGE: after the tile loop the merging warps (token group 0 of each head
-    // and m-tile) each own a slice of that region
-    static constexpr uint32_t MERGE_SLICE = (uint32_t)((SMEM_BYTES - 1024) / (HG * MT)) & ~15u;
+    // dynamic smem: [1024 align slack][stages][comb]
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + COMB_BYTES;
     static_assert(!FP8 || D == 128, "8-bit pages: head_dim 128");
     static_assert(!INT8 || FP8, "int8 codes are 8-bit pages");
     static_assert(!PB || FP8, "per-block scales are for 8-bit pages");
     static_assert(STAGES >= 2, "pipeline needs at least two stages");
-    static_assert(SMEM_BYTES >= 1024 + STAGES * STAGE_BYTES + COMB_BYTES, "stages fit");
     static_assert(TW % 16 == 0, "a warp's token slice must be whole k16 steps");
     static_assert(TW % CH == 0 && CH % 16 == 0, "chunks must split the slice in k16 steps");
     static_assert(NC <= 8, "at most 8 consumer warps");
@@ -394,8 +371,8 @@ __device__ __forceinline__ void lse_fold(float& M, float& W, float4& acc, float 
     // (M, W, acc) holds acc = sum_k 2^(lse_k - M) o_k and W = sum_k 2^(lse_k - M);
     // add a term that is (e, w, v) in the same form: a piece is (lse, 1, o),
     // another slot is (M', W', acc')
-    // explicit roundings: every merge (after the loop, inside it, staged)
-    // rounds the same way, whatever the compiler would contract
+    // explicit roundings: every merge of this kernel rounds the same way,
+    // whatever the compiler would contract
     const float nm = fmaxf(M, e);
     const float base = nm == -INFINITY ? 0.f : nm;
     const float sa = fast_exp2(M - base), sb = fast_exp2(e - base);
@@ -482,77 +459,6 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int64_t t0, in
     }
 }
 
-// Staged merge (STAGE variant) of rows [r_lo, r_hi): rounds of `cnt` rows; in
-// each round every piece's rows [rb, rb + cnt) (contiguous in its partial) are
-// bulk-copied into the warp's slice on one mbarrier, the log2-sum-exp values
-// loaded beside them, and each row folded from shared memory.  Rows are
-// independent, so nothing carries over between rounds.  Returns 0 when done,
-// 1 when even one row of every piece does not fit the slice (the caller merges
-// with register loads instead), -1 when the staging wait gave up.
-template <class C>
-__device__ __forceinline__ int merge_staged(const DecodeArgs& a, int64_t t0, int64_t N, int64_t P,
-                                         int64_t c0, int npieces, bool first_is_tail, int hgi,
-                                         int r_lo, int r_hi, int b, int kvh, uint8_t* slice,
-                                         uint32_t bar, uint32_t& phase) {
-    constexpr int D = C::D;
-    constexpr int CPR = D / 4;                  // float4 chunks per row
-    constexpr int RPP = 32 / CPR;               // rows per pass
-    constexpr uint32_t ROW = D * 4;             // bytes of a partial row
-    const int lane = threadIdx.x % 32;
-    const int rows = a.q_len * a.group;         // query rows per KV head
-    const int piece_rows = C::HG * rows;
-    const int per_row = npieces * (ROW + 4);    // one row of every piece, and its lse
-    const int nrr = (int)(C::MERGE_SLICE / (uint32_t)per_row);
-    if (nrr < 1) return 1;
-    float* lse_base = nullptr;
-    const uint32_t slice_u = smem_u32(slice);
-    const int col = (lane % CPR) * 4;
-    const int rp = lane / CPR;
-    auto slot_of = [&](int k) -> int64_t {
-        const int64_t c = P > N ? span_owner(t0 + k, N, P) : c0 + k;
-        return c * 2 + ((first_is_tail && k == 0) ? 1 : 0);
-    };
-    fence_proxy_async_global();  // the partials were stored by generic stores
-    for (int rb = r_lo; rb < r_hi; rb += nrr) {
-        const int cnt = min(nrr, r_hi - rb);
-        const uint32_t bytes = (uint32_t)cnt * ROW;  // one piece's rows of this round
-        lse_base = reinterpret_cast<float*>(slice + (size_t)npieces * bytes);
-        if (lane == 0) {
-            mbar_arrive_expect_tx(bar, (uint32_t)npieces * bytes);
-            for (int k = 0; k < npieces; ++k)
-                bulk_load(slice_u + k * bytes,
-                          a.part_o + (slot_of(k) * piece_rows + hgi * rows + rb) * D, bytes, bar);
-        }
-        for (int i = lane; i < npieces * cnt; i += 32) {
-            const int k = i / cnt, r = i % cnt;
-            lse_base[i] = __ldcg(a.part_lse + slot_of(k) * piece_rows + hgi * rows + rb + r);
-        }
-        __syncwarp();
-        if (!mbar_wait_warp(bar, phase)) return -1;
-        phase ^= 1u;
-        for (int r = rp; r < cnt; r += RPP) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            float M = -INFINITY, W = 0.f;
-#pragma unroll 4
-            for (int k = 0; k < npieces; ++k) {
-                const float4 v = *reinterpret_cast<const float4*>(slice + k * bytes +
-                                                                  (r * D + col) * 4);
-                lse_fold(M, W, acc, lse_base[k * cnt + r], 1.f, v);
-            }
-            const float w = W > 0.f ? 1.f / W : 0.f;  // no token in any piece: zeros
-            uint2 pk;
-            pk.x = pack_bf16(acc.x * w, acc.y * w);
-            pk.y = pack_bf16(acc.z * w, acc.w * w);
-            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) +
-                                      qrow_offset(a, b, kvh, rb + r) + col) = pk;
-        }
-        // the next round's bulk copies overwrite what these reads saw
-        __syncwarp();
-        fence_proxy_async();
-    }
-    return 0;
-}
-
 // ----------------------------------------------------------------- the kernel
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
@@ -569,7 +475,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     __shared__ __align__(8) uint64_t comb_bar;
     __shared__ StageDesc desc[S];
     __shared__ MergeJob jobs[C::NC][2];  // per consumer warp and partial slot
-    __shared__ __align__(8) uint64_t merge_bar[C::STAGE ? C::NC : 1];  // STAGE: staging barriers
     // 8-bit pages with per-block scales: K (0) and V (1) scale of every head
     // of the unit for each page of the tile in a stage
     __shared__ float qsc[C::PB ? S : 1][2][C::HG][C::PB ? C::MAXP : 1];
@@ -595,8 +500,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_init(smem_u32(&empty_bar[s]), C::NC * 32);
         }
         mbar_init(smem_u32(&comb_bar), C::NC * 32);
-        if constexpr (C::STAGE)
-            for (int w = 0; w < C::NC; ++w) mbar_init(smem_u32(&merge_bar[w]), 1);
         for (int w = 0; w < C::NC; ++w) jobs[w][0].b = jobs[w][1].b = -1;
         aborted = 0;
         fence_barrier_init();
@@ -859,7 +762,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // (relaxed; the merge after the loop fences first), so that if every
         // other piece is in already it skips its fence and arrival
         int pre_cnt = 0;
-        if (!C::SHARE && it == n_tiles - 1 && tg == 0 && (dsc.flags & kSegEnd) &&
+        if (!C::SHARE && !C::SEP && it == n_tiles - 1 && tg == 0 && (dsc.flags & kSegEnd) &&
             (dsc.flags & kSegPartial))
             pre_cnt = ld_relaxed(a.counters +
                                  ((int64_t)dsc.b * a.hkv + dsc.unit * C::HG + hgi) * C::MT + mt);
@@ -1308,7 +1211,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     pl[prow1] = seg_bad ? 0.f : (lt1 > 0.f ? m1 + fast_log2(lt1) : -INFINITY);
             }
         }
-        if constexpr (C::STAGE) fence_proxy_async_global();  // read back by bulk copies
+        if constexpr (C::SEP) continue;  // merged by the run-merge kernel after this one
         // Publish the partial and count it; the warp that brings the count to
         // the number of pieces sets it back to zero and flips the run's flag
         // bit.  Shared merge (cooperative launch, a merge of more than six
@@ -1359,19 +1262,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
     }
     // ---- merge the split runs recorded above
+    if constexpr (C::SEP) return;  // (none: the run-merge kernel merges them)
     if (__any_sync(0xffffffffu, aborted)) return;
     const int r_mine = mt * 16, r_end = min(rows, r_mine + C::ROWS);
-    uint32_t mphase = 0;
-    if constexpr (C::STAGE) {
-        // every consumer warp past the ring (so every copy into it has landed
-        // and been read): from here each merging warp owns a slice of it
-        fence_proxy_async();
-        mbar_arrive(smem_u32(&comb_bar));
-        if (!mbar_wait_warp(smem_u32(&comb_bar), comb_phase)) {
-            if (lane == 0) latch_error(a.err, PGD_ERR_TIMEOUT);
-            return;
-        }
-    }
 #pragma unroll 1
     for (int j = 0; j < 2; ++j) {
         const MergeJob jb = jobs[warp][j];
@@ -1396,17 +1289,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
         }
         __threadfence();
-        if constexpr (C::STAGE) {
-            const int st = merge_staged<C>(a, jb.t0, ss.n_total, ss.parts, jb.c0, jb.npieces,
-                                           jb.first_is_tail != 0, hgi, m_lo, m_hi, jb.b, jb.kvh,
-                                           stage_base + (warp / C::TG) * C::MERGE_SLICE,
-                                           smem_u32(&merge_bar[warp]), mphase);
-            if (st < 0) {
-                if (lane == 0) latch_error(a.err, PGD_ERR_TIMEOUT);
-                return;
-            }
-            if (st == 0) continue;
-        }
         if (m_hi - m_lo <= RPP)
             merge_pieces<C, true>(a, jb.t0, ss.n_total, ss.parts, jb.c0, jb.npieces,
                                   jb.first_is_tail != 0, hgi, m_lo, m_hi, jb.b, jb.kvh);

@@ -1,4 +1,5 @@
-// The TMA decode kernel for head_dim 128 (bf16 pages), staged-merge variant.
+// The TMA decode kernel for head_dim 128 (bf16 pages), separate-merge variant
+// (pieces write partials; the run-merge kernel merges them).
 #include "decode_tma.cuh"
 
 namespace pgd {

@@ -1,5 +1,5 @@
-// The TMA decode kernel for 8-bit (e4m3) K/V pages, head_dim 128, staged-merge
-// variant.
+// The TMA decode kernel for 8-bit (e4m3) K/V pages, head_dim 128,
+// separate-merge variant (pieces write partials; the run-merge kernel merges them).
 #include "decode_tma.cuh"
 
 namespace pgd {

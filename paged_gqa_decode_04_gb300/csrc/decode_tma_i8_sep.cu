@@ -1,5 +1,5 @@
 // The TMA decode kernel for 8-bit K/V pages of int8 codes, head_dim 128,
-// staged-merge variant.
+// separate-merge variant (pieces write partials; the run-merge kernel merges them).
 #include "decode_tma.cuh"
 
 namespace pgd {

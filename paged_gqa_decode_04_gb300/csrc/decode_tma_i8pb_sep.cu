@@ -1,5 +1,6 @@
 // The TMA decode kernel for 8-bit K/V pages of int8 codes with a scale per
-// block and KV head, head_dim 128, staged-merge variant.
+// block and KV head, head_dim 128, separate-merge variant
+// (pieces write partials; the run-merge kernel merges them).
 #include "decode_tma.cuh"
 
 namespace pgd {

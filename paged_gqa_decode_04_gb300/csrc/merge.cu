@@ -12,8 +12,8 @@
 // "Modern LLM Inference ...", section 8.3); it keeps the softmax exact, as the
 // same notes say of FlashAttention's online softmax.
 //
-// One CTA per sequence; used after the CUDA-core kernel, whose units are single
-// KV heads (a run is one (sequence, KV head) pair).  Runs that were not split
+// merge_kernel: one CTA per sequence; used after the CUDA-core kernel, whose
+// units are single KV heads (a run is one (sequence, KV head) pair).  Runs that were not split
 // are left alone (the decode kernel wrote them), sequences of length 0 get
 // zeros, and sequences whose length is out of range get NaN and latch
 // PGD_ERR_SEQ_LEN.
@@ -89,7 +89,80 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeArgs a) {
     }
 }
 
+constexpr int kRunMergeThreads = 128;
+
+// (M, W, acc) holds acc = sum_k 2^(lse_k - M) o_k and W = sum_k 2^(lse_k - M);
+// add piece (e, v), keeping the larger exponent as the reference
+__device__ __forceinline__ void fold_piece(float& M, float& W, float4& acc, float e, float4 v) {
+    const float nm = fmaxf(M, e);
+    const float base = nm == -INFINITY ? 0.f : nm;
+    const float sa = fast_exp2(M - base), sb = fast_exp2(e - base);
+    M = nm;
+    W = W * sa + sb;
+    acc.x = acc.x * sa + v.x * sb;
+    acc.y = acc.y * sa + v.y * sb;
+    acc.z = acc.z * sa + v.z * sb;
+    acc.w = acc.w * sa + v.w * sb;
+}
+
+// Merge of the split runs the TMA decode kernel's separate-merge variant leaves (its
+// pieces only write partials: with many query rows per KV head, a merge fused
+// at the end of the step would pull every piece's rows through one SM while
+// the others still stream).  One CTA per (run, head of the unit): a thread
+// takes (row, 4 columns) items and folds the run's pieces in order.  The
+// pieces and their partial slots follow from the spans exactly as in the
+// decode kernel: with P <= N spans every span holds a tile, so the pieces are
+// CTAs c0 .. c1; with P > N each holds at most one, so piece k is the owner of
+// tile t0 + k.  Runs held whole by one span, and sequences without tiles, were
+// written by the decode kernel and are left alone.
+__global__ void __launch_bounds__(kRunMergeThreads) merge_runs_kernel(DecodeArgs a) {
+    constexpr int D = 128;
+    constexpr int CPR = D / 4;  // float4 items per row
+    const int b = blockIdx.x / a.units, u = blockIdx.x % a.units, hgi = blockIdx.y;
+    const int n_b =
+        tiles_of(a.seq_lens[b], a.max_blocks, a.block_size, a.tile_tokens, a.q_len, a.window);
+    if (n_b == 0) return;
+    const int64_t N = a.tile_base[a.B], P = a.tile_base[a.B + 1];
+    const int W = (int)a.tile_base[a.B + 2];
+    const int64_t t0 = a.tile_base[b] + (int64_t)u * (n_b + W) + W;  // run's first real tile
+    const int64_t c0 = span_owner(t0, N, P);
+    if (c0 == span_owner(t0 + n_b - 1, N, P)) return;
+    const int npieces = P > N ? n_b : (int)(span_owner(t0 + n_b - 1, N, P) - c0 + 1);
+    const bool first_is_tail = P <= N && span_begin(c0, N, P) < t0;
+    const int G = a.group, rows = a.q_len * G;
+    const int piece_rows = a.hg * rows;
+    const int kvh = u * a.hg + hgi;
+    for (int item = threadIdx.x; item < rows * CPR; item += blockDim.x) {
+        const int r = item / CPR, col = (item % CPR) * 4;
+        const int64_t pr = (int64_t)hgi * rows + r;
+        float M = -INFINITY, Wt = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int k = 0; k < npieces; ++k) {
+            const int64_t c = P > N ? span_owner(t0 + k, N, P) : c0 + k;
+            const int64_t sl = c * 2 + ((first_is_tail && k == 0) ? 1 : 0);
+            const float e = __ldg(a.part_lse + sl * piece_rows + pr);
+            const float4 v = __ldg(reinterpret_cast<const float4*>(a.part_o + (sl * piece_rows + pr) * D + col));
+            fold_piece(M, Wt, acc, e, v);
+        }
+        const float w = Wt > 0.f ? 1.f / Wt : 0.f;  // no token in any piece: zeros
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * w, acc.y * w);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * w, acc.w * w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<uint32_t*>(&hi);
+        const int64_t orow = ((int64_t)b * a.q_len + r / G) * a.hq + (int64_t)kvh * G + r % G;
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + orow * D + col) = pk;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_merge_runs(const DecodeArgs& a, cudaStream_t s) {
+    if (a.B == 0 || a.d != 128) return a.B == 0 ? cudaSuccess : cudaErrorInvalidValue;
+    merge_runs_kernel<<<dim3((unsigned)(a.B * a.units), (unsigned)a.hg), kRunMergeThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_merge(const DecodeArgs& a, int dtype, cudaStream_t s) {
     if (a.B == 0) return cudaSuccess;

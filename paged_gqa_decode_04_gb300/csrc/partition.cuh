@@ -221,7 +221,11 @@ __device__ inline void find_span_start(const int32_t* __restrict__ seq_lens, int
         vrun += n;
         rrun += (int64_t)units * nb;
     }
-    if (blockIdx.x == 0 && tid == nt - 1) tile_base_out[B] = out->n_total;
+    if (blockIdx.x == 0 && tid == nt - 1) {
+        tile_base_out[B] = out->n_total;    // then what a separate merge needs
+        tile_base_out[B + 1] = out->parts;  // spans in use
+        tile_base_out[B + 2] = out->run_cost;
+    }
     __syncthreads();
     // (an empty span, r0 == r1, may still find a sequence holding r0: no count)
     if (tid == 0 && out->b >= 0 && r0 < r1) {

@@ -30,9 +30,13 @@ constexpr int kMaxGroup = 64;
 // lane (six batches of 4 row passes x 4 pieces): below that, the waits and the
 // second merge per CTA cost more than they save (measured).
 constexpr int kShareMinLoads = 96;
-// Staged merge (many query rows per head, few pieces): when one warp would need
-// more than two batches of register loads.
-constexpr int kStageMinLoads = 32;
+// Separate merge (a second kernel after the decode) when each split run covers
+// 2 to 5 spans, the runs times the head group fill the SMs and a head has at
+// least this many query rows: then the merges fused at the end of the decode
+// wait on pieces that end together, while the second kernel spreads them over
+// every SM (measured; with longer runs the shared merge, with shorter ones or
+// single rows the last arriver does better).
+constexpr int kSepMinRows = 4;
 
 struct Pool {
     const void* k;
@@ -90,8 +94,9 @@ struct DecodeArgs {
                            // calls) and a flag bit flipped when the last piece arrives
     int merge_variant;     // host's choice of split-merge kernel variant: 0 last arriver,
                            // 1 shared (long runs; falls back to 0 when the grid cannot be
-                           // resident), 2 staged through shared memory (many rows)
-    int64_t* tile_base;    // [B + 1] first flat tile of each sequence
+                           // resident), 2 separate run-merge kernel after the decode (many rows)
+    int64_t* tile_base;    // [B + 3] first flat tile of each sequence, the total, the spans
+                           // in use and the run cost
     float* part_o;         // [num_parts][2][hg * group][d] normalised partial outputs
     float* part_lse;       // [num_parts][2][hg * group]    partial log2-sum-exp
 };
@@ -102,7 +107,8 @@ struct Plan {
     int m_tiles;        // m16 row tiles of one head's query rows
     int tile_tokens;    // tokens per tile
     int parts;          // CTAs of the grid (spans of the tile sequence)
-    int merge_variant;  // 0 last arriver, 1 shared (cooperative), 2 staged, 3 separate kernel
+    int merge_variant;  // 0 last arriver, 1 shared (cooperative), 2 separate run merge,
+                        // 3 float32 merge kernel
 };
 
 // Workspace layout for (B, G, D, parts); returns total bytes and fills offsets.
@@ -131,5 +137,6 @@ const Pool& pool_desc(pgd_pool_t h);
 cudaError_t launch_decode_simple(const DecodeArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_decode_tma(const DecodeArgs& a, const Pool& p, cudaStream_t s);
 cudaError_t launch_merge(const DecodeArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_merge_runs(const DecodeArgs& a, cudaStream_t s);
 
 }  // namespace pgd

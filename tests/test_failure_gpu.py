@@ -34,8 +34,9 @@ def test_wait_that_runs_out_reports_timeout_and_context_survives():
 
 
 # (recipe, overrides, q_len): one workload per split-merge variant the host
-# picks -- last arriver (4 rows, few pieces), shared under a cooperative launch
-# (40 rows of one KV head, long runs), staged (16 rows, few pieces)
+# picks -- last arriver (8 runs of 4 rows), shared under a cooperative launch
+# (40 rows of one KV head, long runs), separate run-merge kernel (40 runs of 16
+# rows, 2 to 5 spans a run: two kernels in the graph)
 GRAPH_CASES = [
     ("llama3_8b", dict(B=8, lens=("uniform", 1, 1500), max_len=1536), 1),
     ("mqa_13b_b1", dict(B=2, lens=[4096, 2500], max_len=4096), 1),

@@ -2,7 +2,8 @@
 
 The span scan every decode CTA runs (csrc/partition.cuh, find_span_start)
 leaves in the workspace the first slot of each sequence in the virtual tile
-sequence the spans cut, and the total (CTA 0 writes them).  This reads that
+sequence the spans cut, the total, and then the spans in use and the run cost
+(CTA 0 writes them; the run-merge kernel reads the last two).  This reads that
 table after real decodes and compares it with the rules written out here:
 
   * tiles per KV-head unit of a sequence: ceil(L / T) minus the whole tiles
@@ -17,7 +18,7 @@ table after real decodes and compares it with the rules written out here:
 So the CUDA scan itself is checked, not only a host restatement of it
 (tests/test_partition_model.py checks the properties of the cut on CPU).
 Workspace layout (the library's own, csrc/api.cpp): one counter word per
-(sequence, KV head, row tile), rounded up to 256 bytes, then the B + 1 int64
+(sequence, KV head, row tile), rounded up to 256 bytes, then the B + 3 int64
 entries of this table.
 """
 import numpy as np
@@ -52,7 +53,7 @@ def expected_table(lens, max_blocks, bs, T, q_len, window, units, parts, auto, r
         p = max(1, min(parts, -(-real // MIN_TILES_PER_CTA)))
     W = run_cost if real >= RUN_COST_MIN_TILES * p else 0
     v = [units * (x + W) if x > 0 else 0 for x in n]
-    return np.concatenate([[0], np.cumsum(v)]).astype(np.int64), W
+    return np.concatenate([[0], np.cumsum(v), [p, W]]).astype(np.int64), W
 
 
 # (recipe, overrides, q_len, window, num_splits)
@@ -98,7 +99,7 @@ def test_device_tile_table_matches_rules(recipe, over, q_len, window, num_splits
     rows = q_len * (w.Hq // w.Hkv)
     mtiles = -(-rows // 16)
     off = -(-(w.B * w.Hkv * mtiles * 4) // 256) * 256
-    got = ws[off:off + 8 * (w.B + 1)].cpu().view(torch.int64).numpy()
+    got = ws[off:off + 8 * (w.B + 3)].cpu().view(torch.int64).numpy()
     units = w.Hkv // plan["head_group"]
     want, W = expected_table(w.lens_np, w.max_blocks, w.block_size, plan["tile_tokens"],
                              1 if f32 else q_len, 0 if f32 else window, units, plan["grid"],

@@ -15,15 +15,26 @@ def plan(dtype, hkv, d, B, Hq, **kw):
     return pgd.paged_gqa_plan(dtype, hkv, d, B, Hq, num_sms=152, **kw)
 
 
-# (name, args, kwargs, expected (head_group, m_tiles, tile_tokens, grid, merge))
+# (name, args, kwargs, expected (head_group, m_tiles, tile_tokens, grid, merge)).
+# Merge: shared when a warp's merge would take many loads (long runs); separate
+# (a second kernel) when runs cover 2 to 5 spans, fill the SMs and have 4+ rows
+# per head; otherwise the last arriver.
 CASES = [
-    ("llama3_8b", (BF16, 8, 128, 64, 32), {}, (8, 1, 16, 152, "last arriver")),
+    ("llama3_8b", (BF16, 8, 128, 64, 32), {}, (8, 1, 16, 152, "separate")),
     ("long_70b", (BF16, 8, 128, 8, 64), {}, (8, 1, 16, 152, "shared (cooperative)")),
     ("mha_13b_b1", (BF16, 40, 128, 1, 40), {}, (8, 1, 16, 152, "last arriver")),
     ("mqa_13b_b1", (BF16, 1, 128, 1, 40), {}, (1, 3, 128, 152, "shared (cooperative)")),
     ("mqa_13b_b8", (BF16, 1, 128, 8, 40), {}, (1, 3, 128, 152, "shared (cooperative)")),
     ("sweep B 256", (BF16, 8, 128, 256, 32), {}, (8, 1, 16, 152, "last arriver")),
-    ("4 query tokens, B 64", (BF16, 8, 128, 64, 32), dict(q_len=4), (8, 1, 16, 152, "staged")),
+    # the separate merge's edges: 152 spans over 32 runs (4.75 a run) separate,
+    # over 96 runs (1.6) last arriver; 4 tokens at B 16 (9.5) shared; MHA B 8
+    # (one row per head) last arriver
+    ("B 32", (BF16, 8, 128, 32, 32), {}, (8, 1, 16, 152, "separate")),
+    ("B 96", (BF16, 8, 128, 96, 32), {}, (8, 1, 16, 152, "last arriver")),
+    ("4 query tokens, B 16", (BF16, 8, 128, 16, 32), dict(q_len=4),
+     (8, 1, 16, 152, "shared (cooperative)")),
+    ("mha_13b_b8", (BF16, 40, 128, 8, 40), {}, (8, 1, 16, 152, "last arriver")),
+    ("4 query tokens, B 64", (BF16, 8, 128, 64, 32), dict(q_len=4), (8, 1, 16, 152, "separate")),
     ("4 query tokens, B 24", (BF16, 8, 128, 24, 32), dict(q_len=4),
      (8, 1, 16, 152, "shared (cooperative)")),
     # 32 / 64 rows per head: 128 / 256 runs over 152 spans, so a run has at most
@@ -33,14 +44,15 @@ CASES = [
      (4, 2, 32, 152, "last arriver")),
     ("64 query rows", (BF16, 8, 128, 64, 128), dict(q_len=4), (2, 4, 64, 152, "last arriver")),
     ("32 rows, B 8", (BF16, 8, 128, 8, 64), dict(q_len=4), (4, 2, 32, 152, "shared (cooperative)")),
-    ("8-bit llama3", (FP8, 8, 128, 64, 32), {}, (8, 1, 32, 152, "last arriver")),
+    ("8-bit llama3", (FP8, 8, 128, 64, 32), {}, (8, 1, 32, 152, "separate")),
     ("8-bit long_70b", (FP8, 8, 128, 8, 64), {}, (8, 1, 32, 152, "shared (cooperative)")),
-    ("int8 llama3", (I8, 8, 128, 64, 32), {}, (8, 1, 32, 152, "last arriver")),
+    ("int8 llama3", (I8, 8, 128, 64, 32), {}, (8, 1, 32, 152, "separate")),
     ("int8 long_70b", (I8, 8, 128, 8, 64), {}, (8, 1, 32, 152, "shared (cooperative)")),
-    ("int8 4 query tokens", (I8, 8, 128, 64, 32), dict(q_len=4), (8, 1, 32, 152, "staged")),
+    ("int8 4 query tokens", (I8, 8, 128, 64, 32), dict(q_len=4), (8, 1, 32, 152, "separate")),
     ("head_dim 64", (BF16, 2, 64, 4, 8), {}, (2, 1, 64, 152, "last arriver")),
     ("Hkv 6", (BF16, 6, 128, 4, 24), {}, (2, 1, 64, 152, "last arriver")),
     ("float32 tiny", (F32, 2, 64, 4, 8), {}, (1, 1, 64, 152, "merge kernel")),
+    # 500 spans over 64 runs: about 8 spans a run, past the separate merge
     ("explicit splits", (BF16, 8, 128, 64, 32), dict(num_splits=500),
      (8, 1, 16, 500, "last arriver")),
     # the shared merge needs its grid resident at once (one CTA per SM): a

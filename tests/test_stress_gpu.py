@@ -15,11 +15,13 @@ import paged_gqa_decode_04_gb300 as pgd
 pytestmark = pytest.mark.gpu
 
 # (recipe, overrides, query tokens, window, steps).  The host's merge choice:
-# last arriver (Llama shape, 32 runs of 4 rows), shared under a cooperative
-# launch (70B-like: 2 long runs of 8 rows; 24 runs of 16 rows), staged
-# (40 runs of 16 rows, with and without a window)
+# separate run-merge kernel (Llama shape, 32 runs of 4 rows, about 5 spans a
+# run), last arriver (8 runs of 4 rows, about 19 pieces each), shared under a
+# cooperative launch (70B-like: 2 long runs of 8 rows; 24 runs of 16 rows),
+# separate (40 runs of 16 rows, with and without a window)
 CASES = [
     ("llama3_8b", dict(B=32, lens=("uniform", 128, 2048), max_len=2048), 1, 0, 600),
+    ("llama3_8b", dict(B=8, lens=("uniform", 128, 2048), max_len=2048), 1, 0, 600),
     ("long_70b", dict(B=2, lens=[40000, 25000], max_len=40960), 1, 0, 300),
     ("llama3_8b", dict(B=24, lens=("uniform", 64, 1500), max_len=1536), 4, 0, 400),
     ("llama3_8b", dict(B=40, lens=("uniform", 64, 1500), max_len=1536), 4, 0, 400),
