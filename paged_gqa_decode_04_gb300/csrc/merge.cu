@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeArgs a) {
     }
 }
 
-constexpr int kRunMergeThreads = 128;
+constexpr int kRunMergeMaxThreads = 512;
 
 // (M, W, acc) holds acc = sum_k 2^(lse_k - M) o_k and W = sum_k 2^(lse_k - M);
 // add piece (e, v), keeping the larger exponent as the reference
@@ -108,14 +108,15 @@ __device__ __forceinline__ void fold_piece(float& M, float& W, float4& acc, floa
 // Merge of the split runs the TMA decode kernel's separate-merge variant leaves (its
 // pieces only write partials: with many query rows per KV head, a merge fused
 // at the end of the step would pull every piece's rows through one SM while
-// the others still stream).  One CTA per (run, head of the unit): a thread
-// takes (row, 4 columns) items and folds the run's pieces in order.  The
+// the others still stream).  One CTA per (run, head of the unit), one thread
+// per (row, 4 columns) item up to 512 threads (so all of a run's loads are in
+// flight at once); a thread folds the run's pieces in order.  The
 // pieces and their partial slots follow from the spans exactly as in the
 // decode kernel: with P <= N spans every span holds a tile, so the pieces are
 // CTAs c0 .. c1; with P > N each holds at most one, so piece k is the owner of
 // tile t0 + k.  Runs held whole by one span, and sequences without tiles, were
 // written by the decode kernel and are left alone.
-__global__ void __launch_bounds__(kRunMergeThreads) merge_runs_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kRunMergeMaxThreads) merge_runs_kernel(DecodeArgs a) {
     constexpr int D = 128;
     constexpr int CPR = D / 4;  // float4 items per row
     const int b = blockIdx.x / a.units, u = blockIdx.x % a.units, hgi = blockIdx.y;
@@ -160,7 +161,9 @@ __global__ void __launch_bounds__(kRunMergeThreads) merge_runs_kernel(DecodeArgs
 
 cudaError_t launch_merge_runs(const DecodeArgs& a, cudaStream_t s) {
     if (a.B == 0 || a.d != 128) return a.B == 0 ? cudaSuccess : cudaErrorInvalidValue;
-    merge_runs_kernel<<<dim3((unsigned)(a.B * a.units), (unsigned)a.hg), kRunMergeThreads, 0, s>>>(a);
+    const int items = a.q_len * a.group * (128 / 4);  // (row, 4 columns) per head; a multiple of 32
+    const int threads = items < kRunMergeMaxThreads ? items : kRunMergeMaxThreads;
+    merge_runs_kernel<<<dim3((unsigned)(a.B * a.units), (unsigned)a.hg), threads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
