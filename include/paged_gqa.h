@@ -270,7 +270,9 @@ size_t paged_gqa_noalloc_scratch_bytes(void);
  * the workspace with cudaMemcpyAsync on `stream` (for pageable memory that
  * copy may block the calling thread).  Either way the call is ordered on
  * `stream`, and h_out holds the result once the stream has synchronised; the
- * inputs must stay unchanged until then.
+ * inputs must stay unchanged until then.  When h_out is written in place, the
+ * split runs are merged inside the decode kernel (plan merge 0 where
+ * paged_gqa_plan reports 2), so that only one kernel writes over the link.
  *   workspace    device buffer of at least paged_gqa_workspace_size_host
  *                bytes, 256-byte aligned; its first
  *                paged_gqa_workspace_size_ex bytes are the decode workspace

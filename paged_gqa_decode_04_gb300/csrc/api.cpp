@@ -325,10 +325,15 @@ int paged_gqa_workspace_size(pgd_pool_t pool, int B, int Hq, int num_splits, siz
     return paged_gqa_workspace_size_ex(pool, B, 1, Hq, num_splits, bytes);
 }
 
-int paged_gqa_decode_ex(pgd_pool_t pool, const void* q, int B, int q_len, int Hq,
-                        const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
-                        int window, float scale, void* out, void* workspace,
-                        size_t workspace_bytes, int num_splits, void* stream) {
+namespace {
+// The decode of paged_gqa_decode_ex; out_on_host: `out` is host memory written
+// through its mapped address (paged_gqa_decode_host), where the merge stays
+// fused in the decode kernel (a second kernel's writes would cross the host
+// link after the first one's: measured slower end to end).
+int decode_ex_impl(pgd_pool_t pool, const void* q, int B, int q_len, int Hq,
+                   const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
+                   int window, float scale, void* out, void* workspace, size_t workspace_bytes,
+                   int num_splits, void* stream, bool out_on_host) {
     if (!pool) return PGD_ERR_ARG;
     const Pool& p = pool->p;
     Plan plan;
@@ -340,6 +345,7 @@ int paged_gqa_decode_ex(pgd_pool_t pool, const void* q, int B, int q_len, int Hq
         if (rc != PGD_OK) return rc;
     }
     if (B == 0) return PGD_OK;
+    if (out_on_host && plan.merge_variant == 2) plan.merge_variant = 0;
     const int G = Hq / p.hkv;
     const int parts = plan.parts;
     const int hg = plan.hg;
@@ -394,6 +400,15 @@ int paged_gqa_decode_ex(pgd_pool_t pool, const void* q, int B, int q_len, int Hq
         if (launch_merge(a, p.dtype, s) != cudaSuccess) return PGD_ERR_CUDA;
     }
     return PGD_OK;
+}
+}  // namespace
+
+int paged_gqa_decode_ex(pgd_pool_t pool, const void* q, int B, int q_len, int Hq,
+                        const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
+                        int window, float scale, void* out, void* workspace,
+                        size_t workspace_bytes, int num_splits, void* stream) {
+    return decode_ex_impl(pool, q, B, q_len, Hq, block_table, max_blocks, seq_lens, window, scale,
+                          out, workspace, workspace_bytes, num_splits, stream, false);
 }
 
 int paged_gqa_decode(pgd_pool_t pool, const void* q, int B, int Hq, const int32_t* block_table,
@@ -485,9 +500,9 @@ int paged_gqa_decode_host(pgd_pool_t pool, const void* h_q, int B, int q_len, in
     void* out = const_cast<void*>(kernel_address(h_out, 16, p.device));
     const bool copy_out = out == nullptr;
     if (copy_out) out = ws + hl.out_off;
-    rc = paged_gqa_decode_ex(pool, q, B, q_len, Hq, static_cast<const int32_t*>(bt), max_blocks,
-                             static_cast<const int32_t*>(sl), window, scale, out, workspace, dec,
-                             num_splits, stream);
+    rc = decode_ex_impl(pool, q, B, q_len, Hq, static_cast<const int32_t*>(bt), max_blocks,
+                        static_cast<const int32_t*>(sl), window, scale, out, workspace, dec,
+                        num_splits, stream, !copy_out);
     if (rc != PGD_OK) return rc;
     if (copy_out && cudaMemcpyAsync(h_out, out, hl.io_bytes, cudaMemcpyDefault, s) != cudaSuccess)
         return PGD_ERR_CUDA;

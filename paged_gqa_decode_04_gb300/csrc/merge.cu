@@ -120,11 +120,13 @@ __global__ void __launch_bounds__(kRunMergeMaxThreads) merge_runs_kernel(DecodeA
     constexpr int D = 128;
     constexpr int CPR = D / 4;  // float4 items per row
     const int b = blockIdx.x / a.units, u = blockIdx.x % a.units, hgi = blockIdx.y;
-    const int n_b =
-        tiles_of(a.seq_lens[b], a.max_blocks, a.block_size, a.tile_tokens, a.q_len, a.window);
-    if (n_b == 0) return;
+    // all from the decode's tile table in device memory (the lengths may sit in
+    // host memory): a sequence spans units * (tiles + W) virtual slots, or none
     const int64_t N = a.tile_base[a.B], P = a.tile_base[a.B + 1];
     const int W = (int)a.tile_base[a.B + 2];
+    const int64_t slots = a.tile_base[b + 1] - a.tile_base[b];
+    if (slots == 0) return;
+    const int n_b = (int)(slots / a.units) - W;
     const int64_t t0 = a.tile_base[b] + (int64_t)u * (n_b + W) + W;  // run's first real tile
     const int64_t c0 = span_owner(t0, N, P);
     if (c0 == span_owner(t0 + n_b - 1, N, P)) return;
