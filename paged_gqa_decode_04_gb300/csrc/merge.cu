@@ -89,7 +89,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeArgs a) {
     }
 }
 
-constexpr int kRunMergeMaxThreads = 512;
+constexpr int kRunMergeMaxThreads = 256;
+constexpr int kRunMergeItems = 2;   // (row, 4 columns) items a thread takes at once
+constexpr int kRunMergePieces = 4;  // pieces whose loads are issued before any fold
 
 // (M, W, acc) holds acc = sum_k 2^(lse_k - M) o_k and W = sum_k 2^(lse_k - M);
 // add piece (e, v), keeping the larger exponent as the reference
@@ -105,20 +107,22 @@ __device__ __forceinline__ void fold_piece(float& M, float& W, float4& acc, floa
     acc.w = acc.w * sa + v.w * sb;
 }
 
-// Merge of the split runs the TMA decode kernel's separate-merge variant leaves (its
-// pieces only write partials: with many query rows per KV head, a merge fused
-// at the end of the step would pull every piece's rows through one SM while
-// the others still stream).  One CTA per (run, head of the unit), one thread
-// per (row, 4 columns) item up to 512 threads (so all of a run's loads are in
-// flight at once); a thread folds the run's pieces in order.  The
-// pieces and their partial slots follow from the spans exactly as in the
-// decode kernel: with P <= N spans every span holds a tile, so the pieces are
-// CTAs c0 .. c1; with P > N each holds at most one, so piece k is the owner of
-// tile t0 + k.  Runs held whole by one span, and sequences without tiles, were
-// written by the decode kernel and are left alone.
+// Merge of the split runs the TMA decode kernel's separate-merge variant leaves
+// (its pieces only write partials: when runs cover a few spans, the merges a
+// decode would fuse all wait at the end of the step for partials written just
+// before).  One CTA per (run, head of the unit); a thread takes two (row, 4
+// columns) items and, for four pieces at a time, first issues every load and
+// then folds the pieces in order, so one batch costs one round trip.  The
+// CTAs (at most 256 threads) fit the GPU in one wave at the shapes this merge
+// is planned for.  The pieces and their partial slots follow from the spans
+// exactly as in the decode kernel: with P <= N spans every span holds a tile,
+// so the pieces are CTAs c0 .. c1; with P > N each holds at most one, so piece
+// k is the owner of tile t0 + k.  Runs held whole by one span, and sequences
+// without tiles, were written by the decode kernel and are left alone.
 __global__ void __launch_bounds__(kRunMergeMaxThreads) merge_runs_kernel(DecodeArgs a) {
     constexpr int D = 128;
     constexpr int CPR = D / 4;  // float4 items per row
+    constexpr int I = kRunMergeItems, K = kRunMergePieces;
     const int b = blockIdx.x / a.units, u = blockIdx.x % a.units, hgi = blockIdx.y;
     // all from the decode's tile table in device memory (the lengths may sit in
     // host memory): a sequence spans units * (tiles + W) virtual slots, or none
@@ -130,32 +134,71 @@ __global__ void __launch_bounds__(kRunMergeMaxThreads) merge_runs_kernel(DecodeA
     const int64_t t0 = a.tile_base[b] + (int64_t)u * (n_b + W) + W;  // run's first real tile
     const int64_t c0 = span_owner(t0, N, P);
     if (c0 == span_owner(t0 + n_b - 1, N, P)) return;
-    const int npieces = P > N ? n_b : (int)(span_owner(t0 + n_b - 1, N, P) - c0 + 1);
-    const bool first_is_tail = P <= N && span_begin(c0, N, P) < t0;
+    const bool dense = P <= N;
+    const int npieces = dense ? (int)(span_owner(t0 + n_b - 1, N, P) - c0 + 1) : n_b;
+    const bool first_is_tail = dense && span_begin(c0, N, P) < t0;
     const int G = a.group, rows = a.q_len * G;
     const int piece_rows = a.hg * rows;
     const int kvh = u * a.hg + hgi;
-    for (int item = threadIdx.x; item < rows * CPR; item += blockDim.x) {
-        const int r = item / CPR, col = (item % CPR) * 4;
-        const int64_t pr = (int64_t)hgi * rows + r;
-        float M = -INFINITY, Wt = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int k = 0; k < npieces; ++k) {
-            const int64_t c = P > N ? span_owner(t0 + k, N, P) : c0 + k;
-            const int64_t sl = c * 2 + ((first_is_tail && k == 0) ? 1 : 0);
-            const float e = __ldg(a.part_lse + sl * piece_rows + pr);
-            const float4 v = __ldg(reinterpret_cast<const float4*>(a.part_o + (sl * piece_rows + pr) * D + col));
-            fold_piece(M, Wt, acc, e, v);
+    const int n_items = rows * CPR;
+    for (int base = threadIdx.x; base < n_items; base += blockDim.x * I) {
+        int64_t pr[I];
+        int col[I];
+        bool ok[I];
+        float M[I], Wt[I];
+        float4 acc[I];
+#pragma unroll
+        for (int i = 0; i < I; ++i) {
+            const int item = base + i * blockDim.x;
+            ok[i] = item < n_items;
+            const int r = ok[i] ? item / CPR : 0;
+            col[i] = ok[i] ? (item % CPR) * 4 : 0;
+            pr[i] = (int64_t)hgi * rows + r;
+            M[i] = -INFINITY;
+            Wt[i] = 0.f;
+            acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        const float w = Wt > 0.f ? 1.f / Wt : 0.f;  // no token in any piece: zeros
-        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * w, acc.y * w);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * w, acc.w * w);
-        uint2 pk;
-        pk.x = *reinterpret_cast<uint32_t*>(&lo);
-        pk.y = *reinterpret_cast<uint32_t*>(&hi);
-        const int64_t orow = ((int64_t)b * a.q_len + r / G) * a.hq + (int64_t)kvh * G + r % G;
-        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + orow * D + col) = pk;
+        for (int k0 = 0; k0 < npieces; k0 += K) {
+            int64_t sl[K];  // partial slots of this batch's pieces
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                const int k = k0 + j < npieces ? k0 + j : npieces - 1;
+                const int64_t c = dense ? c0 + k : span_owner(t0 + k, N, P);
+                sl[j] = c * 2 + ((first_is_tail && k == 0) ? 1 : 0);
+            }
+            float e[I][K];
+            float4 v[I][K];
+#pragma unroll
+            for (int i = 0; i < I; ++i) {
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    const bool ld = ok[i] && k0 + j < npieces;
+                    e[i][j] = ld ? __ldg(a.part_lse + sl[j] * piece_rows + pr[i]) : -INFINITY;
+                    v[i][j] = ld ? __ldg(reinterpret_cast<const float4*>(
+                                       a.part_o + (sl[j] * piece_rows + pr[i]) * D + col[i]))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < I; ++i) {
+#pragma unroll
+                for (int j = 0; j < K; ++j)
+                    if (k0 + j < npieces) fold_piece(M[i], Wt[i], acc[i], e[i][j], v[i][j]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < I; ++i) {
+            if (!ok[i]) continue;
+            const int r = (base + i * blockDim.x) / CPR;
+            const float w = Wt[i] > 0.f ? 1.f / Wt[i] : 0.f;  // no token in any piece: zeros
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc[i].x * w, acc[i].y * w);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc[i].z * w, acc[i].w * w);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t*>(&lo);
+            pk.y = *reinterpret_cast<uint32_t*>(&hi);
+            const int64_t orow = ((int64_t)b * a.q_len + r / G) * a.hq + (int64_t)kvh * G + r % G;
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + orow * D + col[i]) = pk;
+        }
     }
 }
 
@@ -163,8 +206,10 @@ __global__ void __launch_bounds__(kRunMergeMaxThreads) merge_runs_kernel(DecodeA
 
 cudaError_t launch_merge_runs(const DecodeArgs& a, cudaStream_t s) {
     if (a.B == 0 || a.d != 128) return a.B == 0 ? cudaSuccess : cudaErrorInvalidValue;
-    const int items = a.q_len * a.group * (128 / 4);  // (row, 4 columns) per head; a multiple of 32
-    const int threads = items < kRunMergeMaxThreads ? items : kRunMergeMaxThreads;
+    // threads for two items each, a multiple of 32 (items = rows * 32)
+    const int items = a.q_len * a.group * (128 / 4);
+    int threads = (items / kRunMergeItems + 31) / 32 * 32;
+    threads = threads < kRunMergeMaxThreads ? threads : kRunMergeMaxThreads;
     merge_runs_kernel<<<dim3((unsigned)(a.B * a.units), (unsigned)a.hg), threads, 0, s>>>(a);
     return cudaGetLastError();
 }
