@@ -91,20 +91,24 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeArgs a) {
 
 constexpr int kRunMergeMaxThreads = 256;
 constexpr int kRunMergeItems = 2;   // (row, 4 columns) items a thread takes at once
-constexpr int kRunMergePieces = 4;  // pieces whose loads are issued before any fold
+constexpr int kRunMergePieces = 4;  // pieces whose loads are issued before any fold (the
+                                    // decode kernel's merge batch, kPieceBatch)
 
 // (M, W, acc) holds acc = sum_k 2^(lse_k - M) o_k and W = sum_k 2^(lse_k - M);
-// add piece (e, v), keeping the larger exponent as the reference
+// add piece (e, v), keeping the larger exponent as the reference.  The same
+// explicit roundings as the decode kernel's own merge (a fused multiply-add of
+// the rescaled sum and the rounded product), so that a run merged here or
+// inside the decode kernel gives the same bits.
 __device__ __forceinline__ void fold_piece(float& M, float& W, float4& acc, float e, float4 v) {
     const float nm = fmaxf(M, e);
     const float base = nm == -INFINITY ? 0.f : nm;
     const float sa = fast_exp2(M - base), sb = fast_exp2(e - base);
     M = nm;
-    W = W * sa + sb;
-    acc.x = acc.x * sa + v.x * sb;
-    acc.y = acc.y * sa + v.y * sb;
-    acc.z = acc.z * sa + v.z * sb;
-    acc.w = acc.w * sa + v.w * sb;
+    W = __fmaf_rn(W, sa, __fmul_rn(1.f, sb));
+    acc.x = __fmaf_rn(acc.x, sa, __fmul_rn(v.x, sb));
+    acc.y = __fmaf_rn(acc.y, sa, __fmul_rn(v.y, sb));
+    acc.z = __fmaf_rn(acc.z, sa, __fmul_rn(v.z, sb));
+    acc.w = __fmaf_rn(acc.w, sa, __fmul_rn(v.w, sb));
 }
 
 // Merge of the split runs the TMA decode kernel's separate-merge variant leaves
@@ -179,11 +183,13 @@ __global__ void __launch_bounds__(kRunMergeMaxThreads) merge_runs_kernel(DecodeA
                                  : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
+            // every entry of the batch is folded, those past the last piece as
+            // (-inf, 0): the decode kernel's merge folds its batches of four the
+            // same way (kPieceBatch)
 #pragma unroll
             for (int i = 0; i < I; ++i) {
 #pragma unroll
-                for (int j = 0; j < K; ++j)
-                    if (k0 + j < npieces) fold_piece(M[i], Wt[i], acc[i], e[i][j], v[i][j]);
+                for (int j = 0; j < K; ++j) fold_piece(M[i], Wt[i], acc[i], e[i][j], v[i][j]);
             }
         }
 #pragma unroll

@@ -2,7 +2,9 @@
 memory.  Page-locked buffers are used in place by the kernel; pageable or
 misaligned ones are staged through the workspace.  Either way the result is
 the device-memory call's, bit for bit, and within tolerance of the oracle
-(GPU only)."""
+(GPU only).  Where the device-memory call merges split runs in a second kernel
+(runs over 2 to 5 spans), the host entry writing out in place merges them
+inside the decode kernel; the two merges fold alike, so the bits still agree."""
 import pytest
 import torch
 
@@ -31,6 +33,9 @@ CASES = [
     ("llama3_8b", dict(B=3, lens=[90, 300, 17], max_len=320), 3, 64),
     ("llama3_8b_fp8", dict(B=3, lens=[90, 300, 17], max_len=320), 1, 0),
     ("tiny", dict(), 1, 0),
+    # separate merge on the device-memory call, fused when out is used in place
+    ("llama3_8b", dict(B=32, lens=("uniform", 128, 2048), max_len=2048), 1, 0),
+    ("llama3_8b_i8", dict(B=32, lens=("uniform", 128, 2048), max_len=2048), 4, 0),
 ]
 
 # how each of (q, block_table, seq_lens, out) is held on the host
