@@ -111,6 +111,22 @@ __device__ __forceinline__ void fold_piece(float& M, float& W, float4& acc, floa
     acc.w = __fmaf_rn(acc.w, sa, __fmul_rn(v.w, sb));
 }
 
+// Span arithmetic of partition.cuh with a 32-bit unsigned division whenever
+// the numerator and divisor fit (every shape this merge is planned for): the
+// 64-bit division routine is most of the time between the tile table's
+// arrival and the partial loads.
+__device__ __forceinline__ int64_t floor_div(int64_t num, int64_t den) {
+    if (num >= 0 && num <= 0x7fffffff && den <= 0x7fffffff)
+        return (int64_t)((uint32_t)num / (uint32_t)den);
+    return num / den;
+}
+__device__ __forceinline__ int64_t owner_of(int64_t x, int64_t N, int64_t P) {
+    return floor_div((x + 1) * P - 1, N);  // span_owner
+}
+__device__ __forceinline__ int64_t begin_of(int64_t c, int64_t N, int64_t P) {
+    return floor_div(c * N, P);  // span_begin
+}
+
 // Merge of the split runs the TMA decode kernel's separate-merge variant leaves
 // (its pieces only write partials: when runs cover a few spans, the merges a
 // decode would fuse all wait at the end of the step for partials written just
@@ -136,11 +152,12 @@ __global__ void __launch_bounds__(kRunMergeMaxThreads) merge_runs_kernel(DecodeA
     if (slots == 0) return;
     const int n_b = (int)(slots / a.units) - W;
     const int64_t t0 = a.tile_base[b] + (int64_t)u * (n_b + W) + W;  // run's first real tile
-    const int64_t c0 = span_owner(t0, N, P);
-    if (c0 == span_owner(t0 + n_b - 1, N, P)) return;
+    const int64_t c0 = owner_of(t0, N, P);
+    const int64_t c1 = owner_of(t0 + n_b - 1, N, P);
+    if (c0 == c1) return;
     const bool dense = P <= N;
-    const int npieces = dense ? (int)(span_owner(t0 + n_b - 1, N, P) - c0 + 1) : n_b;
-    const bool first_is_tail = dense && span_begin(c0, N, P) < t0;
+    const int npieces = dense ? (int)(c1 - c0 + 1) : n_b;
+    const bool first_is_tail = dense && begin_of(c0, N, P) < t0;
     const int G = a.group, rows = a.q_len * G;
     const int piece_rows = a.hg * rows;
     const int kvh = u * a.hg + hgi;
@@ -167,7 +184,7 @@ __global__ void __launch_bounds__(kRunMergeMaxThreads) merge_runs_kernel(DecodeA
 #pragma unroll
             for (int j = 0; j < K; ++j) {
                 const int k = k0 + j < npieces ? k0 + j : npieces - 1;
-                const int64_t c = dense ? c0 + k : span_owner(t0 + k, N, P);
+                const int64_t c = dense ? c0 + k : owner_of(t0 + k, N, P);
                 sl[j] = c * 2 + ((first_is_tail && k == 0) ? 1 : 0);
             }
             float e[I][K];
