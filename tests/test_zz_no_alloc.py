@@ -2,7 +2,8 @@
 device memory (a plugin inside a runtime that owns all device memory, or a
 path that must not let cudaMalloc / cudaFree synchronise the device).
 
-For each page type (bfloat16, 8-bit e4m3, float32) it is called through the C
+For each page type (bfloat16, 8-bit e4m3, float32, and bfloat16 with the
+separate run merge) it is called through the C
 ABI twice in a row -- the second call reuses the static scratch array the
 first one left behind -- and each result is checked against the float64
 oracle at the parity tolerances and against paged_gqa_decode (the entry point
@@ -34,6 +35,9 @@ CASES = {
     "bf16": dict(name="llama3_8b", B=8, lens=("uniform", 1, 2000), max_len=2048),
     "fp8": dict(name="llama3_8b_fp8", B=8, lens=("uniform", 1, 2000), max_len=2048),
     "f32": dict(name="tiny", B=6, lens=("uniform", 1, 700), max_len=704, num_blocks=None),
+    # runs over 2 to 5 spans: the separate run merge, a second kernel reading
+    # the same static scratch
+    "bf16_separate": dict(name="llama3_8b", B=32, lens=("uniform", 128, 2048), max_len=2048),
 }
 
 
