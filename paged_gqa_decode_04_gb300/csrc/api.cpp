@@ -137,6 +137,10 @@ static int make_plan(int dtype, int hkv, int d, int num_sms, int B, int q_len, i
         else if (nr >= kSepMinRows && 2 * runs <= pl.parts && pl.parts <= 5 * runs &&
                  runs * pl.hg >= num_sms)
             pl.merge_variant = 2;
+        // two or more row tiles per head: sharing each run's merge among its
+        // pieces' warps beats one warp per row tile merging them all (measured)
+        else if (pl.m_tiles >= 2)
+            pl.merge_variant = 1;
         // the shared merge waits on other CTAs, so its grid must be resident
         // at once; the TMA kernel's shared memory (over half an SM's) allows
         // one CTA per SM, so a grid above the SM count takes the last arriver

@@ -18,7 +18,8 @@ def plan(dtype, hkv, d, B, Hq, **kw):
 # (name, args, kwargs, expected (head_group, m_tiles, tile_tokens, grid, merge)).
 # Merge: shared when a warp's merge would take many loads (long runs); separate
 # (a second kernel) when runs cover 2 to 5 spans, fill the SMs and have 4+ rows
-# per head; otherwise the last arriver.
+# per head; else shared with two or more row tiles per head; otherwise the last
+# arriver.  Shared needs the grid resident at once (grid <= SMs).
 CASES = [
     ("llama3_8b", (BF16, 8, 128, 64, 32), {}, (8, 1, 16, 152, "separate")),
     ("long_70b", (BF16, 8, 128, 8, 64), {}, (8, 1, 16, 152, "shared (cooperative)")),
@@ -37,12 +38,12 @@ CASES = [
     ("4 query tokens, B 64", (BF16, 8, 128, 64, 32), dict(q_len=4), (8, 1, 16, 152, "separate")),
     ("4 query tokens, B 24", (BF16, 8, 128, 24, 32), dict(q_len=4),
      (8, 1, 16, 152, "shared (cooperative)")),
-    # 32 / 64 rows per head: 128 / 256 runs over 152 spans, so a run has at most
-    # 152 // runs + 1 = 2 / 1 pieces and a warp's 16 rows x 2 pieces stay within
-    # two batches of loads: the last arriver merges
+    # 32 / 64 rows per head (two / four row tiles): 128 / 256 runs over 152
+    # spans, too short for the separate merge; with several row tiles per head
+    # the shared merge beats the last arriver
     ("8 query rows x 4 tokens", (BF16, 8, 128, 64, 64), dict(q_len=4),
-     (4, 2, 32, 152, "last arriver")),
-    ("64 query rows", (BF16, 8, 128, 64, 128), dict(q_len=4), (2, 4, 64, 152, "last arriver")),
+     (4, 2, 32, 152, "shared (cooperative)")),
+    ("64 query rows", (BF16, 8, 128, 64, 128), dict(q_len=4), (2, 4, 64, 152, "shared (cooperative)")),
     ("32 rows, B 8", (BF16, 8, 128, 8, 64), dict(q_len=4), (4, 2, 32, 152, "shared (cooperative)")),
     ("8-bit llama3", (FP8, 8, 128, 64, 32), {}, (8, 1, 32, 152, "separate")),
     ("8-bit long_70b", (FP8, 8, 128, 8, 64), {}, (8, 1, 32, 152, "shared (cooperative)")),
