@@ -600,8 +600,8 @@ def run_ours(args, world, rank, local):
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "path": "paged_gqa_decode_host, page-locked host q / block table / lengths / "
-                        "out used in place by the kernels, one decode launch per step (and the "
-                        "run merge when planned)",
+                        "out used in place by the kernel, one launch per step (this entry keeps "
+                        "the split-run merge inside the decode kernel)",
                 "copy_path_ms_per_step": round(copy_ms, 5),
                 "copy_path": "cudaMemcpyAsync of the three inputs, paged_gqa_decode, "
                              "cudaMemcpyAsync of out"},
@@ -613,8 +613,8 @@ def run_ours(args, world, rank, local):
         line["roofline"].update({
             "cold_ms": round(cold_ms, 5), "cold_achieved": round(cold, 2),
             "cold_frac": round(cold / peak, 4),
-            "cold_note": "median of %d single launches, each after a read of a buffer "
-                         "twice the L2 size on the same stream; events around the launch alone"
+            "cold_note": "median of %d single steps, each after a read of a buffer "
+                         "twice the L2 size on the same stream; events around the step alone"
                          % args.cold_reps})
     if not args.no_cpu_baseline and world == 1:
         rate, sample, cores, _ = cpu_oracle_rate(w, args.cpu_seconds, args.cpu_threads)
