@@ -35,6 +35,16 @@ CASES = [
     ("4 query tokens, B 16", (BF16, 8, 128, 16, 32), dict(q_len=4),
      (8, 1, 16, 152, "shared (cooperative)")),
     ("mha_13b_b8", (BF16, 40, 128, 8, 40), {}, (8, 1, 16, 152, "last arriver")),
+    # the separate merge's conditions at their edges: 2 runs <= P (76 runs yes,
+    # 77 no), P <= 5 runs (31 yes, 30 no), runs x head group >= SMs (Hkv 2: 40
+    # runs x 2 no, 76 x 2 yes), at least 4 rows per head (G 2 no)
+    ("B 76", (BF16, 8, 128, 76, 32), {}, (8, 1, 16, 152, "separate")),
+    ("B 77", (BF16, 8, 128, 77, 32), {}, (8, 1, 16, 152, "last arriver")),
+    ("B 31", (BF16, 8, 128, 31, 32), {}, (8, 1, 16, 152, "separate")),
+    ("B 30", (BF16, 8, 128, 30, 32), {}, (8, 1, 16, 152, "last arriver")),
+    ("Hkv 2, B 40", (BF16, 2, 128, 40, 8), {}, (2, 1, 64, 152, "last arriver")),
+    ("Hkv 2, B 76", (BF16, 2, 128, 76, 8), {}, (2, 1, 64, 152, "separate")),
+    ("G 2, B 64", (BF16, 8, 128, 64, 16), {}, (8, 1, 16, 152, "last arriver")),
     ("4 query tokens, B 64", (BF16, 8, 128, 64, 32), dict(q_len=4), (8, 1, 16, 152, "separate")),
     ("4 query tokens, B 24", (BF16, 8, 128, 24, 32), dict(q_len=4),
      (8, 1, 16, 152, "shared (cooperative)")),
